@@ -1,0 +1,125 @@
+"""fp64 CPU oracle for the Kimi Delta Attention recurrence (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it; it
+shares no code with the CUDA path.
+
+The arithmetic lives in ``kda_oracle.c`` (a plain token-by-token loop in
+double precision, OpenMP over (sequence, head)).  This module only compiles it
+with gcc and marshals numpy arrays through ctypes.
+
+Definition followed (see the C file header for the page citations):
+``S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T``,
+rows of S are key channels, ``alpha_t = exp(log_alpha_t)``, and
+``o_t = S_t^T q_t`` from the updated state.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkda_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libkda_oracle.so`` (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Open a compiled oracle library and declare its signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    lib.oracle_kda_prefill.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P, P, i32]
+    lib.oracle_kda_prefill.restype = ctypes.c_int
+    lib.oracle_kda_decode_step.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, P, i32]
+    lib.oracle_kda_decode_step.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = [i32]
+    lib.oracle_num_threads.restype = i32
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def _f32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads(requested: int = 0) -> int:
+    return int(_load().oracle_num_threads(int(requested)))
+
+
+def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, nthreads: int = 0, lib=None):
+    """Token-loop prefill over packed sequences.
+
+    q, k, log_alpha: [T, H, dk]; v: [T, H, dv]; beta: [T, H];
+    cu_seqlens: int [N+1]; S0: [N, H, dk, dv] or None (zeros).
+    Values are taken as float32 (exact for bf16 and fp32 inputs).
+    Returns (o [T, H, dv] float64, S_final [N, H, dk, dv] float64).
+    ``lib`` selects another compiled copy of the oracle (used by the tests
+    that plant mistakes in the oracle source); default is the real one.
+    """
+    q, k, v, la, b = (_f32(x) for x in (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    assert k.shape == (T, H, dk) and la.shape == (T, H, dk)
+    assert v.shape == (T, H, dv) and b.shape == (T, H)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    s0 = None if S0 is None else _f32(S0)
+    if s0 is not None:
+        assert s0.shape == (N, H, dk, dv)
+    o = np.zeros((T, H, dv), dtype=np.float64)
+    sf = np.zeros((N, H, dk, dv), dtype=np.float64)
+    rc = (lib or _load()).oracle_kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0),
+                                    _ptr(cu), N, H, dk, dv, _ptr(o), _ptr(sf), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_kda_prefill: malformed cu_seqlens or allocation failure")
+    return o, sf
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, nthreads: int = 0, lib=None):
+    """One decode step, S (float64 [slots, H, dk, dv]) updated IN PLACE.
+
+    q, k, log_alpha: [N, H, dk]; v: [N, H, dv]; beta: [N, H].
+    Returns o [N, H, dv] float64.
+    """
+    q, k, v, la, b = (_f32(x) for x in (q, k, v, log_alpha, beta))
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    assert isinstance(S, np.ndarray) and S.dtype == np.float64 and S.flags.c_contiguous
+    slots = S.shape[0]
+    assert S.shape == (slots, H, dk, dv)
+    idx = None if state_indices is None else np.ascontiguousarray(np.asarray(state_indices, dtype=np.int32))
+    o = np.zeros((N, H, dv), dtype=np.float64)
+    rc = (lib or _load()).oracle_kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(S), slots,
+                                        _ptr(idx), N, H, dk, dv, _ptr(o), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_kda_decode_step: slot index out of range")
+    return o
