@@ -1,0 +1,152 @@
+/*
+ * kda.h -- C ABI of libkda: Kimi Delta Attention (KDA) recurrence on sm_103a.
+ *
+ * The operation (per head, state S is dk x dv, rows = key channels):
+ *
+ *   S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = S_t^T q_t                         (read from the UPDATED state)
+ *
+ * Sources: the KDA equation in "Understanding Kimi Delta Attention"
+ * (pyshine), section "The KDA Recurrence: Scalar Gate vs Channel-wise Gate";
+ * per-row (key-channel) decay and the read o_t = S_t^T q_t in "kimi delta
+ * attn from first principles" (aryagxr), section "KDA".  Page 1 of the
+ * sources reads the state with k_t instead ("Understanding the
+ * Recurrence"); this library follows the query read.
+ *
+ * Conventions shared by every entry point
+ *   - alpha_t = exp(log_alpha_t) (natural log), one gate per key channel;
+ *     beta_t is used as given (the sources give it as a sigmoid in [0, 1]).
+ *   - No scaling or normalisation of q/k inside the library: callers pass
+ *     q and k already L2-normalised per (token, head), as the sources'
+ *     "KDA Architecture" section describes.
+ *   - dk = dv = 128 only (the sources' 128 x 128 state); anything else
+ *     returns KDA_ERR_UNSUPPORTED.
+ *   - All tensors are dense, row-major, caller-owned DEVICE memory.  q, k,
+ *     v, log_alpha, o and the states are 16-byte aligned; beta, cu_seqlens,
+ *     state_indices and device_status 4-byte aligned; the prefill workspace
+ *     256-byte aligned.  The library allocates nothing, keeps no state between
+ *     calls, never synchronises the host, and enqueues all work on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).
+ *   - Argument errors are returned synchronously before anything is
+ *     enqueued.  Data-dependent errors found on the device are OR-ed into
+ *     *device_status (if non-NULL) as KDA_DEV_* bits; the affected sequences
+ *     or slots are skipped and nothing is written out of bounds.  The caller
+ *     reads *device_status after the stream completes and should zero it
+ *     before the call.
+ *   - Calls on different streams that write the same buffers race.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+typedef struct CUstream_st *kda_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, illegal overlap */
+    KDA_ERR_UNSUPPORTED = 2,   /* dk/dv other than 128, unknown dtype, device not sm_103 */
+    KDA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, ...) */
+    KDA_ERR_WORKSPACE = 4      /* workspace smaller than kda_prefill_workspace_bytes() */
+} kda_status;
+
+typedef enum {
+    KDA_DTYPE_BF16 = 0,
+    KDA_DTYPE_F32 = 1
+} kda_dtype;
+
+/* Bits OR-ed into *device_status by the kernels. */
+#define KDA_DEV_BAD_CU_SEQLENS 0x1  /* cu_seqlens not 0 .. total_tokens non-decreasing */
+#define KDA_DEV_BAD_SLOT 0x2        /* state_indices entry outside [0, num_slots) */
+#define KDA_DEV_TIMEOUT 0x4         /* an on-chip wait hit its iteration limit */
+
+/* Version of this header the library was built from. */
+KDA_API int32_t kda_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+KDA_API const char *kda_status_string(kda_status s);
+
+/*
+ * Workspace (device bytes, 256-byte aligned start) that kda_prefill needs
+ * for these arguments: the sequence schedule, plus bf16 copies of q, k, v
+ * when qkv_dtype is KDA_DTYPE_F32.  Returns 0 for invalid arguments.
+ */
+KDA_API size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t H,
+                                   int32_t dk, int32_t dv);
+
+/*
+ * kda_prefill -- chunkwise-parallel prefill over packed variable-length
+ * sequences ("Understanding Kimi Delta Attention" (pyshine), section
+ * "The Chunkwise DPLR Algorithm": fixed-size chunks, exactly equivalent to
+ * the sequential recurrence).  Chunk size 64, fp32 state, bf16 tensor-core
+ * operands with fp32 accumulation.
+ *
+ *   q, k       [total_tokens, H, dk]  qkv_dtype
+ *   v          [total_tokens, H, dv]  qkv_dtype
+ *   log_alpha  [total_tokens, H, dk]  fp32   (per key channel; see below)
+ *   beta       [total_tokens, H]      fp32
+ *   S0         [num_seqs, H, dk, dv]  fp32, or NULL for zero start states
+ *   cu_seqlens [num_seqs + 1]         int32, device; 0 = c_0 <= ... <= c_N = total_tokens
+ *   o          [total_tokens, H, dv]  qkv_dtype (out)
+ *   S_final    [num_seqs, H, dk, dv]  fp32 (out), or NULL
+ *   workspace  device scratch of >= kda_prefill_workspace_bytes(...) bytes
+ *
+ * Sequence n covers tokens [cu_seqlens[n], cu_seqlens[n+1]) and starts from
+ * S0[n] (the prefix-cache state of "Kimi Delta Attention (KDA)"
+ * (codewithdark), section "KV Caching Challenges & vLLM Contribution");
+ * S_final[n] is its state after the last token (S0[n] for an empty
+ * sequence).  S_final may alias S0 exactly; any other overlap between an
+ * output and another buffer returns KDA_ERR_INVALID_ARG.
+ *
+ * Range: the chunk factorisation takes exp(+-(g_r - g_ref)) of the
+ * cumulative log-decay within a chunk, so log_alpha must be >= -2.5 per step
+ * (documented precondition; values below it can overflow to inf/NaN).
+ * q, k, v given as fp32 are rounded to bf16 operands.
+ */
+KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                       const float *log_alpha, const float *beta, const float *S0,
+                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                       int32_t H, int32_t dk, int32_t dv, void *o, float *S_final,
+                       void *workspace, size_t workspace_bytes, int32_t *device_status,
+                       kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one fused recurrent step for N sequences
+ * ("Understanding Kimi Delta Attention" (pyshine), section "The Chunkwise
+ * DPLR Algorithm": the step-by-step "fused recurrent mode" for decode).
+ * Each head's fp32 state is read once and written once, in place.
+ *
+ *   q, k       [N, H, dk]  qkv_dtype        v [N, H, dv] qkv_dtype
+ *   log_alpha  [N, H, dk]  fp32             beta [N, H] fp32
+ *   S          [num_slots, H, dk, dv] fp32, updated in place
+ *   state_indices [N] int32 device, or NULL for slot = n.  Entries must be
+ *              unique (duplicates race); out-of-range entries set
+ *              KDA_DEV_BAD_SLOT and that sequence is skipped (its o row is
+ *              left untouched).  Slots not named are never touched.
+ *   o          [N, H, dv]  qkv_dtype (out)
+ */
+KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                           const float *log_alpha, const float *beta, float *S,
+                           int32_t num_slots, const int32_t *state_indices, int32_t N,
+                           int32_t H, int32_t dk, int32_t dv, void *o,
+                           int32_t *device_status, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

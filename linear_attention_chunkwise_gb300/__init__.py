@@ -1,0 +1,27 @@
+"""GB300-native Kimi Delta Attention: chunkwise prefill and fused decode (libkda).
+
+Python names mirror the C ABI in include/kda.h:
+  kda_prefill, kda_decode_step, kda_prefill_workspace_bytes, kda_status_string.
+The library must be built first (``__graft_entry__.build()`` or
+``python -m linear_attention_chunkwise_gb300._build``); there is no fallback.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED_SYMBOLS,
+    KDA_DEV_BAD_CU_SEQLENS,
+    KDA_DEV_BAD_SLOT,
+    KDA_DEV_TIMEOUT,
+    KDA_DTYPE_BF16,
+    KDA_DTYPE_F32,
+    KDA_ERR_CUDA,
+    KDA_ERR_INVALID_ARG,
+    KDA_ERR_UNSUPPORTED,
+    KDA_ERR_WORKSPACE,
+    KDA_OK,
+    KdaError,
+    kda_decode_step,
+    kda_prefill,
+    kda_prefill_workspace_bytes,
+    kda_status_string,
+    library_path,
+    load_library,
+)

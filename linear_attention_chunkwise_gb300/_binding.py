@@ -1,0 +1,188 @@
+"""ctypes binding of libkda (include/kda.h).  Argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of libkda.so; this
+module checks tensor dtypes/devices/shapes, allocates outputs with torch when
+the caller does not pass them, and forwards raw device pointers and the
+current CUDA stream.  There is no CPU fallback: if the library is missing or
+a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_WORKSPACE = 4
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_F32 = 1
+KDA_DEV_BAD_CU_SEQLENS = 0x1
+KDA_DEV_BAD_SLOT = 0x2
+KDA_DEV_TIMEOUT = 0x4
+
+EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill",
+                    "kda_decode_step")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: {text} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Open libkda.so and declare the C signatures.  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libkda.so is not built ({p}); run __graft_entry__.build() first")
+        lib = ctypes.CDLL(p)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.kda_abi_version.argtypes = []
+        lib.kda_abi_version.restype = i32
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
+        lib.kda_prefill_workspace_bytes.restype = sz
+        lib.kda_prefill.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P, P, sz, P, P]
+        lib.kda_prefill.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
+        lib.kda_decode_step.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def kda_status_string(status: int) -> str:
+    return load_library().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t == torch.float32:
+        return KDA_DTYPE_F32
+    raise TypeError(f"q/k/v dtype must be bfloat16 or float32, got {t}")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor | None, name: str, dtype=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def kda_prefill_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: int, dk: int = 128,
+                                dv: int = 128) -> int:
+    code = qkv_dtype if isinstance(qkv_dtype, int) else _dtype_code(qkv_dtype)
+    return int(load_library().kda_prefill_workspace_bytes(code, int(num_seqs), int(total_tokens), int(H),
+                                                          int(dk), int(dv)))
+
+
+def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, *, o=None, S_final=None, return_final=True,
+                workspace=None, device_status=None, stream=None):
+    """Chunkwise prefill over packed sequences (see include/kda.h).
+
+    q, k: [T, H, 128]; v: [T, H, 128] (bf16 or fp32); log_alpha: [T, H, 128] fp32;
+    beta: [T, H] fp32; cu_seqlens: int32 [N+1] on the device; S0: fp32 [N, H, 128, 128] or None.
+    Returns (o, S_final) -- S_final is None when return_final is False and none was given.
+    """
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    _check(k, "k", q.dtype, dev)
+    _check(v, "v", q.dtype, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _check(S0, "S0", torch.float32, dev)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, dk]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if N < 0:
+        raise ValueError("cu_seqlens must have at least one entry")
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    _check(o, "o", q.dtype, dev)
+    if S_final is None and return_final:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(S_final, "S_final", torch.float32, dev)
+    need = int(lib.kda_prefill_workspace_bytes(code, N, T, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+                         N, T, H, dk, dv, _ptr(o), _ptr(S_final), _ptr(workspace), workspace.numel(),
+                         _ptr(device_status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill", st, kda_status_string(st))
+    return o, S_final
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None, device_status=None, stream=None):
+    """One fused decode step; S [slots, H, 128, 128] fp32 is updated in place.
+
+    q, k, v: [N, H, 128] (bf16 or fp32); log_alpha: [N, H, 128] fp32; beta: [N, H] fp32;
+    state_indices: int32 [N] or None.  Returns o [N, H, 128].
+    """
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    _check(k, "k", q.dtype, dev)
+    _check(v, "v", q.dtype, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    _check(state_indices, "state_indices", torch.int32, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    _check(o, "o", q.dtype, dev)
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S), S.shape[0],
+                             _ptr(state_indices), N, H, dk, dv, _ptr(o), _ptr(device_status),
+                             _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_decode_step", st, kda_status_string(st))
+    return o

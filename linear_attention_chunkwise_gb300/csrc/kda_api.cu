@@ -1,0 +1,254 @@
+// kda_api.cu -- the extern "C" entry points of libkda: argument validation,
+// workspace carving, TMA descriptor encoding, and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kda_internal.h"
+
+namespace {
+
+using kda::kHeadDim;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+// Device must be sm_103 (the kernels are built for sm_103a only).
+kda_status check_device() {
+    static int verdict[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && verdict[dev] != 0) return verdict[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < kMaxDevices) verdict[dev] = ok ? 1 : 2;
+    return ok ? KDA_OK : KDA_ERR_UNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a [T][H][inner] tensor, box = {box_inner, 1, box_rows}.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base, uint64_t inner, uint64_t H,
+              uint64_t T, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {inner, H, T > 0 ? T : 1};
+    const cuuint64_t strides[2] = {inner * esize, H * inner * esize};
+    const cuuint32_t box[3] = {box_inner, 1, box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t esize_of(kda_dtype t) { return t == KDA_DTYPE_F32 ? 4 : 2; }
+
+bool sizes_ok(int64_t a, int64_t b, int64_t c, int64_t d) {  // product fits comfortably in int64
+    const double prod = static_cast<double>(a) * static_cast<double>(b) * static_cast<double>(c) *
+                        static_cast<double>(d);
+    return prod < 4.0e18;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                   int32_t dk, int32_t dv) {
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
+    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return 0;
+    if (!sizes_ok(total_tokens, H, dk > dv ? dk : dv, 4)) return 0;
+    size_t bytes = round_up(static_cast<size_t>(num_seqs > 0 ? num_seqs : 1) * sizeof(int32_t), kAlign);
+    if (qkv_dtype == KDA_DTYPE_F32) {
+        const size_t nk = static_cast<size_t>(total_tokens) * H * dk;
+        const size_t nv = static_cast<size_t>(total_tokens) * H * dv;
+        bytes += 2 * round_up(nk * 2, kAlign) + round_up(nv * 2, kAlign);
+    }
+    return bytes;
+}
+
+kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                       const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
+                       void* workspace, size_t workspace_bytes, int32_t* device_status, kda_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
+    if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (!sizes_ok(total_tokens, H, kHeadDim, 4) || !sizes_ok(num_seqs, H, kHeadDim, kHeadDim * 4))
+        return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
+    const bool have_tokens = total_tokens > 0;
+    if (have_tokens && (!q || !k || !v || !log_alpha || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    const size_t es = esize_of(qkv_dtype);
+    const size_t nqk = static_cast<size_t>(total_tokens) * H * kHeadDim;
+    const size_t nst = static_cast<size_t>(num_seqs) * H * kHeadDim * kHeadDim;
+    if (have_tokens && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+                        !aligned(o, 16) || !aligned(beta, 4)))
+        return KDA_ERR_INVALID_ARG;
+    if ((S0 && !aligned(S0, 16)) || (S_final && !aligned(S_final, 16)) || !aligned(workspace, kAlign) ||
+        !aligned(cu_seqlens, 4) || (device_status && !aligned(device_status, 4)))
+        return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_prefill_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
+    if (need == 0) return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+
+    // Overlap rules: outputs overlap nothing (S_final may equal S0 exactly).
+    const Range r_o = range_of(o, nqk * es), r_sf = range_of(S_final, S_final ? nst * 4 : 0);
+    const Range r_ws = range_of(workspace, need);
+    const Range inputs[] = {range_of(q, nqk * es),          range_of(k, nqk * es),
+                            range_of(v, nqk * es),          range_of(log_alpha, nqk * 4),
+                            range_of(beta, static_cast<size_t>(total_tokens) * H * 4),
+                            range_of(cu_seqlens, static_cast<size_t>(num_seqs + 1) * 4),
+                            range_of(device_status, device_status ? 4 : 0)};
+    const Range r_s0 = range_of(S0, S0 ? nst * 4 : 0);
+    for (const Range& in : inputs) {
+        if (have_tokens && overlap(r_o, in)) return KDA_ERR_INVALID_ARG;
+        if (overlap(r_sf, in) || overlap(r_ws, in)) return KDA_ERR_INVALID_ARG;
+    }
+    if (have_tokens && (overlap(r_o, r_sf) || overlap(r_o, r_ws) || overlap(r_o, r_s0))) return KDA_ERR_INVALID_ARG;
+    if (overlap(r_sf, r_ws) || overlap(r_s0, r_ws)) return KDA_ERR_INVALID_ARG;
+    if (S0 && S_final && S0 != S_final && overlap(r_sf, r_s0)) return KDA_ERR_INVALID_ARG;
+
+    const kda_status dev = check_device();
+    if (dev != KDA_OK) return dev;
+    if (!encode_fn()) return KDA_ERR_CUDA;
+
+    // Workspace: schedule, then (fp32 inputs) bf16 copies of q, k, v.
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* order = reinterpret_cast<int32_t*>(ws);
+    size_t off = round_up(static_cast<size_t>(num_seqs > 0 ? num_seqs : 1) * sizeof(int32_t), kAlign);
+    const void* qb = q;
+    const void* kb = k;
+    const void* vb = v;
+    if (qkv_dtype == KDA_DTYPE_F32 && have_tokens) {
+        void* qc = ws + off;
+        off += round_up(nqk * 2, kAlign);
+        void* kc = ws + off;
+        off += round_up(nqk * 2, kAlign);
+        void* vc = ws + off;
+        if (kda::launch_to_bf16(static_cast<const float*>(q), qc, nqk, stream) != cudaSuccess ||
+            kda::launch_to_bf16(static_cast<const float*>(k), kc, nqk, stream) != cudaSuccess ||
+            kda::launch_to_bf16(static_cast<const float*>(v), vc, nqk, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        qb = qc;
+        kb = kc;
+        vb = vc;
+    }
+    // TMA maps need a valid base even when there are no tokens (never dereferenced then).
+    const void* dummy = workspace;
+    CUtensorMap tm_q, tm_k, tm_v, tm_la;
+    const uint64_t T = static_cast<uint64_t>(total_tokens), Hh = static_cast<uint64_t>(H);
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? qb : dummy, kHeadDim, Hh, T, kHeadDim,
+                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? kb : dummy, kHeadDim, Hh, T, kHeadDim,
+                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? vb : dummy, kHeadDim, Hh, T, 64,
+                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_tokens ? static_cast<const void*>(log_alpha) : dummy,
+                  kHeadDim, Hh, T, kHeadDim, kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return KDA_ERR_CUDA;
+
+    if (kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    kda::PrefillArgs a;
+    a.beta = beta;
+    a.S0 = S0;
+    a.cu_seqlens = cu_seqlens;
+    a.order = order;
+    a.o = o;
+    a.S_final = S_final;
+    a.device_status = device_status;
+    a.total_tokens = total_tokens;
+    a.num_seqs = num_seqs;
+    a.H = H;
+    if (kda::launch_prefill(tm_q, tm_k, tm_v, tm_la, a, qkv_dtype == KDA_DTYPE_F32, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
+                           int32_t H, int32_t dk, int32_t dv, void* o, int32_t* device_status,
+                           kda_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (!sizes_ok(num_slots, H, kHeadDim, kHeadDim * 4) || !sizes_ok(N, H, kHeadDim, 4))
+        return KDA_ERR_INVALID_ARG;
+    if (static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
+    if (!state_indices && num_slots < N) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) || !aligned(o, 16) ||
+        !aligned(S, 16) || !aligned(beta, 4) || (state_indices && !aligned(state_indices, 4)) ||
+        (device_status && !aligned(device_status, 4)))
+        return KDA_ERR_INVALID_ARG;
+    const size_t es = esize_of(qkv_dtype);
+    const size_t nio = static_cast<size_t>(N) * H * kHeadDim;
+    const Range r_o = range_of(o, nio * es);
+    const Range r_s = range_of(S, static_cast<size_t>(num_slots) * H * kHeadDim * kHeadDim * 4);
+    const Range inputs[] = {range_of(q, nio * es),
+                            range_of(k, nio * es),
+                            range_of(v, nio * es),
+                            range_of(log_alpha, nio * 4),
+                            range_of(beta, static_cast<size_t>(N) * H * 4),
+                            range_of(state_indices, state_indices ? static_cast<size_t>(N) * 4 : 0),
+                            range_of(device_status, device_status ? 4 : 0)};
+    for (const Range& in : inputs)
+        if (overlap(r_o, in) || overlap(r_s, in)) return KDA_ERR_INVALID_ARG;
+    if (overlap(r_o, r_s)) return KDA_ERR_INVALID_ARG;
+
+    const kda_status dev = check_device();
+    if (dev != KDA_OK) return dev;
+    if (kda::launch_decode(qkv_dtype == KDA_DTYPE_F32, q, k, v, log_alpha, beta, S, num_slots, state_indices, N, H,
+                           o, device_status, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// kda_decode.cu -- fused single-token KDA update ("fused recurrent mode").
+//
+// One CTA per (sequence, head).  The head's 128 x 128 fp32 state is streamed
+// through registers exactly once: 256 threads, thread (warp w, lane l) holds
+// rows 16w..16w+15, columns 4l..4l+3 (one float4 per row, so every warp reads
+// and writes whole 512-byte rows).  The update is evaluated in the factorised
+// form that needs a single pass over the state:
+//   S' = Diag(alpha) S                         (rows = key channels)
+//   y  = S'^T k,  p = S'^T q                   (column sums over the 128 rows)
+//   u  = beta (v - y)
+//   S_new = S' + k u^T                         (= (I - beta k k^T) S' + beta k v^T)
+//   o  = S_new^T q = p + (k . q) u
+// which is the KDA equation of "Understanding Kimi Delta Attention"
+// (pyshine), "The KDA Recurrence: Scalar Gate vs Channel-wise Gate",
+// rewritten with the erase-then-write delta form of "kimi delta attn from
+// first principles" (aryagxr), section "KDA", step 2.
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 16
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <typename IoT>
+__global__ void __launch_bounds__(kThreads, 2)
+    kda_decode_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k, const IoT* __restrict__ v,
+                      const float* __restrict__ log_alpha, const float* __restrict__ beta, float* S,
+                      int32_t num_slots, const int32_t* __restrict__ state_indices, int32_t H,
+                      IoT* __restrict__ o, int32_t* device_status) {
+    const int unit = blockIdx.x;
+    const int n = unit / H;
+    const int h = unit - n * H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int32_t slot = state_indices ? state_indices[n] : n;
+    if (slot < 0 || slot >= num_slots) {
+        if (tid == 0 && device_status) atomicOr(device_status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+
+    __shared__ float a_s[kHeadDim], k_s[kHeadDim], q_s[kHeadDim];
+    __shared__ __align__(16) float u_s[kHeadDim];
+    __shared__ __align__(16) float red_y[kThreads / 32][kHeadDim];
+    __shared__ __align__(16) float red_p[kThreads / 32][kHeadDim];
+    __shared__ float kq_part[4];
+
+    float* Sg = S + (static_cast<size_t>(slot) * H + h) * kHeadDim * kHeadDim;
+    const int row0 = warp * kRowsPerWarp;
+
+    // Issue the whole 64 KB state read up front (16 independent float4 per thread).
+    float4 s[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+        s[i] = __ldcs(reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row0 + i) * kHeadDim) + lane);
+
+    const size_t tok = static_cast<size_t>(n) * H + h;
+    if (tid < kHeadDim) {
+        const float kk = to_f32(k[tok * kHeadDim + tid]);
+        const float qq = to_f32(q[tok * kHeadDim + tid]);
+        k_s[tid] = kk;
+        q_s[tid] = qq;
+        a_s[tid] = expf(log_alpha[tok * kHeadDim + tid]);
+        float kq = kk * qq;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        if (lane == 0) kq_part[warp] = kq;
+    }
+    __syncthreads();
+
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = row0 + i;
+        const float a = a_s[r], kr = k_s[r], qr = q_s[r];
+        s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+        y.x = fmaf(kr, s[i].x, y.x); y.y = fmaf(kr, s[i].y, y.y);
+        y.z = fmaf(kr, s[i].z, y.z); y.w = fmaf(kr, s[i].w, y.w);
+        p.x = fmaf(qr, s[i].x, p.x); p.y = fmaf(qr, s[i].y, p.y);
+        p.z = fmaf(qr, s[i].z, p.z); p.w = fmaf(qr, s[i].w, p.w);
+    }
+    reinterpret_cast<float4*>(red_y[warp])[lane] = y;
+    reinterpret_cast<float4*>(red_p[warp])[lane] = p;
+    __syncthreads();
+
+    if (tid < kHeadDim) {
+        float yy = 0.f, pp = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            yy += red_y[w][tid];
+            pp += red_p[w][tid];
+        }
+        const float b = beta[tok];
+        const float u = b * (to_f32(v[tok * kHeadDim + tid]) - yy);
+        const float kq = kq_part[0] + kq_part[1] + kq_part[2] + kq_part[3];
+        u_s[tid] = u;
+        o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
+    }
+    __syncthreads();
+
+    const float4 uu = reinterpret_cast<const float4*>(u_s)[lane];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const float kr = k_s[row0 + i];
+        float4 t = s[i];
+        t.x = fmaf(kr, uu.x, t.x); t.y = fmaf(kr, uu.y, t.y);
+        t.z = fmaf(kr, uu.z, t.z); t.w = fmaf(kr, uu.w, t.w);
+        __stcs(reinterpret_cast<float4*>(Sg + static_cast<size_t>(row0 + i) * kHeadDim) + lane, t);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
+                          const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
+                          int32_t N, int32_t H, void* o, int32_t* device_status, cudaStream_t stream) {
+    const long long units = static_cast<long long>(N) * H;
+    if (units == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(units));
+    if (f32_io) {
+        kda_decode_kernel<float><<<grid, kThreads, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), log_alpha,
+            beta, S, num_slots, state_indices, H, static_cast<float*>(o), device_status);
+    } else {
+        kda_decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+            static_cast<const __nv_bfloat16*>(v), log_alpha, beta, S, num_slots, state_indices, H,
+            static_cast<__nv_bfloat16*>(o), device_status);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,115 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments synchronously (no kernel runs)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_chunkwise_gb300 as kda
+from linear_attention_chunkwise_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kda.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]*?\b(kda_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_symbols() == sorted(kda.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kda_abi_version() == 1
+    assert kda.kda_status_string(kda.KDA_OK) == "KDA_OK"
+    assert kda.kda_status_string(kda.KDA_ERR_WORKSPACE) == "KDA_ERR_WORKSPACE"
+    assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256
+    f32 = kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2)
+    assert f32 == 256 + 3 * 256 * 2 * 128 * 2
+    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
+    assert kda.kda_prefill_workspace_bytes(7, 1, 10, 2) == 0
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+BASE = 1 << 40  # fake, never dereferenced: validation fails before any CUDA call
+
+
+def _prefill(lib, **over):
+    T, H, N = 128, 2, 1
+    tok = T * H * 128
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, o=BASE + 12 * tok, Sf=BASE + 14 * tok,
+             ws=BASE + 20 * tok, wsb=1 << 20, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]), P(a["S0"]),
+                           P(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"], P(a["o"]), P(a["Sf"]), P(a["ws"]),
+                           a["wsb"], P(a["status"]), None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dv=256), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dtype=5), kda.KDA_ERR_UNSUPPORTED),
+    (dict(q=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(q=BASE + 8), kda.KDA_ERR_INVALID_ARG),                 # misaligned
+    (dict(ws=BASE + 20 * 128 * 2 * 128 + 16), kda.KDA_ERR_INVALID_ARG),  # workspace not 256-aligned
+    (dict(wsb=16), kda.KDA_ERR_WORKSPACE),
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(o=BASE + 2 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),  # o overlaps k
+    (dict(Sf=BASE + 12 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),  # S_final overlaps o
+    (dict(S0=BASE + 30 * 128 * 2 * 128, Sf=BASE + 30 * 128 * 2 * 128 + 4096), kda.KDA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_arguments(lib, over, expect):
+    assert _prefill(lib, **over) == expect
+
+
+def _decode(lib, **over):
+    N, H = 4, 2
+    io = N * H * 128
+    a = dict(q=BASE, k=BASE + 2 * io, v=BASE + 4 * io, dtype=0, la=BASE + 6 * io, beta=BASE + 10 * io,
+             S=BASE + (1 << 30), slots=N, idx=None, N=N, H=H, dk=128, dv=128, o=BASE + 12 * io, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_decode_step(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]), P(a["S"]),
+                               a["slots"], P(a["idx"]), a["N"], a["H"], a["dk"], a["dv"], P(a["o"]), P(a["status"]),
+                               None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(S=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(slots=2), kda.KDA_ERR_INVALID_ARG),                    # identity slots need num_slots >= N
+    (dict(o=BASE + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(o=BASE + (1 << 30) + 64), kda.KDA_ERR_INVALID_ARG),    # o inside S
+    (dict(N=0), kda.KDA_OK),                                      # nothing to do
+])
+def test_decode_rejects_bad_arguments(lib, over, expect):
+    assert _decode(lib, **over) == expect
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        kda.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,87 @@
+"""GPU parity of kda_decode_step (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import linear_attention_chunkwise_gb300 as kda
+from linear_attention_chunkwise_gb300 import synth
+from tests.conftest import cuda_ok
+from tests.gpu_util import TOL, host, rell2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("permute", [False, True])
+def test_decode_small_parity(dtype, permute):
+    N, H, steps = 6, 3, 4
+    slots = 9 if permute else N
+    d = synth.decode_inputs(N, H, steps, dtype=dtype, seed=31, device="cuda", num_slots=slots,
+                            permute_slots=permute)
+    S_ref = host(d.S).astype(np.float64)
+    S_before = d.S.clone()
+    idx = None if d.state_indices is None else d.state_indices.cpu().numpy()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(steps):
+        o = kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], d.S, d.state_indices,
+                                device_status=status)
+        o_ref = oracle.kda_decode_step(host(d.q[t]), host(d.k[t]), host(d.v[t]), host(d.log_alpha[t]),
+                                       host(d.beta[t]), S_ref, idx)
+        torch.cuda.synchronize()
+        assert rell2(host(o), o_ref) < TOL
+        # the state path is fp32 end to end: much tighter than the bf16 budget
+        assert rell2(host(d.S), S_ref) < 1e-5
+    assert int(status.item()) == 0
+    if permute:
+        named = set(idx.tolist())
+        for s in range(slots):
+            if s not in named:
+                assert torch.equal(d.S[s], S_before[s]), "unnamed slot was touched"
+
+
+def test_decode_bad_slot_is_reported_and_skipped():
+    N, H = 4, 2
+    d = synth.decode_inputs(N, H, 1, seed=5, device="cuda", num_slots=6, permute_slots=True)
+    idx = torch.tensor([0, 7, 2, -1], dtype=torch.int32, device="cuda")
+    S_before = d.S.clone()
+    o = torch.full((N, H, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_decode_step(d.q[0], d.k[0], d.v[0], d.log_alpha[0], d.beta[0], d.S, idx, o=o, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kda.KDA_DEV_BAD_SLOT
+    assert torch.all(o[1] == 3.0) and torch.all(o[3] == 3.0)     # skipped rows untouched
+    for s in (1, 3, 4, 5):
+        assert torch.equal(d.S[s], S_before[s])
+    assert not torch.equal(d.S[0], S_before[0])
+
+
+def test_decode_config3_graph_sampled():
+    """256 sequences x 32 heads, 100 steps captured in one CUDA graph (the bench's launch
+    configuration); o of every step and the final state checked on sampled (seq, head) units."""
+    c = synth.CONFIGS[3]
+    d = synth.config_inputs(3, device="cuda")
+    N, H, steps = c["N"], c["H"], c["steps"]
+    g = torch.Generator().manual_seed(99)
+    units = [(int(n), int(h)) for n, h in zip(torch.randint(0, N, (48,), generator=g),
+                                              torch.randint(0, H, (48,), generator=g))]
+    units = sorted(set(units))
+    S0 = {u: host(d.S[u[0], u[1]]).astype(np.float64) for u in units}
+    o_all = torch.empty((steps, N, H, 128), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        for t in range(steps):
+            kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], d.S, None, o=o_all[t])
+    graph.replay()
+    torch.cuda.synchronize()
+    for (n, h) in units:
+        S = S0[(n, h)][None, None].copy()
+        o_ref = np.zeros((steps, 128))
+        for t in range(steps):
+            sl = lambda x: host(x[t, n:n + 1, h:h + 1])
+            o_ref[t] = oracle.kda_decode_step(sl(d.q), sl(d.k), sl(d.v), sl(d.log_alpha),
+                                              host(d.beta[t, n:n + 1, h:h + 1]), S)[0, 0]
+        assert rell2(host(o_all[:, n, h]), o_ref) < TOL
+        assert rell2(host(d.S[n, h]), S[0, 0]) < 1e-4
