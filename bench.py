@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA hot path on GB300: chunkwise prefill + fused decode.
+
+One step = one kda_prefill call on the 8k workload (B=1, H=32, T=8192,
+d=128, bf16 q/k/v, fp32 gates, fp32 state, S0 = 0).  `value` is prefill
+throughput in Mtok/s (sequence positions, all 32 heads) with inputs resident
+in HBM; the inputs (404 MB per step) are larger than L2, so no flush is
+needed between steps.  The same JSON line carries the decode workload
+(256 sequences x 32 heads, 100 consecutive steps in one CUDA graph) as
+state GB/s under "decode".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same per-GPU workload on its own GPU (the
+(sequence, head) units are independent: weak scaling, no collective on the
+data path); the step time is the max over ranks.  `--impl reference` times
+the fp64 CPU oracle on the host cores instead (bounded token samples).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PREFILL_CFG = 1
+DECODE_CFG = 3
+H, D = 32, 128
+# algorithmic bytes / flops per token-head (q, k, v bf16 + log_alpha fp32 + beta fp32 + o bf16)
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2          # 1540
+PREFILL_FLOPS_PER_TOKEN_HEAD = 10 * 64 * D + 6 * D * D                  # 180,224 (full 64x64 tiles)
+STATE_BYTES = D * D * 4                                                 # 65,536
+DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + PREFILL_BYTES_PER_TOKEN_HEAD  # 132,612
+METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s & % HBM (H=32, d=128)"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return dict(hbm=float(pk["hbm_gbs"]), bf16=float(pk["bf16_tflops"]),
+                    bf16_sustained=float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "linear_attention_chunkwise_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash(src_files):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """SM clocks, power and clock-event (throttle) reasons sampled DURING a timed
+    region: NVML through ctypes every ~2 ms (short regions still get samples),
+    falling back to `nvidia-smi -lms 200`.  Read-only: no setting is changed."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []      # (sm_mhz, max_mhz, reasons_mask, power_w)
+        self._stop = threading.Event()
+        self._t = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+
+    def _init_nvml(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvml handle")
+        self._nvml, self._handle = lib, h
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._reasons_fn = fn
+
+    def _poll_nvml(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self._reasons_fn(h, ctypes.byref(rs))
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            if ok:
+                self.samples.append((float(clk.value), float(mx.value), int(rs.value), pw.value / 1000.0))
+            time.sleep(0.002)
+
+    def _poll_smi(self):
+        fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.draw")
+        self._smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                                      "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for line in self._smi.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                mask = sum(b for b, v in zip(bits, parts[2:6]) if v.lower() == "active")
+                self.samples.append((float(parts[0]), float(parts[1]), mask, float(parts[6])))
+            except (ValueError, IndexError):
+                continue
+
+    def __enter__(self):
+        try:
+            self._init_nvml()
+            target = self._poll_nvml
+            self.source = "nvml"
+        except Exception:
+            target = self._poll_smi
+            self.source = "nvidia-smi"
+        self._t = threading.Thread(target=target, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._smi is not None:
+            self._smi.terminate()
+        if self._t is not None:
+            self._t.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [x[0] for x in self.samples]
+        mask = 0
+        for x in self.samples:
+            mask |= x[2]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(x[1] for x in self.samples),
+                "reasons": sorted(v for b, v in self.REASONS.items() if mask & b),
+                "power_w_max": round(max(x[3] for x in self.samples), 1),
+                "samples": len(sm), "source": self.source}
+
+
+# ----------------------------------------------------------------- ours ----
+
+class Ctx:
+    """Process/device context shared by the two measurements."""
+
+    def __init__(self):
+        import torch
+        import torch.distributed as dist
+        self.torch, self.dist = torch, dist
+        self.ws, self.rank, local = dist_env()
+        if self.ws > 1:
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            torch.cuda.set_device(0)
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        self.stream = torch.cuda.current_stream()
+        self.peaks = load_peaks()
+
+    def barrier(self):
+        if self.ws > 1:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def max_over_ranks(self, x: float) -> float:
+        if self.ws == 1:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64, device=self.dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def events(self):
+        E = self.torch.cuda.Event
+        return E(enable_timing=True), E(enable_timing=True)
+
+
+def bench_prefill(cx: Ctx, args):
+    """Prefill on the 8k workload: device-resident timing, then end to end from pinned host memory."""
+    torch = cx.torch
+    import linear_attention_chunkwise_gb300 as kda
+    from linear_attention_chunkwise_gb300 import synth
+
+    c = synth.CONFIGS[PREFILL_CFG]
+    p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
+                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+    T = p.total_tokens
+    o = torch.empty_like(p.q)
+    sf = torch.empty((1, H, D, D), dtype=torch.float32, device=cx.dev)
+    wsb = kda.kda_prefill_workspace_bytes(torch.bfloat16, 1, T, H)
+    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=cx.dev)
+
+    def step():
+        kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, o=o, S_final=sf,
+                        workspace=work, stream=cx.stream)
+
+    for _ in range(args.warmup):
+        step()
+    cx.barrier()
+    ev0, ev1 = cx.events()
+    with ClockSampler(cx.dev) as clk:
+        ev0.record(cx.stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(cx.stream)
+        cx.barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = cx.max_over_ranks(ms_local)
+    tokens_per_step = T * cx.ws
+    bytes_per_launch = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES  # + S_final write
+    flops_per_launch = T * H * PREFILL_FLOPS_PER_TOKEN_HEAD
+    achieved_gbs = bytes_per_launch / (ms_local * 1e-3) / 1e9
+    achieved_tf = flops_per_launch / (ms_local * 1e-3) / 1e12
+
+    # end to end through the same C-ABI call: pinned host inputs in, o and S_final out, every step
+    names = ("q", "k", "v", "log_alpha", "beta", "cu_seqlens")
+    host = {n: getattr(p, n).cpu().pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(getattr(p, n)) for n in names}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    sf_host = torch.empty(sf.shape, dtype=sf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + sf_host.numel() * sf_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        kda.kda_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["log_alpha"], dev_in["beta"],
+                        dev_in["cu_seqlens"], None, o=o, S_final=sf, workspace=work, stream=cx.stream)
+        o_host.copy_(o, non_blocking=True)
+        sf_host.copy_(sf, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    cx.barrier()
+    ev0.record(cx.stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev1.record(cx.stream)
+    cx.barrier()
+    e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    pk = cx.peaks
+    return {
+        "value": tokens_per_step / (ms * 1e-3) / 1e6,
+        "ms": ms,
+        "launches": 2 * args.steps,  # schedule + prefill kernel per call
+        "tokens": T,
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved_gbs / pk["hbm"], 4),
+                     "traffic": ncu_traffic("kda_prefill_kernel", ["kda_prefill.cu", "kda_ptx.cuh"]),
+                     "kernel": "kda_prefill_kernel", "peak_source": pk["src"] + " burst copy",
+                     "bytes_per_launch": bytes_per_launch},
+        "tensor": {"achieved": round(achieved_tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                   "frac": round(achieved_tf / pk["bf16"], 4), "flops_per_launch": flops_per_launch,
+                   "peak_source": pk["src"] + " bf16 burst"},
+        "e2e": {"value": round(tokens_per_step / (e2e_ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+    }
+
+
+def bench_decode(cx: Ctx, args):
+    """Decode: 256 x 32 heads, 100 consecutive steps captured in one CUDA graph."""
+    torch = cx.torch
+    import linear_attention_chunkwise_gb300 as kda
+    from linear_attention_chunkwise_gb300 import synth
+
+    dc = synth.CONFIGS[DECODE_CFG]
+    d = synth.decode_inputs(dc["N"], dc["H"], dc["steps"], D, dc["dtype"], dc["lo"], dc["s_std"],
+                            synth.config_seed(DECODE_CFG) + 1000 * cx.rank, cx.dev)
+    n_units = dc["N"] * dc["H"]
+    steps = dc["steps"]
+    od = torch.empty((steps, dc["N"], dc["H"], D), dtype=torch.bfloat16, device=cx.dev)
+    gstream = torch.cuda.Stream(device=cx.dev)
+    kda.kda_decode_step(d.q[0], d.k[0], d.v[0], d.log_alpha[0], d.beta[0], d.S, None, o=od[0])  # load + warm
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
+        for t in range(steps):
+            kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], d.S, None, o=od[t])
+    reps = max(1, args.decode_reps)
+    for _ in range(max(1, args.warmup)):
+        graph.replay()
+    cx.barrier()
+    ev0, ev1 = cx.events()
+    # CUDAGraph.replay() launches on the current stream: time it there
+    with ClockSampler(cx.dev) as clk:
+        ev0.record(cx.stream)
+        for _ in range(reps):
+            graph.replay()
+        ev1.record(cx.stream)
+        cx.barrier()
+    ms_local = ev0.elapsed_time(ev1) / (reps * steps)
+    ms = cx.max_over_ranks(ms_local)
+    state_gbs = cx.ws * n_units * 2 * STATE_BYTES / (ms * 1e-3) / 1e9
+    achieved = n_units * DECODE_BYTES_PER_UNIT / (ms_local * 1e-3) / 1e9
+
+    # end to end: each step's inputs H2D from pinned memory and its o D2H; the states stay in HBM
+    names = ("q", "k", "v", "log_alpha", "beta")
+    hq = [getattr(d, n)[0].cpu().pin_memory() for n in names]
+    dq = [getattr(d, n)[0].clone() for n in names]
+    oh = torch.empty(od[0].shape, dtype=od.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hq)
+    d2h = oh.numel() * oh.element_size()
+
+    def e2e_step():
+        for a_, b_ in zip(dq, hq):
+            a_.copy_(b_, non_blocking=True)
+        kda.kda_decode_step(dq[0], dq[1], dq[2], dq[3], dq[4], d.S, None, o=od[0], stream=cx.stream)
+        oh.copy_(od[0], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    cx.barrier()
+    n_e2e = 100
+    ev0.record(cx.stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    ev1.record(cx.stream)
+    cx.barrier()
+    e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / n_e2e)
+    pk = cx.peaks
+    return {
+        "workload": "KDA decode step, 256 sequences x 32 heads, d=128, bf16 q/k/v, fp32 states (512 MiB) "
+                    "updated in place, 100 consecutive steps in one CUDA graph",
+        "value": round(state_gbs, 1), "unit": "state GB/s", "us_per_step": round(ms * 1e3, 2),
+        "gpu_launches": reps * steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4),
+                     "traffic": ncu_traffic("kda_decode_kernel", ["kda_decode.cu"]),
+                     "kernel": "kda_decode_kernel", "peak_source": pk["src"] + " burst copy",
+                     "bytes_per_launch": n_units * DECODE_BYTES_PER_UNIT},
+        "e2e": {"value": round(cx.ws * n_units * 2 * STATE_BYTES / (e2e_ms * 1e-3) / 1e9, 1),
+                "unit": "state GB/s", "us_per_step": round(e2e_ms * 1e3, 2),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+    }
+
+
+def run_ours(args):
+    from linear_attention_chunkwise_gb300 import _build
+    _build.build()
+    cx = Ctx()
+    pf = bench_prefill(cx, args) if args.only in ("all", "prefill") else None
+    dc = bench_decode(cx, args) if args.only in ("all", "decode") else None
+    out = {"metric": METRIC}
+    if pf is not None:
+        out.update({
+            "value": round(pf["value"], 3), "unit": "Mtok/s", "n_gpus": cx.ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(pf["ms"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta sigmoid(N(0,1)), "
+                    "log_alpha U[-0.2,0])",
+            "config": {"workload": "KDA chunkwise prefill B=1 H=32 T=8192 dk=dv=128, bf16 q/k/v, "
+                                   "fp32 gates and state, S0=0, chunk 64",
+                       "tokens_per_step_per_gpu": pf["tokens"], "heads": H,
+                       "l2": "inputs larger than L2 (404 MB read per step), no flush",
+                       "parallelism": f"independent problem per GPU x{cx.ws}"},
+            "roofline": pf["roofline"], "tensor": pf["tensor"], "e2e": pf["e2e"],
+            "gpu_launches": pf["launches"], "clocks": pf["clocks"],
+        })
+    if dc is not None:
+        out["decode"] = dc
+    if cx.rank == 0 and not args.no_cpu_baseline and pf is not None:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if cx.rank == 0:
+        print(json.dumps(out), flush=True)
+    if cx.ws > 1:
+        cx.dist.barrier()
+        cx.dist.destroy_process_group()
+
+
+# ------------------------------------------------------- oracle timing ----
+
+def _oracle_inputs(tokens: int, seed: int):
+    """The 8k prefill workload's inputs (or its first `tokens` tokens), generated on the CPU."""
+    from linear_attention_chunkwise_gb300 import synth
+    c = synth.CONFIGS[PREFILL_CFG]
+    pi = synth.prefill_inputs([tokens], c["H"], D, c["dtype"], c["lo"], None, seed, "cpu")
+    f = lambda t: t.float().numpy()
+    return f(pi.q), f(pi.k), f(pi.v), f(pi.log_alpha), f(pi.beta), [0, tokens]
+
+
+def _time_oracle_runs(target_seconds: float, max_steps: int | None = None):
+    """Time the oracle on the 8k workload: whole-workload passes repeated to fill
+    about target_seconds, or a token prefix when one pass would take longer."""
+    import oracle
+    oracle.build()
+    T = synth_tokens()
+    q, k, v, la, b, _ = _oracle_inputs(T, seed=5)
+    oracle.kda_prefill(q[:16], k[:16], v[:16], la[:16], b[:16], [0, 16], None)   # load, touch
+    t0 = time.perf_counter()
+    oracle.kda_prefill(q[:256], k[:256], v[:256], la[:256], b[:256], [0, 256], None)
+    per_token = (time.perf_counter() - t0) / 256
+    tokens = int(min(T, max(64, target_seconds / max(per_token, 1e-9))))
+    reps = max(1, int(round(target_seconds / max(per_token * tokens, 1e-9))))
+    if max_steps is not None:
+        reps = max(1, min(reps, max_steps))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.kda_prefill(q[:tokens], k[:tokens], v[:tokens], la[:tokens], b[:tokens], [0, tokens], None)
+        times.append(time.perf_counter() - t0)
+    return tokens, times, oracle.num_threads(0)
+
+
+def synth_tokens() -> int:
+    from linear_attention_chunkwise_gb300 import synth
+    return int(synth.CONFIGS[PREFILL_CFG]["lengths"][0])
+
+
+def cpu_baseline(target_seconds: float):
+    tokens, times, cores = _time_oracle_runs(target_seconds)
+    total = sum(times)
+    return {"value": round(len(times) * tokens / total / 1e6, 6), "unit": "Mtok/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{len(times)} pass(es) over {tokens} of the 8192 tokens x 32 heads of the 8k prefill "
+                      f"workload, fp64 token loop, {total:.1f} s wall"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    # warm-up: one short untimed oracle call is made inside _time_oracle_runs
+    tokens, times, cores = _time_oracle_runs(args.cpu_seconds / max(1, args.steps), max_steps=1)
+    step_times = times
+    for _ in range(args.steps - 1):
+        step_times += _time_oracle_runs_fixed(tokens)
+    s = sum(step_times) / len(step_times)
+    value = tokens / s / 1e6
+    out = {
+        "metric": METRIC, "value": round(value, 6), "unit": "Mtok/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(s * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "KDA chunkwise prefill B=1 H=32 T=8192 dk=dv=128, bf16 q/k/v, fp32 gates and state, "
+                               "S0=0, chunk 64", "sample_tokens_per_step": tokens, "heads": H},
+        "cpu_baseline": {"value": round(value, 6), "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tokens} of the 8192 tokens x 32 heads per step, fp64 token loop"},
+        "e2e": {"value": round(value, 6), "unit": "Mtok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def _time_oracle_runs_fixed(tokens: int):
+    import oracle
+    q, k, v, la, b, _ = _oracle_inputs(tokens, seed=5)
+    t0 = time.perf_counter()
+    oracle.kda_prefill(q, k, v, la, b, [0, tokens], None)
+    return [time.perf_counter() - t0]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-reps", type=int, default=5, help="replays of the 100-step decode graph")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling aid: run only one workload (the JSON line then lacks the other)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
