@@ -145,6 +145,37 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                            int32_t H, int32_t dk, int32_t dv, void *o,
                            int32_t *device_status, kda_stream_t stream);
 
+/*
+ * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device
+ * memory.  The sources have no counterpart to this entry point; it exists for
+ * integration.  Some callers cannot hand the library a workspace: a plugin
+ * that an inference engine gives only the tensors it owns, after the engine
+ * has reserved all of HBM for its caches, or a latency-critical path where
+ * cudaMalloc's implicit device synchronisation is not allowed.
+ *
+ * Same arguments and results as kda_prefill, minus the workspace.  Its
+ * scratch (the sequence schedule) lives in a fixed array in device global
+ * memory inside libkda: KDA_NOALLOC_MAX_SEQS int32 (256 KiB), held on every
+ * GPU that loads the library until the process exits.  It allocates nothing
+ * and calls no allocating routine.
+ *   - num_seqs > KDA_NOALLOC_MAX_SEQS returns KDA_ERR_WORKSPACE; fp32 q/k/v
+ *     (which need token-sized scratch) return KDA_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (each call rewrites the part it reads before reading it).  Calls whose
+ *     work overlaps on the GPU -- on different streams, or from different
+ *     threads -- race on it: serialise them.
+ */
+#define KDA_NOALLOC_MAX_SEQS 65536
+
+KDA_API kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                       const float *log_alpha, const float *beta, const float *S0,
+                                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                       int32_t H, int32_t dk, int32_t dv, void *o, float *S_final,
+                                       int32_t *device_status, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
 
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill",
-                    "kda_decode_step")
+                    "kda_decode_step", "kda_prefill_noalloc")
 
 _lock = threading.Lock()
 _lib = None
