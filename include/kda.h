@@ -80,13 +80,26 @@ KDA_API int32_t kda_abi_version(void);
 KDA_API const char *kda_status_string(kda_status s);
 
 /*
- * Workspace (device bytes, 256-byte aligned start) that kda_prefill needs
- * for these arguments: the sequence schedule, plus bf16 copies of q, k, v
- * when qkv_dtype is KDA_DTYPE_F32.  Returns 0 for invalid arguments.
+ * Workspace (device bytes, 256-byte aligned start) for kda_prefill's
+ * two-pass path (the fast one): the sequence schedule, the chunk table, bf16
+ * copies of q, k, v when qkv_dtype is KDA_DTYPE_F32, and 67,072 bytes per
+ * (chunk, head) of prepared operands, counting ceil(total_tokens/64) +
+ * num_seqs chunks -- about 1.05 KB per token and head.  Returns 0 for
+ * invalid arguments.
  */
 KDA_API size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
                                    int64_t total_tokens, int32_t H,
                                    int32_t dk, int32_t dv);
+
+/*
+ * Smallest workspace kda_prefill accepts: the schedule (+ bf16 copies for
+ * fp32 inputs).  With less than kda_prefill_workspace_bytes() it runs the
+ * single-pass path, one CTA per (sequence, head), which is slower for few
+ * long sequences.  Returns 0 for invalid arguments.
+ */
+KDA_API size_t kda_prefill_min_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
+                                       int64_t total_tokens, int32_t H,
+                                       int32_t dk, int32_t dv);
 
 /*
  * kda_prefill -- chunkwise-parallel prefill over packed variable-length
@@ -103,14 +116,22 @@ KDA_API size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs
  *   cu_seqlens [num_seqs + 1]         int32, device; 0 = c_0 <= ... <= c_N = total_tokens
  *   o          [total_tokens, H, dv]  qkv_dtype (out)
  *   S_final    [num_seqs, H, dk, dv]  fp32 (out), or NULL
- *   workspace  device scratch of >= kda_prefill_workspace_bytes(...) bytes
+ *   workspace  device scratch: >= kda_prefill_workspace_bytes(...) bytes
+ *              selects the two-pass path (chunk preparation for all
+ *              (chunk, head) pairs in parallel, then a scan over chunks per
+ *              (sequence, head, 64-column slice of dv)); >=
+ *              kda_prefill_min_workspace_bytes(...) selects the single-pass
+ *              path; less returns KDA_ERR_WORKSPACE.  Both paths compute the
+ *              same chunk algebra.
  *
  * Sequence n covers tokens [cu_seqlens[n], cu_seqlens[n+1]) and starts from
  * S0[n] (the prefix-cache state of "Kimi Delta Attention (KDA)"
  * (codewithdark), section "KV Caching Challenges & vLLM Contribution");
  * S_final[n] is its state after the last token (S0[n] for an empty
  * sequence).  S_final may alias S0 exactly; any other overlap between an
- * output and another buffer returns KDA_ERR_INVALID_ARG.
+ * output and another buffer returns KDA_ERR_INVALID_ARG.  A malformed
+ * cu_seqlens sets KDA_DEV_BAD_CU_SEQLENS; the single-pass path then skips the
+ * sequences whose bounds are invalid, the two-pass path writes nothing.
  *
  * Range: the chunk factorisation takes exp(+-(g_r - g_ref)) of the
  * cumulative log-decay within a chunk, so log_alpha must be >= -2.5 per step
@@ -154,10 +175,12 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
  * cudaMalloc's implicit device synchronisation is not allowed.
  *
  * Same arguments and results as kda_prefill, minus the workspace.  Its
- * scratch (the sequence schedule) lives in a fixed array in device global
- * memory inside libkda: KDA_NOALLOC_MAX_SEQS int32 (256 KiB), held on every
- * GPU that loads the library until the process exits.  It allocates nothing
- * and calls no allocating routine.
+ * scratch lives in a fixed array in device global memory inside libkda:
+ * KDA_NOALLOC_MAX_SEQS int32 (256 KiB), held on every GPU that loads the
+ * library until the process exits.  That is passed to kda_prefill as its
+ * workspace, so the single-pass path runs (the two-pass path only for inputs
+ * small enough to fit).  It allocates nothing and calls no allocating
+ * routine.
  *   - num_seqs > KDA_NOALLOC_MAX_SEQS returns KDA_ERR_WORKSPACE; fp32 q/k/v
  *     (which need token-sized scratch) return KDA_ERR_UNSUPPORTED.
  *   - The first call on each device looks up the array's device address

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     KdaError,
     kda_decode_step,
     kda_prefill,
+    kda_prefill_min_workspace_bytes,
     kda_prefill_workspace_bytes,
     kda_status_string,
     library_path,

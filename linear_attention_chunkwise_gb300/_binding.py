@@ -27,8 +27,8 @@ KDA_DEV_BAD_CU_SEQLENS = 0x1
 KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
 
-EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes", "kda_prefill",
-                    "kda_decode_step", "kda_prefill_noalloc")
+EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
+                    "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_prefill_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,8 @@ def load_library(path: str | None = None):
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_prefill_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
         lib.kda_prefill_workspace_bytes.restype = sz
+        lib.kda_prefill_min_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
+        lib.kda_prefill_min_workspace_bytes.restype = sz
         lib.kda_prefill.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P, P, sz, P, P]
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
@@ -114,13 +116,22 @@ def kda_prefill_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: 
                                                           int(dk), int(dv)))
 
 
+def kda_prefill_min_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: int, dk: int = 128,
+                                    dv: int = 128) -> int:
+    code = qkv_dtype if isinstance(qkv_dtype, int) else _dtype_code(qkv_dtype)
+    return int(load_library().kda_prefill_min_workspace_bytes(code, int(num_seqs), int(total_tokens), int(H),
+                                                              int(dk), int(dv)))
+
+
 def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, *, o=None, S_final=None, return_final=True,
-                workspace=None, device_status=None, stream=None):
+                workspace=None, device_status=None, stream=None, path="two_pass"):
     """Chunkwise prefill over packed sequences (see include/kda.h).
 
     q, k: [T, H, 128]; v: [T, H, 128] (bf16 or fp32); log_alpha: [T, H, 128] fp32;
     beta: [T, H] fp32; cu_seqlens: int32 [N+1] on the device; S0: fp32 [N, H, 128, 128] or None.
-    Returns (o, S_final) -- S_final is None when return_final is False and none was given.
+    path: "two_pass" or "single_pass" -- sizes the workspace allocated here (the library picks
+    the path from the workspace size).  Returns (o, S_final) -- S_final is None when
+    return_final is False and none was given.
     """
     lib = load_library()
     dev = q.device
@@ -145,7 +156,10 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, *, o=None, S_fina
     if S_final is None and return_final:
         S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     _check(S_final, "S_final", torch.float32, dev)
-    need = int(lib.kda_prefill_workspace_bytes(code, N, T, H, dk, dv))
+    if path not in ("two_pass", "single_pass"):
+        raise ValueError(f"unknown prefill path {path!r}")
+    query = lib.kda_prefill_workspace_bytes if path == "two_pass" else lib.kda_prefill_min_workspace_bytes
+    need = int(query(code, N, T, H, dk, dv))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", torch.uint8, dev)

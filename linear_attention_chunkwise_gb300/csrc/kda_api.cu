@@ -73,10 +73,44 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* 
 
 size_t esize_of(kda_dtype t) { return t == KDA_DTYPE_F32 ? 4 : 2; }
 
+// Workspace layouts.  Two-pass path: [schedule][chunk table][bf16 q,k,v if
+// fp32 inputs][per-(chunk, head) operand images].  Single-pass path:
+// [schedule][bf16 q,k,v if fp32 inputs].
+struct WsLayout {
+    size_t table = 0, copies = 0, blobs = 0, total = 0;
+};
+size_t copies_bytes(kda_dtype t, int64_t T, int32_t H) {
+    if (t != KDA_DTYPE_F32) return 0;
+    const size_t n = static_cast<size_t>(T) * H * kHeadDim;
+    return 3 * round_up(n * 2, kAlign);
+}
+int64_t max_chunks(int32_t N, int64_t T) { return (T + kda::kChunk - 1) / kda::kChunk + N; }
+WsLayout split_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
+    WsLayout w;
+    w.table = round_up(static_cast<size_t>(N > 0 ? N : 1) * 4, kAlign);
+    w.copies = w.table + round_up(static_cast<size_t>(N + 2) * 4, kAlign);
+    w.blobs = w.copies + copies_bytes(t, T, H);
+    w.total = w.blobs + static_cast<size_t>(max_chunks(N, T)) * H * kda::kPrefillBlobBytes;
+    return w;
+}
+WsLayout fused_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
+    WsLayout w;
+    w.copies = round_up(static_cast<size_t>(N > 0 ? N : 1) * 4, kAlign);
+    w.total = w.copies + copies_bytes(t, T, H);
+    return w;
+}
+bool ws_args_ok(kda_dtype t, int32_t N, int64_t T, int32_t H, int32_t dk, int32_t dv);
+
 bool sizes_ok(int64_t a, int64_t b, int64_t c, int64_t d) {  // product fits comfortably in int64
     const double prod = static_cast<double>(a) * static_cast<double>(b) * static_cast<double>(c) *
                         static_cast<double>(d);
     return prod < 4.0e18;
+}
+
+bool ws_args_ok(kda_dtype t, int32_t N, int64_t T, int32_t H, int32_t dk, int32_t dv) {
+    if (N < 0 || T < 0 || H <= 0 || dk != kHeadDim || dv != kHeadDim) return false;
+    if (t != KDA_DTYPE_BF16 && t != KDA_DTYPE_F32) return false;
+    return sizes_ok(T + N + 1, H, kda::kPrefillBlobBytes, 1) && sizes_ok(T, H, kHeadDim, 4);
 }
 
 }  // namespace
@@ -98,16 +132,14 @@ const char* kda_status_string(kda_status s) {
 
 size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens, int32_t H,
                                    int32_t dk, int32_t dv) {
-    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
-    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return 0;
-    if (!sizes_ok(total_tokens, H, dk > dv ? dk : dv, 4)) return 0;
-    size_t bytes = round_up(static_cast<size_t>(num_seqs > 0 ? num_seqs : 1) * sizeof(int32_t), kAlign);
-    if (qkv_dtype == KDA_DTYPE_F32) {
-        const size_t nk = static_cast<size_t>(total_tokens) * H * dk;
-        const size_t nv = static_cast<size_t>(total_tokens) * H * dv;
-        bytes += 2 * round_up(nk * 2, kAlign) + round_up(nv * 2, kAlign);
-    }
-    return bytes;
+    if (!ws_args_ok(qkv_dtype, num_seqs, total_tokens, H, dk, dv)) return 0;
+    return split_layout(qkv_dtype, num_seqs, total_tokens, H).total;
+}
+
+size_t kda_prefill_min_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                       int32_t dk, int32_t dv) {
+    if (!ws_args_ok(qkv_dtype, num_seqs, total_tokens, H, dk, dv)) return 0;
+    return fused_layout(qkv_dtype, num_seqs, total_tokens, H).total;
 }
 
 kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
@@ -132,9 +164,15 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     if ((S0 && !aligned(S0, 16)) || (S_final && !aligned(S_final, 16)) || !aligned(workspace, kAlign) ||
         !aligned(cu_seqlens, 4) || (device_status && !aligned(device_status, 4)))
         return KDA_ERR_INVALID_ARG;
-    const size_t need = kda_prefill_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
-    if (need == 0) return KDA_ERR_INVALID_ARG;
-    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    // Path by workspace size: the two-pass path when the workspace holds the
+    // per-(chunk, head) operand images, else the single-pass path.
+    if (kda_prefill_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv) == 0) return KDA_ERR_INVALID_ARG;
+    const WsLayout two = split_layout(qkv_dtype, num_seqs, total_tokens, H);
+    const WsLayout one = fused_layout(qkv_dtype, num_seqs, total_tokens, H);
+    const bool two_pass = workspace_bytes >= two.total;
+    if (!two_pass && workspace_bytes < one.total) return KDA_ERR_WORKSPACE;
+    const WsLayout& lay = two_pass ? two : one;
+    const size_t need = lay.total;
 
     // Overlap rules: outputs overlap nothing (S_final may equal S0 exactly).
     const Range r_o = range_of(o, nqk * es), r_sf = range_of(S_final, S_final ? nst * 4 : 0);
@@ -157,10 +195,9 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     if (dev != KDA_OK) return dev;
     if (!encode_fn()) return KDA_ERR_CUDA;
 
-    // Workspace: schedule, then (fp32 inputs) bf16 copies of q, k, v.
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int32_t* order = reinterpret_cast<int32_t*>(ws);
-    size_t off = round_up(static_cast<size_t>(num_seqs > 0 ? num_seqs : 1) * sizeof(int32_t), kAlign);
+    size_t off = lay.copies;
     const void* qb = q;
     const void* kb = k;
     const void* vb = v;
@@ -182,10 +219,11 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     const void* dummy = workspace;
     CUtensorMap tm_q, tm_k, tm_v, tm_la;
     const uint64_t T = static_cast<uint64_t>(total_tokens), Hh = static_cast<uint64_t>(H);
-    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? qb : dummy, kHeadDim, Hh, T, kHeadDim,
-                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? kb : dummy, kHeadDim, Hh, T, kHeadDim,
-                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    // q, k, v: 64-channel boxes in the 128B-swizzled layout the tensor cores read
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? qb : dummy, kHeadDim, Hh, T, 64,
+                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? kb : dummy, kHeadDim, Hh, T, 64,
+                  kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, have_tokens ? vb : dummy, kHeadDim, Hh, T, 64,
                   kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_tokens ? static_cast<const void*>(log_alpha) : dummy,
@@ -199,14 +237,24 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     a.S0 = S0;
     a.cu_seqlens = cu_seqlens;
     a.order = order;
+    a.chunk_off = two_pass ? reinterpret_cast<const int32_t*>(ws + two.table) : nullptr;
+    a.blobs = two_pass ? ws + two.blobs : nullptr;
     a.o = o;
     a.S_final = S_final;
     a.device_status = device_status;
     a.total_tokens = total_tokens;
     a.num_seqs = num_seqs;
     a.H = H;
-    if (kda::launch_prefill(tm_q, tm_k, tm_v, tm_la, a, qkv_dtype == KDA_DTYPE_F32, stream) != cudaSuccess)
+    const bool out_f32 = qkv_dtype == KDA_DTYPE_F32;
+    if (two_pass) {
+        if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, reinterpret_cast<int32_t*>(ws + two.table),
+                                    device_status, stream) != cudaSuccess ||
+            kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, a, max_chunks(num_seqs, total_tokens), out_f32,
+                                      stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    } else if (kda::launch_prefill_fused(tm_q, tm_k, tm_v, tm_la, a, out_f32, stream) != cudaSuccess) {
         return KDA_ERR_CUDA;
+    }
     return KDA_OK;
 }
 

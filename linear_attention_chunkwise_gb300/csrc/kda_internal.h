@@ -23,7 +23,9 @@ struct PrefillArgs {
     const float* beta;
     const float* S0;
     const int32_t* cu_seqlens;
-    const int32_t* order;     // schedule: longest sequences first (workspace)
+    const int32_t* order;      // schedule: longest sequences first (workspace)
+    const int32_t* chunk_off;  // two-pass path: chunk offsets [N + 2] (workspace)
+    uint8_t* blobs;            // two-pass path: per (chunk, head) operand images (workspace)
     void* o;
     float* S_final;
     int32_t* device_status;
@@ -32,6 +34,10 @@ struct PrefillArgs {
     int32_t H;
 };
 
+// Bytes per (chunk, head) of the two-pass path's operand images:
+// [-W; Qh] 32 KB | Kb 16 KB | Tb 8 KB | M 8 KB | exp(gm), exp(gC), exp(gC-gm) 1.5 KB.
+constexpr size_t kPrefillBlobBytes = 67072;
+
 // Sequence schedule (longest first) + cu_seqlens validation.
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* order,
                             int32_t* device_status, cudaStream_t stream);
@@ -39,8 +45,17 @@ cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t num_seqs, int64_t
 // fp32 -> bf16 copy (for fp32 q/k/v inputs).
 cudaError_t launch_to_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
 
-// The chunkwise prefill kernel; q/k/v/log_alpha are read through TMA maps.
-cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                           const CUtensorMap& tm_la, const PrefillArgs& a, bool out_f32, cudaStream_t stream);
+// Single-pass chunkwise prefill (one CTA per (sequence, head)); needs only
+// the schedule as scratch.  q/k/v/log_alpha are read through TMA maps.
+cudaError_t launch_prefill_fused(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_la, const PrefillArgs& a, bool out_f32, cudaStream_t stream);
+
+// Two-pass chunkwise prefill: chunk table, then per-(chunk, head) prep into
+// the workspace, then the per-(sequence, head, dv slice) scan.
+cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
+                               int32_t* device_status, cudaStream_t stream);
+cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
+                                 cudaStream_t stream);
 
 }  // namespace kda

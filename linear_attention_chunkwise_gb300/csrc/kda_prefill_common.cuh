@@ -1,0 +1,256 @@
+// kda_prefill_common.cuh -- device code shared by the prefill kernels: the
+// per-chunk gate phase, the triangular inverse, TMEM/packing helpers.
+//
+// Chunk algebra (derived from the KDA equation of "Understanding Kimi Delta
+// Attention" (pyshine), section "The KDA Recurrence", and o_t = S_t^T q_t of
+// "kimi delta attn from first principles" (aryagxr), section "KDA"), per chunk
+// of C = 64 rows with start state S (dk x dv, rows = key channels):
+//   g   = inclusive cumsum of log_alpha over the chunk rows (per channel)
+//   gm  = g at row 31 (reference row), gC = g at row 63
+//   Kh  = k*exp(g-gm),  Qh = q*exp(g-gm),  Kb = k*exp(gm-g)            (bf16)
+//   A   = Kh Kb^T (strictly lower part),  M = lower(Qh Kb^T) (incl. diagonal)
+//   T   = (I + Diag(beta) A)^-1,  Tb = T Diag(beta)
+//   W   = Tb Kh,  U0 = Tb V,  Sm = Diag(exp(gm)) S
+//   U   = U0 - W Sm,  O = Qh Sm + M U
+//   S  <- Diag(exp(gC)) S + Diag(exp(gC-gm)) Kb^T U
+// Rows past the sequence end are masked to k = q = v = 0, beta = 0,
+// log_alpha = 0, which makes them exact no-ops.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kda_internal.h"
+#include "kda_ptx.cuh"
+
+namespace kda {
+namespace pf {
+
+constexpr int C = kChunk;    // 64
+constexpr int D = kHeadDim;  // 128
+constexpr int NT = 256;      // threads per CTA
+constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clock
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t tmem_lane(int quarter) { return static_cast<uint32_t>(32 * quarter) << 16; }
+
+// 2^x with the hardware approximation (relative error ~2^-22); exp(y) is
+// evaluated as 2^(y log2 e).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// fp32 [64][64] scratch with the float4 column index xor-swizzled by the row
+// (conflict-free row-per-thread and column-per-thread accesses).
+__device__ __forceinline__ float4& m4(float* M, int r, int c4) {
+    return *reinterpret_cast<float4*>(M + r * 64 + (((c4 ^ r) & 15) << 2));
+}
+__device__ __forceinline__ float& m1(float* M, int r, int c) {
+    return M[r * 64 + ((((c >> 2) ^ r) & 15) << 2) + (c & 3)];
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    uint4 pk;
+    pk.x = pack_bf16(v[0], v[1]);
+    pk.y = pack_bf16(v[2], v[3]);
+    pk.z = pack_bf16(v[4], v[5]);
+    pk.w = pack_bf16(v[6], v[7]);
+    return pk;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_out8(OutT* dst, const float* v);
+template <>
+__device__ __forceinline__ void store_out8<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+    *reinterpret_cast<uint4*>(dst) = pack8(v);
+}
+template <>
+__device__ __forceinline__ void store_out8<float>(float* dst, const float* v) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+__device__ __forceinline__ float4 fma4(float s, const float4& a, const float4& acc) {
+    return make_float4(fmaf(s, a.x, acc.x), fmaf(s, a.y, acc.y), fmaf(s, a.z, acc.z), fmaf(s, a.w, acc.w));
+}
+
+// Gate phase of one chunk (all NT threads; one __syncthreads inside).
+//   la_s : [64][128] f32 log_alpha of the chunk (plain rows)
+//   opa  : operand tile [2 blk][128 rows][128 B]; rows 0..63 hold k and rows
+//          64..127 hold q on entry (128B-swizzled bf16), Kh and Qh on exit
+//   opkb : [2 blk][64 rows][128 B], receives Kb
+//   Lc   : valid rows of the chunk; red: f32 [4][128] scratch
+//   beta_s[64] receives beta (masked) from beta_cur of threads 0..63
+//   egm/egc/egcm[128] receive exp(gm), exp(gC), exp(gC - gm) per channel
+__device__ __forceinline__ void gate_chunk(const float* la_s, uint8_t* opa, uint8_t* opkb, int Lc, float* red,
+                                           float* beta_s, float beta_cur, float* egm, float* egc, float* egcm,
+                                           int tid) {
+    const int cp = tid & 63;  // channel pair (2cp, 2cp+1)
+    const int rq = tid >> 6;  // rows 16rq .. 16rq+15
+    float g0[16], g1[16];
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * rq + i;
+        float2 l2 = make_float2(0.f, 0.f);
+        if (r < Lc) l2 = *reinterpret_cast<const float2*>(la_s + r * D + 2 * cp);
+        acc0 += l2.x;
+        acc1 += l2.y;
+        g0[i] = acc0;
+        g1[i] = acc1;
+    }
+    reinterpret_cast<float2*>(red + rq * D)[cp] = make_float2(acc0, acc1);
+    if (tid < C) beta_s[tid] = (tid < Lc) ? beta_cur : 0.f;
+    __syncthreads();
+    float2 part[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) part[qq] = reinterpret_cast<const float2*>(red + qq * D)[cp];
+    float off0 = 0.f, off1 = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq)
+        if (qq < rq) { off0 += part[qq].x; off1 += part[qq].y; }
+    const float gm0 = part[0].x + part[1].x, gm1 = part[0].y + part[1].y;
+    const float gC0 = gm0 + part[2].x + part[3].x, gC1 = gm1 + part[2].y + part[3].y;
+    if (rq == 0) {
+        egm[2 * cp] = expf(gm0); egm[2 * cp + 1] = expf(gm1);
+        egc[2 * cp] = expf(gC0); egc[2 * cp + 1] = expf(gC1);
+        egcm[2 * cp] = expf(gC0 - gm0); egcm[2 * cp + 1] = expf(gC1 - gm1);
+    }
+    const float c0 = (off0 - gm0) * kLog2e, c1 = (off1 - gm1) * kLog2e;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * rq + i;
+        const float x0 = fmaf(g0[i], kLog2e, c0), x1 = fmaf(g1[i], kLog2e, c1);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        const float f0 = ex2_approx(-x0), f1 = ex2_approx(-x1);
+        const uint32_t koff = sw128_off(r, 2 * cp, 16384);
+        const uint32_t qoff = sw128_off(64 + r, 2 * cp, 16384);
+        float2 kk = make_float2(0.f, 0.f), qv = kk;
+        if (r < Lc) {
+            kk = unpack_bf16(*reinterpret_cast<const uint32_t*>(opa + koff));
+            qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(opa + qoff));
+        }
+        *reinterpret_cast<uint32_t*>(opa + koff) = pack_bf16(kk.x * e0, kk.y * e1);
+        *reinterpret_cast<uint32_t*>(opa + qoff) = pack_bf16(qv.x * e0, qv.y * e1);
+        *reinterpret_cast<uint32_t*>(opkb + sw128_off(r, 2 * cp, 8192)) = pack_bf16(kk.x * f0, kk.y * f1);
+    }
+}
+
+// Write N = Diag(beta) strict_lower(A) for row r (32 columns starting at
+// 32*hw) from a 32-column TMEM read into the fp32 scratch.
+__device__ __forceinline__ void store_n_row(float* Nf, int r, int hw, float br, const float* a) {
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+        const int i0 = 32 * hw + 4 * j4;
+        m4(Nf, r, 8 * hw + j4) =
+            make_float4(i0 + 0 < r ? br * a[4 * j4 + 0] : 0.f, i0 + 1 < r ? br * a[4 * j4 + 1] : 0.f,
+                        i0 + 2 < r ? br * a[4 * j4 + 2] : 0.f, i0 + 3 < r ? br * a[4 * j4 + 3] : 0.f);
+    }
+}
+
+// M row rr: lower(Qh Kb^T) entries i <= rr of 32 columns starting at 32*hw,
+// as bf16 into a 128B-swizzled row (chunks 4hw..4hw+3).
+__device__ __forceinline__ void store_m_row(uint8_t* tile, int row, int rr, int hw, const float* a) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = (32 * hw + 8 * ch + e <= rr) ? a[8 * ch + e] : 0.f;
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, 4 * hw + ch)) = pack8(m8);
+    }
+}
+
+// Tb = T Diag(beta) (lower incl. diagonal) -> bf16 rows 0..63 of a swizzled tile.
+__device__ __forceinline__ void store_tb(uint8_t* tile, float* Tf, const float* beta_s, int tid) {
+    const int r = tid >> 2, c0 = 16 * (tid & 3);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float m8[8];
+#pragma unroll
+        for (int e4 = 0; e4 < 2; ++e4) {
+            const int i0 = c0 + 8 * hf + 4 * e4;
+            const float4 tv = m4(Tf, r, i0 >> 2);
+            const float4 bv = *reinterpret_cast<const float4*>(beta_s + i0);
+            m8[4 * e4 + 0] = i0 + 0 <= r ? tv.x * bv.x : 0.f;
+            m8[4 * e4 + 1] = i0 + 1 <= r ? tv.y * bv.y : 0.f;
+            m8[4 * e4 + 2] = i0 + 2 <= r ? tv.z * bv.z : 0.f;
+            m8[4 * e4 + 3] = i0 + 3 <= r ? tv.w * bv.w : 0.f;
+        }
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(r, (c0 >> 3) + hf)) = pack8(m8);
+    }
+}
+
+// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
+// diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
+// for block distance d = R - I = 1, 2, 3.  All NT threads; ends synchronised.
+__device__ __forceinline__ void lower_inverse(float* Nf, float* Tf, float* Xs, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < 4 && lane < 16) {
+        const int B = warp, j = lane;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int row = 16 * B + r;
+            float nv[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                if (4 * q4 < r) {
+                    const float4 v = m4(Nf, row, 4 * B + q4);
+                    nv[4 * q4] = v.x; nv[4 * q4 + 1] = v.y; nv[4 * q4 + 2] = v.z; nv[4 * q4 + 3] = v.w;
+                }
+            }
+            float s0 = (r == j) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i + 1 < r; i += 2) {
+                s0 = fmaf(-nv[i], t[i], s0);
+                s1 = fmaf(-nv[i + 1], t[i + 1], s1);
+            }
+            if (r & 1) s0 = fmaf(-nv[r - 1], t[r - 1], s0);
+            t[r] = s0 + s1;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) m1(Tf, 16 * B + r, 16 * B + j) = t[r];
+    }
+    __syncthreads();
+    const int I = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
+#pragma unroll 1
+    for (int d = 1; d <= 3; ++d) {
+        const bool act = I < 4 - d;
+        const int R = I + d;
+        if (act) {
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+            for (int J = I; J < R; ++J) {
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const float4 nv = m4(Nf, 16 * R + r, 4 * J + mm);
+                    acc0 = fma4(nv.x, m4(Tf, 16 * J + 4 * mm + 0, 4 * I + cq), acc0);
+                    acc1 = fma4(nv.y, m4(Tf, 16 * J + 4 * mm + 1, 4 * I + cq), acc1);
+                    acc0 = fma4(nv.z, m4(Tf, 16 * J + 4 * mm + 2, 4 * I + cq), acc0);
+                    acc1 = fma4(nv.w, m4(Tf, 16 * J + 4 * mm + 3, 4 * I + cq), acc1);
+                }
+            }
+            reinterpret_cast<float4*>(Xs)[(I * 16 + r) * 4 + cq] =
+                make_float4(acc0.x + acc1.x, acc0.y + acc1.y, acc0.z + acc1.z, acc0.w + acc1.w);
+        }
+        __syncthreads();
+        if (act) {
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+            const float4* X4 = reinterpret_cast<const float4*>(Xs);
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float4 tv = m4(Tf, 16 * R + r, 4 * R + mm);
+                acc0 = fma4(tv.x, X4[(I * 16 + 4 * mm + 0) * 4 + cq], acc0);
+                acc1 = fma4(tv.y, X4[(I * 16 + 4 * mm + 1) * 4 + cq], acc1);
+                acc0 = fma4(tv.z, X4[(I * 16 + 4 * mm + 2) * 4 + cq], acc0);
+                acc1 = fma4(tv.w, X4[(I * 16 + 4 * mm + 3) * 4 + cq], acc1);
+            }
+            m4(Tf, 16 * R + r, 4 * I + cq) = make_float4(-(acc0.x + acc1.x), -(acc0.y + acc1.y),
+                                                         -(acc0.z + acc1.z), -(acc0.w + acc1.w));
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace pf
+}  // namespace kda

@@ -1,0 +1,536 @@
+// kda_prefill_split.cu -- two-pass chunkwise KDA prefill (tcgen05 + TMEM + TMA).
+//
+// Same chunk algebra as kda_prefill_common.cuh (derived from the KDA equation
+// of "Understanding Kimi Delta Attention" (pyshine), "The KDA Recurrence", and
+// the chunkwise form of its "The Chunkwise DPLR Algorithm" section), split so
+// that the work that does NOT depend on the state runs fully in parallel:
+//
+//   pass 0  chunk table: chunk offsets of every sequence (from cu_seqlens).
+//   pass 1  chunk prep, one CTA per (chunk, head), two CTAs per SM: gates,
+//           Kh/Qh/Kb, MMA [Kh;Qh] Kb^T, the triangular inverse, Tb, M and
+//           MMA W = Tb Kh.  It writes the scan's operands to the workspace as
+//           ready-to-copy images of the swizzled shared-memory tiles:
+//             [-W; Qh] (32 KB) | Kb (16 KB) | Tb (8 KB) | M (8 KB) |
+//             exp(gm), exp(gC), exp(gC-gm) (3 x 512 B)
+//   pass 2  scan, one CTA per (sequence, head, 64-column slice of dv): the
+//           sequential chain only.  Per chunk it bulk-copies the images (one
+//           chunk ahead, double-buffered), TMA-loads its slice of v, and runs
+//             X  = [Tb; 0] V + [-W; Qh] Sm      (= [U; Qh Sm])
+//             D_S = Kb^T U,  X += [0; M] U      (= [U; O])
+//             S <- Diag(exp(gC)) S + Diag(exp(gC-gm)) D_S
+//           with the fp32 state slice in registers.
+// Every on-chip wait is bounded; on expiry KDA_DEV_TIMEOUT is set and the
+// CTA winds down instead of hanging.
+#include <cuda_bf16.h>
+
+#include "kda_prefill_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace pf;
+
+constexpr uint32_t kBlobA = 0;          // [-W; Qh]
+constexpr uint32_t kBlobKb = 32768;     // Kb
+constexpr uint32_t kBlobTb = 49152;     // Tb (rows 0..63 of [Tb; M])
+constexpr uint32_t kBlobM = 57344;      // M
+constexpr uint32_t kBlobEv = 65536;     // exp(gm) | exp(gC) | exp(gC - gm), f32 [3][128]
+static_assert(kBlobEv + 1536 == kPrefillBlobBytes, "blob layout");
+
+// ---- bulk copies (non-tensor), 16-byte aligned, sizes multiple of 16 ----
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// =========================================================== pass 0 ======
+// chunk_off[n] = number of 64-token chunks in sequences 0..n-1, chunk_off[N]
+// = total; chunk_off[N+1] = 1 when cu_seqlens is well formed (0 = c_0 <= ...
+// <= c_N = total_tokens), else 0 and every offset 0 (nothing is computed).
+__global__ void __launch_bounds__(1024) kda_chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N,
+                                                               int64_t total, int32_t* chunk_off,
+                                                               int32_t* device_status) {
+    __shared__ int s_bad;
+    __shared__ long long s_warp[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_bad = (cu[0] != 0 || static_cast<int64_t>(cu[N]) != total) ? 1 : 0;
+    __syncthreads();
+    const int per = (N + 1023) / 1024;
+    const int i0 = min(N, tid * per), i1 = min(N, i0 + per);
+    long long local = 0;
+    bool bad = false;
+    for (int n = i0; n < i1; ++n) {
+        const int64_t a = cu[n], b = cu[n + 1];
+        if (a < 0 || b < a || b > total) bad = true;
+        else local += (b - a + C - 1) / C;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    // block-wide exclusive scan of `local`
+    long long incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += y;
+        }
+        s_warp[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+    const bool ok = s_bad == 0;
+    for (int n = i0; n < i1; ++n) {
+        chunk_off[n] = ok ? static_cast<int32_t>(run) : 0;
+        if (ok) run += (static_cast<int64_t>(cu[n + 1]) - cu[n] + C - 1) / C;
+    }
+    if (tid == 1023) {
+        chunk_off[N] = ok ? static_cast<int32_t>(s_warp[31]) : 0;
+        chunk_off[N + 1] = ok ? 1 : 0;
+    }
+    if (tid == 0 && !ok && device_status) atomicOr(device_status, KDA_DEV_BAD_CU_SEQLENS);
+}
+
+// =========================================================== pass 1 ======
+struct PrepSmem {
+    static constexpr uint32_t OP_A = 0;          // [2 blk][128 rows][128 B]: [k;q] -> [Kh;Qh] -> [-W;Qh]
+    static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb
+    static constexpr uint32_t OP_A3 = 49152;     // [Tb (64 rows) | M (64 rows)] x 128 B
+    static constexpr uint32_t LA = 65536;        // [64][128] f32 log_alpha; then the inverse scratch
+    static constexpr uint32_t INV_N = LA;        // f32 [64][64]
+    static constexpr uint32_t INV_T = LA + 16384;
+    static constexpr uint32_t XS = LA + 32768;   // f32 [3][16][16]
+    static constexpr uint32_t BETA = XS + 3072;  // f32 [64]
+    static constexpr uint32_t RED = BETA + 256;  // f32 [4][128]
+    static constexpr uint32_t EV = RED + 2048;   // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
+    static constexpr uint32_t BARS = EV + 1536;  // 3 x u64
+    static constexpr uint32_t TMEM_SLOT = BARS + 24;
+    static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
+    static constexpr uint32_t ALLOC = TOTAL + 1024;
+};
+static_assert(2 * (PrepSmem::ALLOC + 1024) <= 233472, "two prep CTAs must fit on one SM");
+
+__global__ void __launch_bounds__(NT, 2)
+    kda_chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_la, const PrefillArgs p) {
+    using L = PrepSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qw = warp & 3, hw = warp >> 2;
+    const int H = p.H, N = p.num_seqs;
+    const int32_t* co = p.chunk_off;
+    const int j = blockIdx.x / H;
+    const int h = blockIdx.x - j * H;
+    if (co[N + 1] == 0 || j >= co[N]) return;
+    int lo = 0, hi = N - 1;  // the sequence owning chunk j: largest n with co[n] <= j
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (co[mid] <= j) lo = mid;
+        else hi = mid - 1;
+    }
+    const int seq = lo;
+    const int64_t t0 = static_cast<int64_t>(p.cu_seqlens[seq]) + static_cast<int64_t>(j - co[seq]) * C;
+    const int64_t rem = p.cu_seqlens[seq + 1] - t0;
+    const int Lc = static_cast<int>(rem < C ? rem : C);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);  // 0: log_alpha, 1: q/k, 2: mma
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
+    float* ev = reinterpret_cast<float*>(sm + L::EV);
+    float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bars[0], C * D * 4);
+        tma_load_3d(sm + L::LA, &tm_la, &bars[0], 0, h, static_cast<int32_t>(t0));
+        mbar_arrive_expect_tx(&bars[1], 4 * 8192);
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+            tma_load_3d(sm + L::OP_A + kh * 16384, &tm_k, &bars[1], 64 * kh, h, static_cast<int32_t>(t0));
+            tma_load_3d(sm + L::OP_A + kh * 16384 + 8192, &tm_q, &bars[1], 64 * kh, h, static_cast<int32_t>(t0));
+        }
+    }
+    const float beta_cur = (tid < Lc) ? p.beta[(t0 + tid) * H + h] : 0.f;
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tq = tmem + tmem_lane(qw);
+    bool ok = mbar_wait(&bars[0], 0, kWaitLimit);
+    ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
+
+    gate_chunk(reinterpret_cast<const float*>(sm + L::LA), sm + L::OP_A, sm + L::OP_KB, Lc,
+               reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev, ev + 128, ev + 256, tid);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    const uint32_t a_base = smem_u32(sm + L::OP_A), kb_base = smem_u32(sm + L::OP_KB);
+    const uint32_t a3_base = smem_u32(sm + L::OP_A3);
+    if (tid == 0) {  // D = [Kh; Qh] Kb^T  (128 x 64)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            mma_bf16(tmem, sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                     sdesc_sw128(kb_base + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), id, s > 0);
+        mma_commit(&bars[2]);
+    }
+    ok = mbar_wait(&bars[2], 0, kWaitLimit) && ok;
+    tc_fence_after();
+    float* Nf = reinterpret_cast<float*>(sm + L::INV_N);
+    float* Tf = reinterpret_cast<float*>(sm + L::INV_T);
+    {
+        float a[32];
+        tmem_ld32(tq + 32 * hw, a);
+        tmem_ld_wait();
+        if (qw < 2) {
+            const int r = 32 * qw + lane;
+            store_n_row(Nf, r, hw, beta_s[r], a);
+        } else {
+            const int rr = 32 * (qw - 2) + lane;
+            store_m_row(sm + L::OP_A3, 64 + rr, rr, hw, a);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    lower_inverse(Nf, Tf, reinterpret_cast<float*>(sm + L::XS), tid);
+    store_tb(sm + L::OP_A3, Tf, beta_s, tid);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // [W; M Kh] = [Tb; M] Kh
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem, sdesc_sw128(a3_base + s * 32, 16, 1024), sdesc_sw128(a_base + s * 2048, 16384, 1024), id,
+                     s > 0);
+        mma_commit(&bars[2]);
+    }
+    ok = mbar_wait(&bars[2], 1, kWaitLimit) && ok;
+    tc_fence_after();
+    if (qw < 2) {  // -W -> rows 0..63 of OP_A
+        const int r = 32 * qw + lane;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float a[32];
+            tmem_ld32(tq + 64 * hw + 32 * part, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = -a[e];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4*>(sm + L::OP_A + hw * 16384 + sw128_chunk(r, 4 * part + ch)) = pack8(a + 8 * ch);
+        }
+    }
+    if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        uint8_t* blob = p.blobs + (static_cast<size_t>(j) * H + h) * kPrefillBlobBytes;
+        bulk_s2g(blob + kBlobA, sm + L::OP_A, 32768);
+        bulk_s2g(blob + kBlobKb, sm + L::OP_KB, 16384);
+        bulk_s2g(blob + kBlobTb, sm + L::OP_A3, 16384);  // Tb and M, adjacent in both layouts
+        bulk_s2g(blob + kBlobEv, sm + L::EV, 1536);
+        bulk_commit();
+        bulk_wait_all();
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// =========================================================== pass 2 ======
+constexpr int NV = 64;  // dv columns per scan CTA
+
+struct ScanSmem {
+    // one operand set per chunk parity
+    static constexpr uint32_t SET = 83968;       // 82 KB
+    static constexpr uint32_t S_A = 0;           // [2 blk][128 rows][128 B]: [-W; Qh]
+    static constexpr uint32_t S_KB = 32768;      // [2 blk][64 rows][128 B]: Kb
+    static constexpr uint32_t S_A3 = 49152;      // [Tb | zeros | M] x 64 rows x 128 B
+    static constexpr uint32_t S_V = 73728;       // [64 rows][128 B]: v slice (TMA, swizzled)
+    static constexpr uint32_t S_EV = 81920;      // f32 [3][128]
+    static constexpr uint32_t OP_SM = 2 * SET;   // [128 rows][128 B]: Sm slice
+    static constexpr uint32_t OP_U = OP_SM + 16384;  // [64 rows][128 B]: U slice
+    static constexpr uint32_t BARS = OP_U + 8192;    // 5 x u64: load0, load1, c1, c2, fin
+    static constexpr uint32_t TMEM_SLOT = BARS + 40;
+    static constexpr uint32_t ABORT = TMEM_SLOT + 4;
+    static constexpr uint32_t TOTAL = ABORT + 4;
+    static constexpr uint32_t ALLOC = TOTAL + 1024;
+};
+static_assert(ScanSmem::ALLOC <= 232448, "scan shared memory over the per-CTA limit");
+constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
+
+template <typename OutT>
+__global__ void __launch_bounds__(NT, 1)
+    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
+    using L = ScanSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qw = warp & 3, hw = warp >> 2;
+    const int H = p.H, N = p.num_seqs;
+    const int32_t* co = p.chunk_off;
+    constexpr int NSLICE = D / NV;
+    const int slice = blockIdx.x % NSLICE;
+    const int h = (blockIdx.x / NSLICE) % H;
+    const int pos = blockIdx.x / (NSLICE * H);
+    if (co[N + 1] == 0) return;  // malformed cu_seqlens: nothing is written
+    const int seq = p.order ? p.order[pos] : pos;
+    const int64_t t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
+    const int nch = co[seq + 1] - co[seq];
+    const int jb = co[seq];
+    const int j0 = slice * NV;
+
+    // state: row rho, columns [j0 + 32*hw, +32)
+    const int rho = 32 * qw + lane;
+    float S[32];
+    const size_t srow = ((static_cast<size_t>(seq) * H + h) * D + rho) * D + j0 + 32 * hw;
+    if (p.S0) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(p.S0 + srow + j);
+            S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = 0.f;
+    }
+    if (nch == 0) {
+        if (p.S_final) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(p.S_final + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
+        return;
+    }
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
+    volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
+    if (tid == 0) {
+        *abort_s = 0;
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_v);
+    }
+    for (int e = tid; e < 2 * 512; e += NT)  // zero rows of both [Tb | 0 | M] tiles
+        reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 256);
+        tmem_relinquish();
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tq = tmem + tmem_lane(qw);
+    constexpr uint32_t TM_X = 0;    // + 64 * parity
+    constexpr uint32_t TM_DS = 128;
+
+    auto issue_loads = [&](int c) {
+        uint8_t* set = sm + (c & 1) * L::SET;
+        uint64_t* bar = &bars[c & 1];
+        const uint8_t* blob = p.blobs + (static_cast<size_t>(jb + c) * H + h) * kPrefillBlobBytes;
+        mbar_arrive_expect_tx(bar, kLoadBytes);
+        bulk_g2s(set + L::S_A, blob + kBlobA, 32768, bar);
+        bulk_g2s(set + L::S_KB, blob + kBlobKb, 16384, bar);
+        bulk_g2s(set + L::S_A3, blob + kBlobTb, 8192, bar);
+        bulk_g2s(set + L::S_A3 + 16384, blob + kBlobM, 8192, bar);
+        bulk_g2s(set + L::S_EV, blob + kBlobEv, 1536, bar);
+        tma_load_3d(set + L::S_V, &tm_v, bar, j0, h, static_cast<int32_t>(t_begin + static_cast<int64_t>(c) * C));
+    };
+    if (tid == 0) {
+        issue_loads(0);
+        if (nch > 1) issue_loads(1);
+    }
+    uint32_t ph_load[2] = {0, 0}, ph_c1 = 0, ph_c2 = 0;
+    auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
+        if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
+        ph ^= 1u;
+    };
+    const uint32_t sm_base = smem_u32(sm + L::OP_SM), u_base = smem_u32(sm + L::OP_U);
+
+    for (int c = 0; c < nch; ++c) {
+        const int b = c & 1;
+        uint8_t* set = sm + b * L::SET;
+        const float* evs = reinterpret_cast<const float*>(set + L::S_EV);
+        const int64_t t0 = t_begin + static_cast<int64_t>(c) * C;
+        const int Lc = static_cast<int>(t_end - t0 < C ? t_end - t0 : C);
+        wait_bar(&bars[b], ph_load[b]);
+        if (Lc < C) {  // rows of v past the sequence end -> 0
+            for (int e = tid; e < (C - Lc) * 8; e += NT) {
+                const int r = Lc + (e >> 3);
+                *reinterpret_cast<uint4*>(set + L::S_V + sw128_chunk(r, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks 4hw..4hw+3)
+            const float sc = evs[rho];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float m8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m8[e] = sc * S[8 * ch + e];
+                *reinterpret_cast<uint4*>(sm + L::OP_SM + sw128_chunk(rho, 4 * hw + ch)) = pack8(m8);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (*abort_s) break;  // a bounded wait expired: every thread sees it after the barrier
+        const uint32_t a_base = smem_u32(set + L::S_A), kb_base = smem_u32(set + L::S_KB);
+        const uint32_t a3_base = smem_u32(set + L::S_A3), v_base = smem_u32(set + L::S_V);
+        const uint32_t tx = tmem + TM_X + 64 * b;
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16_f32(128, NV, false, true);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)  // X = [Tb; 0] V
+                mma_bf16(tx, sdesc_sw128(a3_base + s * 32, 16, 1024), sdesc_sw128(v_base + s * 2048, 8192, 1024), id,
+                         s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // X += [-W; Qh] Sm
+                mma_bf16(tx, sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
+                         sdesc_sw128(sm_base + s * 2048, 8192, 1024), id, 1u);
+            mma_commit(&bars[2]);
+            if (c >= 1 && c + 1 < nch) issue_loads(c + 1);  // the other set held chunk c-1, now consumed
+        }
+        wait_bar(&bars[2], ph_c1);
+        tc_fence_after();
+        if (qw < 2) {  // U -> OP_U (row r, chunks 4hw..4hw+3)
+            const int r = 32 * qw + lane;
+            float a[32];
+            tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4*>(sm + L::OP_U + sw128_chunk(r, 4 * hw + ch)) = pack8(a + 8 * ch);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id_s = idesc_bf16_f32(128, NV, true, true);
+            constexpr uint32_t id_o = idesc_bf16_f32(128, NV, false, true);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)  // D_S = Kb^T U
+                mma_bf16(tmem + TM_DS, sdesc_sw128(kb_base + s * 2048, 8192, 1024),
+                         sdesc_sw128(u_base + s * 2048, 8192, 1024), id_s, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)  // X += [0; M] U
+                mma_bf16(tx, sdesc_sw128(a3_base + 8192 + s * 32, 16, 1024), sdesc_sw128(u_base + s * 2048, 8192, 1024),
+                         id_o, 1u);
+            mma_commit(&bars[3]);
+        }
+        wait_bar(&bars[3], ph_c2);
+        tc_fence_after();
+        {
+            const float dc = evs[128 + rho], dcm = evs[256 + rho];
+            float a[32];
+            tmem_ld32(tq + TM_DS + 32 * hw, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) S[e] = fmaf(dc, S[e], dcm * a[e]);
+        }
+        if (qw >= 2) {  // O rows -> global
+            const int rr = 32 * (qw - 2) + lane;
+            float a[32];
+            tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
+            tmem_ld_wait();
+            if (rr < Lc) {
+                OutT* dst = static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + 32 * hw;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    const bool ok = *abort_s == 0;
+    if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
+    if (tid == 0) {  // every MMA and copy this CTA issued has landed before it exits
+        mma_commit(&bars[4]);
+        (void)mbar_wait(&bars[4], 0, kWaitLimit);
+    }
+    if (p.S_final && ok) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(p.S_final + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
+                               int32_t* device_status, cudaStream_t stream) {
+    kda_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, chunk_off, device_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
+                                 cudaStream_t stream) {
+    static int cfg_prep[64], cfg_scan_bf[64], cfg_scan_f[64];
+    cudaError_t err = set_smem(kda_chunk_prep_kernel, PrepSmem::ALLOC, cfg_prep);
+    if (err != cudaSuccess) return err;
+    const long long prep_ctas = static_cast<long long>(max_chunks) * a.H;
+    if (prep_ctas > 0) {
+        kda_chunk_prep_kernel<<<static_cast<unsigned>(prep_ctas), NT, PrepSmem::ALLOC, stream>>>(tm_q, tm_k, tm_la, a);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
+    if (scan_ctas == 0) return cudaSuccess;
+    if (out_f32) {
+        err = set_smem(kda_chunk_scan_kernel<float>, ScanSmem::ALLOC, cfg_scan_f);
+        if (err != cudaSuccess) return err;
+        kda_chunk_scan_kernel<float><<<static_cast<unsigned>(scan_ctas), NT, ScanSmem::ALLOC, stream>>>(tm_v, a);
+    } else {
+        err = set_smem(kda_chunk_scan_kernel<__nv_bfloat16>, ScanSmem::ALLOC, cfg_scan_bf);
+        if (err != cudaSuccess) return err;
+        kda_chunk_scan_kernel<__nv_bfloat16>
+            <<<static_cast<unsigned>(scan_ctas), NT, ScanSmem::ALLOC, stream>>>(tm_v, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -39,12 +39,21 @@ def test_abi_version_and_status_strings(lib):
     assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
 
 
+BLOB = 67072  # bytes of prepared operands per (chunk, head), two-pass path
+
+
 def test_workspace_bytes(lib):
-    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256
-    f32 = kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2)
-    assert f32 == 256 + 3 * 256 * 2 * 128 * 2
-    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
-    assert kda.kda_prefill_workspace_bytes(7, 1, 10, 2) == 0
+    # single-pass path: schedule (+ bf16 copies of fp32 inputs)
+    assert kda.kda_prefill_min_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256
+    assert kda.kda_prefill_min_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2) == 256 + 3 * 256 * 2 * 128 * 2
+    # two-pass path: schedule + chunk table + (copies) + (ceil(T/64) + N) chunks x H operand images
+    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256 + 256 + (16 + 16) * 32 * BLOB
+    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2) == \
+        256 + 256 + 3 * 256 * 2 * 128 * 2 + (4 + 1) * 2 * BLOB
+    for fn in (kda.kda_prefill_workspace_bytes, kda.kda_prefill_min_workspace_bytes):
+        assert fn(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
+        assert fn(7, 1, 10, 2) == 0
+        assert fn(kda.KDA_DTYPE_BF16, 1, 10, 2, 64, 128) == 0
 
 
 def _fake(addr):

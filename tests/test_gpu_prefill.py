@@ -1,9 +1,11 @@
 """GPU parity of kda_prefill (through the C ABI) against the fp64 oracle.
 
 Small cases span several chunks and ragged tails; the five benchmark
-workloads run at full size in the launch configuration the bench times, the
-oracle checking all heads (8k prefill), sampled heads per sequence (varlen)
-or two sampled heads over the full length (1M tokens).
+workloads run at full size in the launch configuration the bench times (the
+two-pass path), the oracle checking all heads (8k prefill), sampled heads per
+sequence (varlen) or two sampled heads over the full length (1M tokens).
+Both prefill paths (two-pass and single-pass, chosen by workspace size) are
+checked on the small and edge cases.
 """
 import numpy as np
 import pytest
@@ -16,6 +18,9 @@ from tests.conftest import cuda_ok
 from tests.gpu_util import TOL, host, oracle_prefill_heads, rell2
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+
+PATHS = ["two_pass", "single_pass"]
 
 
 def run_gpu(p, **kw):
@@ -40,31 +45,34 @@ def check_against_oracle(p, o, sf, heads_per_seq=None, tol=TOL):
     return errs
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("lengths", [[1], [63], [64], [65], [200], [1000]])
-def test_prefill_single_sequence(lengths):
+def test_prefill_single_sequence(lengths, path):
     p = synth.prefill_inputs(lengths, 3, seed=sum(lengths), device="cuda")
-    o, sf, st = run_gpu(p)
+    o, sf, st = run_gpu(p, path=path)
     assert st == 0
     check_against_oracle(p, o, sf)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_prefill_varlen_with_states(dtype):
+def test_prefill_varlen_with_states(dtype, path):
     lengths = [130, 0, 7, 64, 300, 1, 129]
     p = synth.prefill_inputs(lengths, 4, dtype=dtype, s0_std=0.02, seed=17, device="cuda")
-    o, sf, st = run_gpu(p)
+    o, sf, st = run_gpu(p, path=path)
     assert st == 0
     check_against_oracle(p, o, sf)
     # the empty sequence returns its start state bit for bit
     assert torch.equal(sf[1], p.S0[1])
 
 
-def test_prefill_identity_gates_keep_state_exactly():
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_identity_gates_keep_state_exactly(path):
     """beta = 0, alpha = 1: every chunk is the identity on S (fp32 path, exact)."""
     p = synth.prefill_inputs([70, 200], 2, s0_std=0.5, seed=3, device="cuda")
     p.beta.zero_()
     p.log_alpha.zero_()
-    o, sf, st = run_gpu(p)
+    o, sf, st = run_gpu(p, path=path)
     assert st == 0
     assert torch.equal(sf, p.S0)
 
@@ -101,7 +109,8 @@ def test_prefill_equals_decode_steps():
     assert rell2(host(S), host(sf)) < TOL
 
 
-def test_prefill_deterministic_and_in_bounds():
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_deterministic_and_in_bounds(path):
     p = synth.prefill_inputs([333, 64, 5], 3, s0_std=0.02, seed=4, device="cuda")
     T, H = p.q.shape[:2]
     pad = 4096
@@ -109,21 +118,22 @@ def test_prefill_deterministic_and_in_bounds():
     o = o_buf[pad:pad + T * H * 128].view(T, H, 128)
     sf_buf = torch.full((3 * H * 128 * 128 + 2 * pad,), 9.0, dtype=torch.float32, device="cuda")
     sf = sf_buf[pad:pad + 3 * H * 128 * 128].view(3, H, 128, 128)
-    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf)
+    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf, path=path)
     o1, sf1 = o.clone(), sf.clone()
-    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf)
+    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf, path=path)
     torch.cuda.synchronize()
     assert torch.equal(o, o1) and torch.equal(sf, sf1)
     assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
     assert torch.all(sf_buf[:pad] == 9.0) and torch.all(sf_buf[-pad:] == 9.0)
 
 
-def test_prefill_bad_cu_seqlens_reported():
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_bad_cu_seqlens_reported(path):
     p = synth.prefill_inputs([100, 50], 2, seed=2, device="cuda")
     p.cu_seqlens.copy_(torch.tensor([0, 120, 110], dtype=torch.int32))   # decreasing, wrong total
     o = torch.full_like(p.q, 5.0)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, o=o, device_status=status)
+    kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, o=o, device_status=status, path=path)
     torch.cuda.synchronize()
     assert int(status.item()) & kda.KDA_DEV_BAD_CU_SEQLENS
     assert torch.all(o[120:] == 5.0)        # the malformed sequence wrote nothing
@@ -136,9 +146,10 @@ def test_prefill_config0_tiny_fp32():
     check_against_oracle(p, o, sf)
 
 
-def test_prefill_config1_all_heads():
+@pytest.mark.parametrize("path", PATHS)
+def test_prefill_config1_all_heads(path):
     p = synth.config_inputs(1, device="cuda")
-    o, sf, st = run_gpu(p)
+    o, sf, st = run_gpu(p, path=path)
     assert st == 0
     errs = check_against_oracle(p, o, sf)
     assert max(errs) < TOL
