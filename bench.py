@@ -41,6 +41,9 @@ PREFILL_FLOPS_PER_TOKEN_HEAD = 10 * 64 * D + 6 * D * D                  # 180,22
 STATE_BYTES = D * D * 4                                                 # 65,536
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + PREFILL_BYTES_PER_TOKEN_HEAD  # 132,612
 METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s & % HBM (H=32, d=128)"
+# sources whose ncu DRAM counters profiles/ncu_traffic.json records (null once they change)
+PREFILL_SOURCES = ["kda_api.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh"]
+DECODE_SOURCES = ["kda_decode.cu"]
 
 
 def dist_env():
@@ -174,6 +177,23 @@ class ClockSampler:
                 "samples": len(sm), "source": self.source}
 
 
+# ------------------------------------------------------ multi-rank math ----
+
+def max_over_ranks(dist, x: float, device) -> float:
+    """Max of a per-rank scalar over all ranks (the step time every rank reports)."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_mtok_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes its own problem; value = all tokens / slowest rank."""
+    return tokens_per_rank * world / (ms_max * 1e-3) / 1e6
+
+
 # ----------------------------------------------------------------- ours ----
 
 class Ctx:
@@ -199,11 +219,7 @@ class Ctx:
         self.torch.cuda.synchronize()
 
     def max_over_ranks(self, x: float) -> float:
-        if self.ws == 1:
-            return x
-        t = self.torch.tensor([x], dtype=self.torch.float64, device=self.dev)
-        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(self.dist, x, self.dev)
 
     def events(self):
         E = self.torch.cuda.Event
@@ -275,14 +291,15 @@ def bench_prefill(cx: Ctx, args):
     e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
     pk = cx.peaks
     return {
-        "value": tokens_per_step / (ms * 1e-3) / 1e6,
+        "value": whole_job_mtok_s(T, cx.ws, ms),
         "ms": ms,
         "launches": 2 * args.steps,  # schedule + prefill kernel per call
         "tokens": T,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved_gbs / pk["hbm"], 4),
-                     "traffic": ncu_traffic("kda_prefill_kernel", ["kda_prefill.cu", "kda_ptx.cuh"]),
-                     "kernel": "kda_prefill_kernel", "peak_source": pk["src"] + " burst copy",
+                     "traffic": ncu_traffic("kda_prefill_two_pass", PREFILL_SOURCES),
+                     "kernel": "kda_prefill call (chunk table + chunk prep + scan kernels)",
+                     "peak_source": pk["src"] + " burst copy",
                      "bytes_per_launch": bytes_per_launch},
         "tensor": {"achieved": round(achieved_tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                    "frac": round(achieved_tf / pk["bf16"], 4), "flops_per_launch": flops_per_launch,
@@ -361,7 +378,7 @@ def bench_decode(cx: Ctx, args):
         "gpu_launches": reps * steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm"], 4),
-                     "traffic": ncu_traffic("kda_decode_kernel", ["kda_decode.cu"]),
+                     "traffic": ncu_traffic("kda_decode_kernel", DECODE_SOURCES),
                      "kernel": "kda_decode_kernel", "peak_source": pk["src"] + " burst copy",
                      "bytes_per_launch": n_units * DECODE_BYTES_PER_UNIT},
         "e2e": {"value": round(cx.ws * n_units * 2 * STATE_BYTES / (e2e_ms * 1e-3) / 1e9, 1),
