@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(NT, 1)
         if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
         ph ^= 1u;
     };
-    const uint32_t sm_base = smem_u32(sm + L::OP_SM), u_base = smem_u32(sm + L::OP_U);
+    const uint64_t d_sm = sdesc_sw128(smem_u32(sm + L::OP_SM), 8192, 1024);
+    const uint64_t d_u = sdesc_sw128(smem_u32(sm + L::OP_U), 8192, 1024);
 
     for (int c = 0; c < nch; ++c) {
         const int b = c & 1;
@@ -402,23 +403,26 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_before();
         __syncthreads();
         if (*abort_s) break;  // a bounded wait expired: every thread sees it after the barrier
-        const uint32_t a_base = smem_u32(set + L::S_A), kb_base = smem_u32(set + L::S_KB);
-        const uint32_t a3_base = smem_u32(set + L::S_A3), v_base = smem_u32(set + L::S_V);
+        // shared-memory descriptors; a K-step adds its byte offset / 16 to the start-address field
+        const uint64_t d_a = sdesc_sw128(smem_u32(set + L::S_A), 16, 1024);
+        const uint64_t d_kb = sdesc_sw128(smem_u32(set + L::S_KB), 8192, 1024);
+        const uint64_t d_a3 = sdesc_sw128(smem_u32(set + L::S_A3), 16, 1024);
+        const uint64_t d_v = sdesc_sw128(smem_u32(set + L::S_V), 8192, 1024);
         const uint32_t tx = tmem + TM_X + 64 * b;
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16_f32(128, NV, false, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s)  // X = [Tb; 0] V
-                mma_bf16(tx, sdesc_sw128(a3_base + s * 32, 16, 1024), sdesc_sw128(v_base + s * 2048, 8192, 1024), id,
-                         s > 0);
+                mma_bf16(tx, d_a3 + 2 * s, d_v + 128 * s, id, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // X += [-W; Qh] Sm
-                mma_bf16(tx, sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
-                         sdesc_sw128(sm_base + s * 2048, 8192, 1024), id, 1u);
+                mma_bf16(tx, d_a + (s >> 2) * 1024 + (s & 3) * 2, d_sm + 128 * s, id, 1u);
             mma_commit(&bars[2]);
-            if (c >= 1 && c + 1 < nch) issue_loads(c + 1);  // the other set held chunk c-1, now consumed
         }
+        // the other set held chunk c-1, consumed by the end of the previous step: fetch chunk c+1
+        // (a warp other than the MMA issuer issues the copies)
+        if (tid == 32 && c >= 1 && c + 1 < nch) issue_loads(c + 1);
         wait_bar(&bars[2], ph_c1);
         tc_fence_after();
         if (qw < 2) {  // U -> OP_U (row r, chunks 4hw..4hw+3)
@@ -439,12 +443,10 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr uint32_t id_o = idesc_bf16_f32(128, NV, false, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s)  // D_S = Kb^T U
-                mma_bf16(tmem + TM_DS, sdesc_sw128(kb_base + s * 2048, 8192, 1024),
-                         sdesc_sw128(u_base + s * 2048, 8192, 1024), id_s, s > 0);
+                mma_bf16(tmem + TM_DS, d_kb + 128 * s, d_u + 128 * s, id_s, s > 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)  // X += [0; M] U
-                mma_bf16(tx, sdesc_sw128(a3_base + 8192 + s * 32, 16, 1024), sdesc_sw128(u_base + s * 2048, 8192, 1024),
-                         id_o, 1u);
+            for (int s = 0; s < 4; ++s)  // X += [0; M] U  (zero rows, then M, at 8 KB into the tile)
+                mma_bf16(tx, d_a3 + 512 + 2 * s, d_u + 128 * s, id_o, 1u);
             mma_commit(&bars[3]);
         }
         wait_bar(&bars[3], ph_c2);
