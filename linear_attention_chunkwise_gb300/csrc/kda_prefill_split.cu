@@ -51,7 +51,7 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // =========================================================== pass 0 ======
 // chunk_off[n] = number of 64-token chunks in sequences 0..n-1, chunk_off[N]
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(NT, 2)
         bulk_s2g(blob + kBlobTb, sm + L::OP_A3, 16384);  // Tb and M, adjacent in both layouts
         bulk_s2g(blob + kBlobEv, sm + L::EV, 1536);
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read();  // shared memory may go once the copies have read it
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
