@@ -346,6 +346,35 @@ def bench_decode(cx: Ctx, args):
     state_gbs = cx.ws * n_units * 2 * STATE_BYTES / (ms * 1e-3) / 1e9
     achieved = n_units * DECODE_BYTES_PER_UNIT / (ms_local * 1e-3) / 1e9
 
+    # multi-token step (speculative verify): T_MULTI tokens per sequence in one launch
+    T_MULTI = 4
+    dm = synth.decode_inputs(dc["N"], dc["H"], T_MULTI, D, dc["dtype"], dc["lo"], dc["s_std"],
+                             synth.config_seed(DECODE_CFG) + 5000 + 1000 * cx.rank, cx.dev)
+    tm = lambda x: x.transpose(0, 1).contiguous()
+    mq, mk, mv, mla, mb = tm(dm.q), tm(dm.k), tm(dm.v), tm(dm.log_alpha), tm(dm.beta)
+    mo = torch.empty_like(mq)
+
+    def multi_step():
+        kda.kda_decode_multi(mq, mk, mv, mla, mb, dm.S, None, o=mo, stream=cx.stream)
+
+    for _ in range(max(1, args.warmup)):
+        multi_step()
+    cx.barrier()
+    n_multi = 50
+    ev0.record(cx.stream)
+    for _ in range(n_multi):
+        multi_step()
+    ev1.record(cx.stream)
+    cx.barrier()
+    m_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / n_multi)
+    multi = {"tokens_per_launch_per_sequence": T_MULTI, "us_per_launch": round(m_ms * 1e3, 2),
+             "tokens_per_s": round(cx.ws * n_units // dc["H"] * T_MULTI / (m_ms * 1e-3), 1),
+             "state_gbs": round(cx.ws * n_units * 2 * STATE_BYTES / (m_ms * 1e-3) / 1e9, 1),
+             "bytes_per_launch": n_units * (2 * STATE_BYTES + T_MULTI * PREFILL_BYTES_PER_TOKEN_HEAD),
+             "hbm_frac": round(n_units * (2 * STATE_BYTES + T_MULTI * PREFILL_BYTES_PER_TOKEN_HEAD)
+                               / (m_ms * 1e-3) / 1e9 / cx.peaks["hbm"], 4)}
+    del dm, mq, mk, mv, mla, mb, mo
+
     # end to end: each step's inputs H2D from pinned memory and its o D2H; the states stay in HBM
     names = ("q", "k", "v", "log_alpha", "beta")
     hq = [getattr(d, n)[0].cpu().pin_memory() for n in names]
@@ -385,6 +414,7 @@ def bench_decode(cx: Ctx, args):
                 "unit": "state GB/s", "us_per_step": round(e2e_ms * 1e3, 2),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
+        "multi_token": multi,
     }
 
 

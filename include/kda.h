@@ -167,6 +167,31 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                            int32_t *device_status, kda_stream_t stream);
 
 /*
+ * kda_decode_multi -- T consecutive tokens per sequence in one launch: a
+ * speculative-decoding verify step or a short continuation (the fused
+ * recurrent mode of "Understanding Kimi Delta Attention" (pyshine), "The
+ * Chunkwise DPLR Algorithm", over T steps; the speculative-decoding path of
+ * its "Scaling to Kimi K3" section).  Each head's fp32 state is read once,
+ * carried through the T updates on chip, and written once, in place.  The
+ * per-token arithmetic is exactly kda_decode_step's.
+ *
+ *   q, k       [N, T, H, dk]  qkv_dtype        v [N, T, H, dv] qkv_dtype
+ *   log_alpha  [N, T, H, dk]  fp32             beta [N, T, H] fp32
+ *   S          [num_slots, H, dk, dv] fp32, updated in place to the state
+ *              after all T tokens
+ *   state_indices, device_status: as kda_decode_step
+ *   o          [N, T, H, dv]  qkv_dtype (out), o[n, t] read after token t
+ *   S_steps    [N, T, H, dk, dv] fp32 (out) or NULL: the state after each
+ *              token, for rolling back to an accepted prefix
+ * T = 0 is a no-op.
+ */
+KDA_API kda_status kda_decode_multi(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                    const float *log_alpha, const float *beta, float *S,
+                                    int32_t num_slots, const int32_t *state_indices, int32_t N,
+                                    int32_t T, int32_t H, int32_t dk, int32_t dv, void *o,
+                                    float *S_steps, int32_t *device_status, kda_stream_t stream);
+
+/*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device
  * memory.  The sources have no counterpart to this entry point; it exists for
  * integration.  Some callers cannot hand the library a workspace: a plugin

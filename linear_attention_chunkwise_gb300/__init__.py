@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     KDA_ERR_WORKSPACE,
     KDA_OK,
     KdaError,
+    kda_decode_multi,
     kda_decode_step,
     kda_prefill,
     kda_prefill_min_workspace_bytes,

@@ -28,7 +28,8 @@ KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
 
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
-                    "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_prefill_noalloc")
+                    "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
+                    "kda_prefill_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def load_library(path: str | None = None):
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_multi.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P, P, P]
+        lib.kda_decode_multi.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -200,3 +203,40 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None, 
     if st != KDA_OK:
         raise KdaError("kda_decode_step", st, kda_status_string(st))
     return o
+
+
+def kda_decode_multi(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None, S_steps=None,
+                     return_steps=False, device_status=None, stream=None):
+    """T tokens per sequence in one launch; S [slots, H, 128, 128] fp32 is updated in place.
+
+    q, k, v: [N, T, H, 128] (bf16 or fp32); log_alpha: [N, T, H, 128] fp32; beta: [N, T, H] fp32;
+    state_indices: int32 [N] or None.  Returns o [N, T, H, 128], or (o, S_steps) when
+    return_steps (S_steps [N, T, H, 128, 128] fp32: the state after each token).
+    """
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    _check(k, "k", q.dtype, dev)
+    _check(v, "v", q.dtype, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    _check(state_indices, "state_indices", torch.int32, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    if q.dim() != 4:
+        raise ValueError("q must be [N, T, H, dk]")
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((N, T, H, dv), dtype=q.dtype, device=dev)
+    _check(o, "o", q.dtype, dev)
+    if S_steps is None and return_steps:
+        S_steps = torch.empty((N, T, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(S_steps, "S_steps", torch.float32, dev)
+    st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S), S.shape[0],
+                              _ptr(state_indices), N, T, H, dk, dv, _ptr(o), _ptr(S_steps), _ptr(device_status),
+                              _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_decode_multi", st, kda_status_string(st))
+    return (o, S_steps) if return_steps else o

@@ -299,4 +299,47 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtyp
     return KDA_OK;
 }
 
+kda_status kda_decode_multi(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                            const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
+                            int32_t T, int32_t H, int32_t dk, int32_t dv, void* o, float* S_steps,
+                            int32_t* device_status, kda_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || T < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    if (!sizes_ok(num_slots, H, kHeadDim, kHeadDim * 4) || !sizes_ok(N, T, H, kHeadDim * 4) ||
+        (S_steps && !sizes_ok(static_cast<int64_t>(N) * T, H, kHeadDim, kHeadDim * 4)))
+        return KDA_ERR_INVALID_ARG;
+    if (static_cast<long long>(N) * H > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (N == 0 || T == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
+    if (!state_indices && num_slots < N) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) || !aligned(o, 16) ||
+        !aligned(S, 16) || (S_steps && !aligned(S_steps, 16)) || !aligned(beta, 4) ||
+        (state_indices && !aligned(state_indices, 4)) || (device_status && !aligned(device_status, 4)))
+        return KDA_ERR_INVALID_ARG;
+    const size_t es = esize_of(qkv_dtype);
+    const size_t nio = static_cast<size_t>(N) * T * H * kHeadDim;
+    const Range r_o = range_of(o, nio * es);
+    const Range r_s = range_of(S, static_cast<size_t>(num_slots) * H * kHeadDim * kHeadDim * 4);
+    const Range r_st = range_of(S_steps, S_steps ? nio * kHeadDim * 4 : 0);
+    const Range inputs[] = {range_of(q, nio * es),
+                            range_of(k, nio * es),
+                            range_of(v, nio * es),
+                            range_of(log_alpha, nio * 4),
+                            range_of(beta, static_cast<size_t>(N) * T * H * 4),
+                            range_of(state_indices, state_indices ? static_cast<size_t>(N) * 4 : 0),
+                            range_of(device_status, device_status ? 4 : 0)};
+    for (const Range& in : inputs)
+        if (overlap(r_o, in) || overlap(r_s, in) || overlap(r_st, in)) return KDA_ERR_INVALID_ARG;
+    if (overlap(r_o, r_s) || overlap(r_o, r_st) || overlap(r_s, r_st)) return KDA_ERR_INVALID_ARG;
+
+    const kda_status dev = check_device();
+    if (dev != KDA_OK) return dev;
+    if (kda::launch_decode_multi(qkv_dtype == KDA_DTYPE_F32, q, k, v, log_alpha, beta, S, num_slots, state_indices,
+                                 N, T, H, o, S_steps, device_status, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
 }  // extern "C"

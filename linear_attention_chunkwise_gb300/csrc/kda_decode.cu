@@ -125,7 +125,123 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// T consecutive tokens per sequence in one launch (a speculative-decoding
+// verify step, or a short prefill): the state stays in registers across the
+// tokens, so it is read once and written once per launch.  The per-token
+// arithmetic is the single-step kernel's, token after token.  The small
+// per-token vectors are double-buffered by token parity so one barrier at the
+// top of each token separates its writes from the previous token's reads.
+template <typename IoT>
+__global__ void __launch_bounds__(kThreads, 2)
+    kda_decode_multi_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k, const IoT* __restrict__ v,
+                            const float* __restrict__ log_alpha, const float* __restrict__ beta, float* S,
+                            int32_t num_slots, const int32_t* __restrict__ state_indices, int32_t T, int32_t H,
+                            IoT* __restrict__ o, float* S_steps, int32_t* device_status) {
+    const int unit = blockIdx.x;
+    const int n = unit / H;
+    const int h = unit - n * H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int32_t slot = state_indices ? state_indices[n] : n;
+    if (slot < 0 || slot >= num_slots) {
+        if (tid == 0 && device_status) atomicOr(device_status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+
+    __shared__ float a_s[2][kHeadDim], k_s[2][kHeadDim], q_s[2][kHeadDim];
+    __shared__ __align__(16) float u_s[2][kHeadDim];
+    __shared__ __align__(16) float red_y[kThreads / 32][kHeadDim];
+    __shared__ __align__(16) float red_p[kThreads / 32][kHeadDim];
+    __shared__ float kq_part[2][4];
+
+    float* Sg = S + (static_cast<size_t>(slot) * H + h) * kHeadDim * kHeadDim;
+    const int row0 = warp * kRowsPerWarp;
+    float4 s[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+        s[i] = __ldcs(reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row0 + i) * kHeadDim) + lane);
+
+    for (int t = 0; t < T; ++t) {
+        const int b = t & 1;
+        const size_t tok = (static_cast<size_t>(n) * T + t) * H + h;
+        if (tid < kHeadDim) {
+            const float kk = to_f32(k[tok * kHeadDim + tid]);
+            const float qq = to_f32(q[tok * kHeadDim + tid]);
+            k_s[b][tid] = kk;
+            q_s[b][tid] = qq;
+            a_s[b][tid] = expf(log_alpha[tok * kHeadDim + tid]);
+            float kq = kk * qq;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if (lane == 0) kq_part[b][warp] = kq;
+        }
+        __syncthreads();
+
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int r = row0 + i;
+            const float a = a_s[b][r], kr = k_s[b][r], qr = q_s[b][r];
+            s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+            y.x = fmaf(kr, s[i].x, y.x); y.y = fmaf(kr, s[i].y, y.y);
+            y.z = fmaf(kr, s[i].z, y.z); y.w = fmaf(kr, s[i].w, y.w);
+            p.x = fmaf(qr, s[i].x, p.x); p.y = fmaf(qr, s[i].y, p.y);
+            p.z = fmaf(qr, s[i].z, p.z); p.w = fmaf(qr, s[i].w, p.w);
+        }
+        reinterpret_cast<float4*>(red_y[warp])[lane] = y;
+        reinterpret_cast<float4*>(red_p[warp])[lane] = p;
+        __syncthreads();
+
+        if (tid < kHeadDim) {
+            float yy = 0.f, pp = 0.f;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                yy += red_y[w][tid];
+                pp += red_p[w][tid];
+            }
+            const float u = beta[tok] * (to_f32(v[tok * kHeadDim + tid]) - yy);
+            const float kq = kq_part[b][0] + kq_part[b][1] + kq_part[b][2] + kq_part[b][3];
+            u_s[b][tid] = u;
+            o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
+        }
+        __syncthreads();
+
+        const float4 uu = reinterpret_cast<const float4*>(u_s[b])[lane];
+        float* Ss = S_steps ? S_steps + tok * kHeadDim * kHeadDim : nullptr;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const float kr = k_s[b][row0 + i];
+            s[i].x = fmaf(kr, uu.x, s[i].x); s[i].y = fmaf(kr, uu.y, s[i].y);
+            s[i].z = fmaf(kr, uu.z, s[i].z); s[i].w = fmaf(kr, uu.w, s[i].w);
+            if (Ss) __stcs(reinterpret_cast<float4*>(Ss + static_cast<size_t>(row0 + i) * kHeadDim) + lane, s[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+        __stcs(reinterpret_cast<float4*>(Sg + static_cast<size_t>(row0 + i) * kHeadDim) + lane, s[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
+                                const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
+                                int32_t N, int32_t T, int32_t H, void* o, float* S_steps, int32_t* device_status,
+                                cudaStream_t stream) {
+    const long long units = static_cast<long long>(N) * H;
+    if (units == 0 || T == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(units));
+    if (f32_io) {
+        kda_decode_multi_kernel<float><<<grid, kThreads, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), log_alpha,
+            beta, S, num_slots, state_indices, T, H, static_cast<float*>(o), S_steps, device_status);
+    } else {
+        kda_decode_multi_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+            static_cast<const __nv_bfloat16*>(v), log_alpha, beta, S, num_slots, state_indices, T, H,
+            static_cast<__nv_bfloat16*>(o), S_steps, device_status);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,

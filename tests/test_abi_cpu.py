@@ -122,3 +122,29 @@ def test_decode_rejects_bad_arguments(lib, over, expect):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         kda.load_library(str(tmp_path / "nope.so"))
+
+
+def _decode_multi(lib, **over):
+    N, T, H = 2, 3, 2
+    io = N * T * H * 128
+    a = dict(q=BASE, k=BASE + 2 * io, v=BASE + 4 * io, dtype=0, la=BASE + 6 * io, beta=BASE + 10 * io,
+             S=BASE + (1 << 30), slots=N, idx=None, N=N, T=T, H=H, dk=128, dv=128, o=BASE + 12 * io, steps=None,
+             status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_decode_multi(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]), P(a["S"]),
+                                a["slots"], P(a["idx"]), a["N"], a["T"], a["H"], a["dk"], a["dv"], P(a["o"]),
+                                P(a["steps"]), P(a["status"]), None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dv=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(T=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(T=0), kda.KDA_OK),
+    (dict(q=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(steps=BASE + 8), kda.KDA_ERR_INVALID_ARG),                    # misaligned
+    (dict(steps=BASE + (1 << 30) + 4096), kda.KDA_ERR_INVALID_ARG),     # S_steps inside S
+    (dict(o=BASE + 2 * 2 * 3 * 2 * 128), kda.KDA_ERR_INVALID_ARG),      # o overlaps k
+])
+def test_decode_multi_rejects_bad_arguments(lib, over, expect):
+    assert _decode_multi(lib, **over) == expect

@@ -85,3 +85,63 @@ def test_decode_config3_graph_sampled():
                                               host(d.beta[t, n:n + 1, h:h + 1]), S)[0, 0]
         assert rell2(host(o_all[:, n, h]), o_ref) < TOL
         assert rell2(host(d.S[n, h]), S[0, 0]) < 1e-4
+
+
+# ------------------------------------------------------------ multi-token --
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_multi_equals_single_steps(dtype):
+    """T tokens in one launch == T single-step launches (same per-token arithmetic)."""
+    N, H, T = 5, 3, 6
+    d = synth.decode_inputs(N, H, T, dtype=dtype, seed=71, device="cuda", num_slots=8, permute_slots=True)
+    S_single = d.S.clone()
+    o_single = torch.stack([kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], S_single,
+                                                d.state_indices) for t in range(T)], dim=1)
+    tm = lambda x: x.transpose(0, 1).contiguous()  # [T, N, ...] -> [N, T, ...]
+    S_multi = d.S.clone()
+    o_multi, steps = kda.kda_decode_multi(tm(d.q), tm(d.k), tm(d.v), tm(d.log_alpha), tm(d.beta), S_multi,
+                                          d.state_indices, return_steps=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_multi, o_single)
+    assert torch.equal(S_multi, S_single)
+    idx = d.state_indices.long()
+    assert torch.equal(steps[:, -1], S_multi[idx])
+    # state after token t == state after t+1 single steps
+    S_ref = d.S.clone()
+    for t in range(T):
+        kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], S_ref, d.state_indices)
+        torch.cuda.synchronize()
+        assert torch.equal(steps[:, t], S_ref[idx])
+
+
+def test_decode_multi_oracle_and_slots():
+    N, H, T = 6, 4, 4
+    d = synth.decode_inputs(N, H, T, seed=72, device="cuda", num_slots=10, permute_slots=True)
+    S_before = d.S.clone()
+    S_ref = host(d.S).astype(np.float64)
+    idx = d.state_indices.cpu().numpy()
+    o_ref = np.stack([oracle.kda_decode_step(host(d.q[t]), host(d.k[t]), host(d.v[t]), host(d.log_alpha[t]),
+                                             host(d.beta[t]), S_ref, idx) for t in range(T)], axis=1)
+    tm = lambda x: x.transpose(0, 1).contiguous()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = kda.kda_decode_multi(tm(d.q), tm(d.k), tm(d.v), tm(d.log_alpha), tm(d.beta), d.S, d.state_indices,
+                             device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert rell2(host(o), o_ref) < TOL
+    assert rell2(host(d.S), S_ref) < 1e-5
+    for s in set(range(10)) - set(idx.tolist()):
+        assert torch.equal(d.S[s], S_before[s])
+
+
+def test_decode_multi_equals_prefill():
+    """T decode tokens == a prefill over the same T tokens from the same start state."""
+    N, H, T = 3, 2, 70
+    p = synth.prefill_inputs([T] * N, H, s0_std=0.02, seed=73, device="cuda")
+    o_p, sf = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0)
+    S = p.S0.clone()
+    r = lambda x: x.view(N, T, *x.shape[1:]).contiguous()
+    o_m = kda.kda_decode_multi(r(p.q), r(p.k), r(p.v), r(p.log_alpha), r(p.beta), S)
+    torch.cuda.synchronize()
+    assert rell2(host(o_m.view_as(o_p)), host(o_p)) < TOL
+    assert rell2(host(S), host(sf)) < TOL
