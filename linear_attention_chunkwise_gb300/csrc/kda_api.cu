@@ -44,6 +44,71 @@ kda_status check_device() {
     return ok ? KDA_OK : KDA_ERR_UNSUPPORTED;
 }
 
+int sm_count() {
+    static int count[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) count[dev] = c;
+    }
+    return count[dev];
+}
+
+// Piecewise schedule of the two-pass prefill.  When the scan has fewer CTAs
+// than the GPU has SMs (few sequences), the chunks are processed in pieces of
+// kPieceChunks per sequence: pass 1 of piece i+1 runs on the SMs the scan of
+// piece i leaves idle, and pass 2 reads operand images that pass 1 wrote
+// moments earlier (still in L2).  Pass 1 stays on the caller's stream; pass 2
+// runs on a library-owned high-priority stream per device, ordered by events,
+// and the caller's stream waits for the last scan before the call returns.
+// Pass 1 of piece i+1 is held back (a stream wait on a counter the scan CTAs
+// bump as they start) until every scan CTA of piece i is resident, so the
+// prep CTAs cannot take the SMs the scan needs.
+constexpr int kPieceChunks = 32;
+
+struct PieceStreams {
+    std::mutex mu;  // one call at a time enqueues record/wait pairs on these
+    cudaStream_t scan = nullptr;
+    cudaEvent_t prep_done = nullptr, scan_done = nullptr;
+    bool failed = false;
+};
+PieceStreams* piece_streams() {
+    static PieceStreams res[kMaxDevices];
+    static std::mutex init_mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    PieceStreams& r = res[dev];
+    std::lock_guard<std::mutex> g(init_mu);
+    if (r.failed) return nullptr;
+    if (!r.scan) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&r.scan, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+            cudaEventCreateWithFlags(&r.prep_done, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&r.scan_done, cudaEventDisableTiming) != cudaSuccess) {
+            r.failed = true;
+            return nullptr;
+        }
+    }
+    return &r;
+}
+
+// cuStreamWaitValue32 (driver entry point), or null when unavailable.
+PFN_cuStreamWaitValue32_v11070 wait_value_fn() {
+    static PFN_cuStreamWaitValue32_v11070 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 11070, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(p);
+    });
+    return fn;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -88,7 +153,7 @@ int64_t max_chunks(int32_t N, int64_t T) { return (T + kda::kChunk - 1) / kda::k
 WsLayout split_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
     WsLayout w;
     w.table = round_up(static_cast<size_t>(N > 0 ? N : 1) * 4, kAlign);
-    w.copies = w.table + round_up(static_cast<size_t>(N + 2) * 4, kAlign);
+    w.copies = w.table + round_up(static_cast<size_t>(N + 3) * 4, kAlign);  // chunk table + start counter
     w.blobs = w.copies + copies_bytes(t, T, H);
     w.total = w.blobs + static_cast<size_t>(max_chunks(N, T)) * H * kda::kPrefillBlobBytes;
     return w;
@@ -248,10 +313,44 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     const bool out_f32 = qkv_dtype == KDA_DTYPE_F32;
     if (two_pass) {
         if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, reinterpret_cast<int32_t*>(ws + two.table),
-                                    device_status, stream) != cudaSuccess ||
-            kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, a, max_chunks(num_seqs, total_tokens), out_f32,
-                                      stream) != cudaSuccess)
+                                    device_status, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
+        // chunks of the longest possible sequence bound the number of pieces
+        const int64_t seq_chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
+        const int64_t pieces = (seq_chunks + kPieceChunks - 1) / kPieceChunks;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        PieceStreams* ps = nullptr;
+        if (S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
+            cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
+            ps = piece_streams();
+        if (!ps)
+            return kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, a, max_chunks(num_seqs, total_tokens), out_f32,
+                                             stream) == cudaSuccess
+                       ? KDA_OK
+                       : KDA_ERR_CUDA;
+        std::lock_guard<std::mutex> g(ps->mu);
+        auto wait_value = wait_value_fn();
+        uint32_t* started = reinterpret_cast<uint32_t*>(ws + two.table) + num_seqs + 2;
+        const uint32_t scan_ctas = static_cast<uint32_t>(num_seqs) * H * 2;
+        bool ok = !wait_value || cudaMemsetAsync(started, 0, 4, stream) == cudaSuccess;
+        a.piece_len = kPieceChunks;
+        a.started = wait_value ? started : nullptr;
+        for (int64_t i = 0; i < pieces && ok; ++i) {
+            a.piece_begin = static_cast<int32_t>(i * kPieceChunks);
+            if (i > 0 && wait_value)
+                ok = wait_value(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(started),
+                                static_cast<cuuint32_t>(i * scan_ctas), CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
+            ok = ok &&
+                 kda::launch_chunk_prep(tm_q, tm_k, tm_la, a, static_cast<int64_t>(num_seqs) * kPieceChunks, stream) ==
+                     cudaSuccess &&
+                 cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
+                 cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess &&
+                 kda::launch_chunk_scan(tm_v, a, out_f32, ps->scan) == cudaSuccess;
+        }
+        // join even after a failed launch so later work on `stream` stays ordered
+        const bool joined = cudaEventRecord(ps->scan_done, ps->scan) == cudaSuccess &&
+                            cudaStreamWaitEvent(stream, ps->scan_done, 0) == cudaSuccess;
+        return ok && joined ? KDA_OK : KDA_ERR_CUDA;
     } else if (kda::launch_prefill_fused(tm_q, tm_k, tm_v, tm_la, a, out_f32, stream) != cudaSuccess) {
         return KDA_ERR_CUDA;
     }

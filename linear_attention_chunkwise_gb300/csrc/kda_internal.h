@@ -37,6 +37,12 @@ struct PrefillArgs {
     int64_t total_tokens;
     int32_t num_seqs;
     int32_t H;
+    // Two-pass path run in pieces: chunks [piece_begin, piece_begin + piece_len)
+    // of every sequence; piece_len = 0 means all chunks in one launch pair.
+    int32_t piece_begin = 0;
+    int32_t piece_len = 0;
+    // piece mode: every pass-2 CTA adds 1 here when it starts (workspace word)
+    uint32_t* started = nullptr;
 };
 
 // Bytes per (chunk, head) of the two-pass path's operand images:
@@ -62,5 +68,11 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                  const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
                                  cudaStream_t stream);
+// The two passes separately, for the piecewise schedule.  Pass 1's grid is
+// `units` x H CTAs: units = chunk slots of the whole batch (piece_len = 0) or
+// num_seqs x piece_len (piece mode).  Pass 2 has num_seqs x H x 2 CTAs.
+cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_la,
+                              const PrefillArgs& a, int64_t units, cudaStream_t stream);
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream);
 
 }  // namespace kda

@@ -136,16 +136,26 @@ __global__ void __launch_bounds__(NT, 2)
     const int qw = warp & 3, hw = warp >> 2;
     const int H = p.H, N = p.num_seqs;
     const int32_t* co = p.chunk_off;
-    const int j = blockIdx.x / H;
-    const int h = blockIdx.x - j * H;
-    if (co[N + 1] == 0 || j >= co[N]) return;
-    int lo = 0, hi = N - 1;  // the sequence owning chunk j: largest n with co[n] <= j
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (co[mid] <= j) lo = mid;
-        else hi = mid - 1;
+    const int unit = blockIdx.x / H;
+    const int h = blockIdx.x - unit * H;
+    if (co[N + 1] == 0) return;
+    int j, seq;  // global chunk index, owning sequence
+    if (p.piece_len > 0) {  // unit = (sequence, chunk of the piece)
+        seq = unit / p.piece_len;
+        const int c = p.piece_begin + (unit - seq * p.piece_len);
+        if (seq >= N || c >= co[seq + 1] - co[seq]) return;
+        j = co[seq] + c;
+    } else {  // unit = global chunk; its sequence is the largest n with co[n] <= j
+        j = unit;
+        if (j >= co[N]) return;
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (co[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        seq = lo;
     }
-    const int seq = lo;
     const int64_t t0 = static_cast<int64_t>(p.cu_seqlens[seq]) + static_cast<int64_t>(j - co[seq]) * C;
     const int64_t rem = p.cu_seqlens[seq + 1] - t0;
     const int Lc = static_cast<int>(rem < C ? rem : C);
@@ -298,21 +308,32 @@ __global__ void __launch_bounds__(NT, 1)
     const int slice = blockIdx.x % NSLICE;
     const int h = (blockIdx.x / NSLICE) % H;
     const int pos = blockIdx.x / (NSLICE * H);
+    if (p.started && tid == 0) atomicAdd(p.started, 1u);  // before any early exit: the host gates on it
     if (co[N + 1] == 0) return;  // malformed cu_seqlens: nothing is written
     const int seq = p.order ? p.order[pos] : pos;
-    const int64_t t_begin = p.cu_seqlens[seq], t_end = p.cu_seqlens[seq + 1];
-    const int nch = co[seq + 1] - co[seq];
-    const int jb = co[seq];
+    const int nch_seq = co[seq + 1] - co[seq];
+    // chunks [cb, cb + nch) of the sequence; in piece mode the state enters
+    // from S_final (the previous piece's carry) unless the piece is the first
+    int cb = 0, nch = nch_seq;
+    if (p.piece_len > 0) {
+        cb = p.piece_begin;
+        if (cb > 0 && cb >= nch_seq) return;
+        nch = min(nch_seq - cb, p.piece_len);
+        if (nch < 0) nch = 0;
+    }
+    const int64_t t_begin = p.cu_seqlens[seq] + static_cast<int64_t>(cb) * C, t_end = p.cu_seqlens[seq + 1];
+    const int jb = co[seq] + cb;
     const int j0 = slice * NV;
+    const float* S_in = cb == 0 ? p.S0 : p.S_final;
 
     // state: row rho, columns [j0 + 32*hw, +32)
     const int rho = 32 * qw + lane;
     float S[32];
     const size_t srow = ((static_cast<size_t>(seq) * H + h) * D + rho) * D + j0 + 32 * hw;
-    if (p.S0) {
+    if (S_in) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(p.S0 + srow + j);
+            const float4 t = *reinterpret_cast<const float4*>(S_in + srow + j);
             S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
         }
     } else {
@@ -508,18 +529,30 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
-                                 cudaStream_t stream) {
-    static int cfg_prep[64], cfg_scan_bf[64], cfg_scan_f[64];
+cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_la,
+                              const PrefillArgs& a, int64_t units, cudaStream_t stream) {
+    static int cfg_prep[64];
     cudaError_t err = set_smem(kda_chunk_prep_kernel, PrepSmem::ALLOC, cfg_prep);
     if (err != cudaSuccess) return err;
-    const long long prep_ctas = static_cast<long long>(max_chunks) * a.H;
+    const long long prep_ctas = static_cast<long long>(units) * a.H;
     if (prep_ctas > 0) {
         kda_chunk_prep_kernel<<<static_cast<unsigned>(prep_ctas), NT, PrepSmem::ALLOC, stream>>>(tm_q, tm_k, tm_la, a);
         err = cudaGetLastError();
-        if (err != cudaSuccess) return err;
     }
+    return err;
+}
+
+cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                 const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
+                                 cudaStream_t stream) {
+    const cudaError_t err = launch_chunk_prep(tm_q, tm_k, tm_la, a, max_chunks, stream);
+    if (err != cudaSuccess) return err;
+    return launch_chunk_scan(tm_v, a, out_f32, stream);
+}
+
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
+    static int cfg_scan_bf[64], cfg_scan_f[64];
+    cudaError_t err;
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
     if (out_f32) {
