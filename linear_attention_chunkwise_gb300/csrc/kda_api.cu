@@ -57,7 +57,7 @@ int sm_count() {
 
 // Piecewise schedule of the two-pass prefill.  When the scan has fewer CTAs
 // than the GPU has SMs (few sequences), the chunks are processed in pieces of
-// kPieceChunks per sequence: pass 1 of piece i+1 runs on the SMs the scan of
+// kPieceChunks (64) per sequence: pass 1 of piece i+1 runs on the SMs the scan of
 // piece i leaves idle, and pass 2 reads operand images that pass 1 wrote
 // moments earlier (still in L2).  Pass 1 stays on the caller's stream; pass 2
 // runs on a library-owned high-priority stream per device, ordered by events,
@@ -65,7 +65,7 @@ int sm_count() {
 // Pass 1 of piece i+1 is held back (a stream wait on a counter the scan CTAs
 // bump as they start) until every scan CTA of piece i is resident, so the
 // prep CTAs cannot take the SMs the scan needs.
-constexpr int kPieceChunks = 32;
+constexpr int kPieceChunks = 64;
 
 struct PieceStreams {
     std::mutex mu;  // one call at a time enqueues record/wait pairs on these
