@@ -72,6 +72,7 @@ typedef enum {
 #define KDA_DEV_BAD_CU_SEQLENS 0x1  /* cu_seqlens not 0 .. total_tokens non-decreasing */
 #define KDA_DEV_BAD_SLOT 0x2        /* state_indices entry outside [0, num_slots) */
 #define KDA_DEV_TIMEOUT 0x4         /* an on-chip wait hit its iteration limit */
+#define KDA_DEV_BAD_SNAPSHOT 0x8    /* kda_prefill_snapshots: a (sequence, position) entry is invalid */
 
 /* Version of this header the library was built from. */
 KDA_API int32_t kda_abi_version(void);
@@ -144,6 +145,35 @@ KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v, kda_
                        int32_t H, int32_t dk, int32_t dv, void *o, float *S_final,
                        void *workspace, size_t workspace_bytes, int32_t *device_status,
                        kda_stream_t stream);
+
+/*
+ * kda_prefill_snapshots -- kda_prefill that also records the state at
+ * caller-chosen positions inside the sequences: the prefix-cache boundaries
+ * of "Kimi Delta Attention (KDA)" (codewithdark), section "KV Caching
+ * Challenges & vLLM Contribution", where a cached prefix is resumed from its
+ * state instead of being recomputed.
+ *
+ *   snap_seq   [num_snaps] int32, device: sequence index of each entry
+ *   snap_pos   [num_snaps] int32, device: tokens of that sequence consumed,
+ *              a multiple of 64 or the sequence length, 0 < pos <= length
+ *   S_snap     [num_snaps, H, dk, dv] fp32 (out): entry i receives the
+ *              state after the first snap_pos[i] tokens of sequence
+ *              snap_seq[i] -- exactly the S_final a kda_prefill over that
+ *              prefix alone would return
+ *
+ * Entries must be sorted by (sequence, position) with no repeats.  An entry
+ * that breaks a rule sets KDA_DEV_BAD_SNAPSHOT; its S_snap slice may then be
+ * left unwritten (never a write outside S_snap).  All other arguments and
+ * errors are those of kda_prefill; snapshots need the two-pass workspace
+ * (>= kda_prefill_workspace_bytes), else KDA_ERR_WORKSPACE.
+ */
+KDA_API kda_status kda_prefill_snapshots(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                 const float *log_alpha, const float *beta, const float *S0,
+                                 const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                 int32_t H, int32_t dk, int32_t dv, void *o, float *S_final,
+                                 const int32_t *snap_seq, const int32_t *snap_pos, int32_t num_snaps,
+                                 float *S_snap, void *workspace, size_t workspace_bytes,
+                                 int32_t *device_status, kda_stream_t stream);
 
 /*
  * kda_decode_step -- one fused recurrent step for N sequences

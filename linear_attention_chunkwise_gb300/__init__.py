@@ -1,7 +1,8 @@
 """GB300-native Kimi Delta Attention: chunkwise prefill and fused decode (libkda).
 
 Python names mirror the C ABI in include/kda.h:
-  kda_prefill, kda_decode_step, kda_prefill_workspace_bytes, kda_status_string.
+  kda_prefill, kda_prefill_snapshots, kda_decode_step, kda_decode_multi,
+  kda_prefill_workspace_bytes, kda_status_string.
 The library must be built first (``__graft_entry__.build()`` or
 ``python -m linear_attention_chunkwise_gb300._build``); there is no fallback.
 """
@@ -9,6 +10,7 @@ from ._binding import (  # noqa: F401
     EXPORTED_SYMBOLS,
     KDA_DEV_BAD_CU_SEQLENS,
     KDA_DEV_BAD_SLOT,
+    KDA_DEV_BAD_SNAPSHOT,
     KDA_DEV_TIMEOUT,
     KDA_DTYPE_BF16,
     KDA_DTYPE_F32,
@@ -22,6 +24,7 @@ from ._binding import (  # noqa: F401
     kda_decode_step,
     kda_prefill,
     kda_prefill_min_workspace_bytes,
+    kda_prefill_snapshots,
     kda_prefill_workspace_bytes,
     kda_status_string,
     library_path,

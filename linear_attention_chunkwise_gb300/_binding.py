@@ -26,10 +26,11 @@ KDA_DTYPE_F32 = 1
 KDA_DEV_BAD_CU_SEQLENS = 0x1
 KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
+KDA_DEV_BAD_SNAPSHOT = 0x8
 
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
-                    "kda_prefill_noalloc")
+                    "kda_prefill_noalloc", "kda_prefill_snapshots")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +66,9 @@ def load_library(path: str | None = None):
         lib.kda_prefill_min_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
         lib.kda_prefill_min_workspace_bytes.restype = sz
         lib.kda_prefill.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P, P, sz, P, P]
+        lib.kda_prefill_snapshots.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
+                                              P, P, i32, P, P, sz, P, P]
+        lib.kda_prefill_snapshots.restype = ctypes.c_int
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -173,6 +177,52 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, *, o=None, S_fina
     if st != KDA_OK:
         raise KdaError("kda_prefill", st, kda_status_string(st))
     return o, S_final
+
+
+def kda_prefill_snapshots(q, k, v, log_alpha, beta, cu_seqlens, snap_seq, snap_pos, S0=None, *, o=None,
+                          S_final=None, S_snap=None, workspace=None, device_status=None, stream=None):
+    """kda_prefill that also returns the state at (sequence, position) entries (see include/kda.h).
+
+    snap_seq, snap_pos: int32 [M] on the device, sorted by (sequence, position); each position is a
+    multiple of 64 or the sequence length.  Returns (o, S_final, S_snap) with S_snap [M, H, 128, 128].
+    """
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    for t, n, dt in ((k, "k", q.dtype), (v, "v", q.dtype), (log_alpha, "log_alpha", torch.float32),
+                     (beta, "beta", torch.float32), (cu_seqlens, "cu_seqlens", torch.int32),
+                     (snap_seq, "snap_seq", torch.int32), (snap_pos, "snap_pos", torch.int32),
+                     (S0, "S0", torch.float32)):
+        _check(t, n, dt, dev)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, dk]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    M = snap_seq.numel()
+    if snap_pos.numel() != M:
+        raise ValueError("snap_seq and snap_pos must have the same length")
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if S_final is None:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if S_snap is None:
+        S_snap = torch.empty((M, H, dk, dv), dtype=torch.float32, device=dev)
+    for t, n in ((o, "o"), (S_final, "S_final"), (S_snap, "S_snap")):
+        _check(t, n, q.dtype if n == "o" else torch.float32, dev)
+    need = int(lib.kda_prefill_workspace_bytes(code, N, T, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    st = lib.kda_prefill_snapshots(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                                   _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(o), _ptr(S_final), _ptr(snap_seq),
+                                   _ptr(snap_pos), M, _ptr(S_snap), _ptr(workspace), workspace.numel(),
+                                   _ptr(device_status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_snapshots", st, kda_status_string(st))
+    return o, S_final, S_snap
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None, device_status=None, stream=None):

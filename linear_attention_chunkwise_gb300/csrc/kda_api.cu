@@ -207,10 +207,22 @@ size_t kda_prefill_min_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, in
     return fused_layout(qkv_dtype, num_seqs, total_tokens, H).total;
 }
 
-kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
-                       const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
-                       int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
-                       void* workspace, size_t workspace_bytes, int32_t* device_status, kda_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+struct Snapshots {
+    const int32_t* seq = nullptr;
+    const int32_t* pos = nullptr;
+    int32_t count = 0;
+    float* S = nullptr;
+};
+
+kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
+                        int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
+                        const Snapshots& snap, void* workspace, size_t workspace_bytes, int32_t* device_status,
+                        kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
@@ -238,6 +250,13 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     if (!two_pass && workspace_bytes < one.total) return KDA_ERR_WORKSPACE;
     const WsLayout& lay = two_pass ? two : one;
     const size_t need = lay.total;
+    if (snap.count < 0) return KDA_ERR_INVALID_ARG;
+    if (snap.count > 0) {
+        if (!snap.seq || !snap.pos || !snap.S || !aligned(snap.seq, 4) || !aligned(snap.pos, 4) || !aligned(snap.S, 16))
+            return KDA_ERR_INVALID_ARG;
+        if (!sizes_ok(snap.count, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
+        if (!two_pass) return KDA_ERR_WORKSPACE;
+    }
 
     // Overlap rules: outputs overlap nothing (S_final may equal S0 exactly).
     const Range r_o = range_of(o, nqk * es), r_sf = range_of(S_final, S_final ? nst * 4 : 0);
@@ -255,6 +274,16 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     if (have_tokens && (overlap(r_o, r_sf) || overlap(r_o, r_ws) || overlap(r_o, r_s0))) return KDA_ERR_INVALID_ARG;
     if (overlap(r_sf, r_ws) || overlap(r_s0, r_ws)) return KDA_ERR_INVALID_ARG;
     if (S0 && S_final && S0 != S_final && overlap(r_sf, r_s0)) return KDA_ERR_INVALID_ARG;
+    if (snap.count > 0) {  // S_snap is an output: it overlaps nothing
+        const Range r_ss = range_of(snap.S, static_cast<size_t>(snap.count) * H * kHeadDim * kHeadDim * 4);
+        const Range r_sq = range_of(snap.seq, static_cast<size_t>(snap.count) * 4);
+        const Range r_sp = range_of(snap.pos, static_cast<size_t>(snap.count) * 4);
+        for (const Range& in : inputs)
+            if (overlap(r_ss, in)) return KDA_ERR_INVALID_ARG;
+        if (overlap(r_ss, r_sq) || overlap(r_ss, r_sp) || overlap(r_ss, r_ws) || overlap(r_ss, r_s0) ||
+            overlap(r_ss, r_sf) || (have_tokens && overlap(r_ss, r_o)))
+            return KDA_ERR_INVALID_ARG;
+    }
 
     const kda_status dev = check_device();
     if (dev != KDA_OK) return dev;
@@ -307,13 +336,17 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
     a.o = o;
     a.S_final = S_final;
     a.device_status = device_status;
+    a.snap_seq = snap.seq;
+    a.snap_pos = snap.pos;
+    a.num_snaps = snap.count;
+    a.S_snap = snap.S;
     a.total_tokens = total_tokens;
     a.num_seqs = num_seqs;
     a.H = H;
     const bool out_f32 = qkv_dtype == KDA_DTYPE_F32;
     if (two_pass) {
         if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, reinterpret_cast<int32_t*>(ws + two.table),
-                                    device_status, stream) != cudaSuccess)
+                                    device_status, snap.seq, snap.pos, snap.count, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
         // chunks of the longest possible sequence bound the number of pieces
         const int64_t seq_chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
@@ -355,6 +388,33 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
         return KDA_ERR_CUDA;
     }
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                       const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
+                       void* workspace, size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
+    return prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv, o,
+                        S_final, Snapshots{}, workspace, workspace_bytes, device_status, stream);
+}
+
+kda_status kda_prefill_snapshots(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                 const float* log_alpha, const float* beta, const float* S0,
+                                 const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                 int32_t dk, int32_t dv, void* o, float* S_final, const int32_t* snap_seq,
+                                 const int32_t* snap_pos, int32_t num_snaps, float* S_snap, void* workspace,
+                                 size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
+    Snapshots snap;
+    snap.seq = snap_seq;
+    snap.pos = snap_pos;
+    snap.count = num_snaps;
+    snap.S = S_snap;
+    return prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv, o,
+                        S_final, snap, workspace, workspace_bytes, device_status, stream);
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,

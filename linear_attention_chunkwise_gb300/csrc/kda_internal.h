@@ -43,6 +43,11 @@ struct PrefillArgs {
     int32_t piece_len = 0;
     // piece mode: every pass-2 CTA adds 1 here when it starts (workspace word)
     uint32_t* started = nullptr;
+    // state snapshots (two-pass path): sorted (sequence, position) entries
+    const int32_t* snap_seq = nullptr;
+    const int32_t* snap_pos = nullptr;
+    int32_t num_snaps = 0;
+    float* S_snap = nullptr;
 };
 
 // Bytes per (chunk, head) of the two-pass path's operand images:
@@ -64,7 +69,8 @@ cudaError_t launch_prefill_fused(const CUtensorMap& tm_q, const CUtensorMap& tm_
 // Two-pass chunkwise prefill: chunk table, then per-(chunk, head) prep into
 // the workspace, then the per-(sequence, head, dv slice) scan.
 cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
-                               int32_t* device_status, cudaStream_t stream);
+                               int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
+                               int32_t num_snaps, cudaStream_t stream);
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                  const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
                                  cudaStream_t stream);

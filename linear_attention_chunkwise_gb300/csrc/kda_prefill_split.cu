@@ -23,6 +23,8 @@
 // CTA winds down instead of hanging.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "kda_prefill_common.cuh"
 
 namespace kda {
@@ -59,7 +61,8 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // <= c_N = total_tokens), else 0 and every offset 0 (nothing is computed).
 __global__ void __launch_bounds__(1024) kda_chunk_table_kernel(const int32_t* __restrict__ cu, int32_t N,
                                                                int64_t total, int32_t* chunk_off,
-                                                               int32_t* device_status) {
+                                                               int32_t* device_status, const int32_t* snap_seq,
+                                                               const int32_t* snap_pos, int32_t num_snaps) {
     __shared__ int s_bad;
     __shared__ long long s_warp[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,6 +108,19 @@ __global__ void __launch_bounds__(1024) kda_chunk_table_kernel(const int32_t* __
         chunk_off[N + 1] = ok ? 1 : 0;
     }
     if (tid == 0 && !ok && device_status) atomicOr(device_status, KDA_DEV_BAD_CU_SEQLENS);
+    // snapshot entries: sequence in range, 0 < pos <= length, pos a multiple of the chunk or the
+    // length, sorted by (sequence, position) without repeats
+    if (ok && device_status) {
+        bool bad_snap = false;
+        for (int i = tid; i < num_snaps; i += 1024) {
+            const int sq = snap_seq[i], ps = snap_pos[i];
+            if (sq < 0 || sq >= N) { bad_snap = true; continue; }
+            const int64_t len = static_cast<int64_t>(cu[sq + 1]) - cu[sq];
+            if (ps <= 0 || ps > len || (ps % C != 0 && ps != len)) bad_snap = true;
+            if (i > 0 && (snap_seq[i - 1] > sq || (snap_seq[i - 1] == sq && snap_pos[i - 1] >= ps))) bad_snap = true;
+        }
+        if (bad_snap) atomicOr(device_status, KDA_DEV_BAD_SNAPSHOT);
+    }
 }
 
 // =========================================================== pass 1 ======
@@ -325,6 +341,27 @@ __global__ void __launch_bounds__(NT, 1)
     const int jb = co[seq] + cb;
     const int j0 = slice * NV;
     const float* S_in = cb == 0 ? p.S0 : p.S_final;
+    // snapshot entries of this sequence (sorted by sequence, then position): [si, se)
+    int si = 0, se = 0;
+    if (p.num_snaps > 0) {
+        int lo = 0, hi = p.num_snaps;  // first entry with sequence >= seq
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (p.snap_seq[mid] < seq) lo = mid + 1;
+            else hi = mid;
+        }
+        si = lo;
+        hi = p.num_snaps;  // first entry with sequence > seq
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (p.snap_seq[mid] <= seq) lo = mid + 1;
+            else hi = mid;
+        }
+        se = lo;
+        while (si < se && p.snap_pos[si] <= cb * C) ++si;  // taken by an earlier piece
+    }
+    const int64_t seq_len = static_cast<int64_t>(p.cu_seqlens[seq + 1]) - p.cu_seqlens[seq];
+    int next_snap = si < se ? p.snap_pos[si] : INT_MAX;
 
     // state: row rho, columns [j0 + 32*hw, +32)
     const int rho = 32 * qw + lane;
@@ -480,6 +517,19 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) S[e] = fmaf(dc, S[e], dcm * a[e]);
         }
+        {  // state snapshots at the end of this chunk (positions are sequence-relative)
+            const int64_t done = min(static_cast<int64_t>(cb + c + 1) * C, seq_len);
+            while (next_snap <= done) {
+                if (next_snap == done) {
+                    float* dst = p.S_snap + ((static_cast<size_t>(si) * H + h) * D + rho) * D + j0 + 32 * hw;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+                }
+                ++si;
+                next_snap = si < se ? p.snap_pos[si] : INT_MAX;
+            }
+        }
         if (qw >= 2) {  // O rows -> global
             const int rr = 32 * (qw - 2) + lane;
             float a[32];
@@ -524,8 +574,10 @@ cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
 }  // namespace
 
 cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
-                               int32_t* device_status, cudaStream_t stream) {
-    kda_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, chunk_off, device_status);
+                               int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
+                               int32_t num_snaps, cudaStream_t stream) {
+    kda_chunk_table_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, chunk_off, device_status,
+                                                   snap_seq, snap_pos, num_snaps);
     return cudaGetLastError();
 }
 

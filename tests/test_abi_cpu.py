@@ -95,6 +95,36 @@ def test_prefill_rejects_bad_arguments(lib, over, expect):
     assert _prefill(lib, **over) == expect
 
 
+def _snapshots(lib, **over):
+    T, H, N = 128, 2, 1
+    tok = T * H * 128
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, o=BASE + 12 * tok, Sf=BASE + 14 * tok,
+             sseq=BASE + 16 * tok, spos=BASE + 16 * tok + 256, M=2, Ss=BASE + 60 * tok, ws=BASE + 20 * tok,
+             wsb=1 << 20, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill_snapshots(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]),
+                                     P(a["S0"]), P(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"], P(a["o"]),
+                                     P(a["Sf"]), P(a["sseq"]), P(a["spos"]), a["M"], P(a["Ss"]), P(a["ws"]),
+                                     a["wsb"], P(a["status"]), None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(M=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(sseq=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(spos=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(Ss=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(Ss=BASE + 60 * 128 * 2 * 128 + 8), kda.KDA_ERR_INVALID_ARG),    # misaligned
+    (dict(Ss=BASE + 12 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),        # S_snap overlaps o
+    (dict(Ss=BASE + 19 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),        # S_snap overlaps the workspace
+    (dict(wsb=4096), kda.KDA_ERR_WORKSPACE),                              # single-pass workspace only
+    (dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
+])
+def test_prefill_snapshots_rejects_bad_arguments(lib, over, expect):
+    assert _snapshots(lib, **over) == expect
+
+
 def _decode(lib, **over):
     N, H = 4, 2
     io = N * H * 128
