@@ -16,17 +16,21 @@
  * Conventions shared by every entry point
  *   - alpha_t = exp(log_alpha_t) (natural log), one gate per key channel;
  *     beta_t is used as given (the sources give it as a sigmoid in [0, 1]).
- *   - No scaling or normalisation of q/k inside the library: callers pass
- *     q and k already L2-normalised per (token, head), as the sources'
- *     "KDA Architecture" section describes.
+ *   - No scaling or normalisation of q/k in the plain entry points: callers
+ *     pass q and k already L2-normalised per (token, head), as the sources'
+ *     "KDA Architecture" section describes (the _ex entry points can do it
+ *     inside the kernels, see kda_fusion).
  *   - dk = dv = 128 only (the sources' 128 x 128 state); anything else
  *     returns KDA_ERR_UNSUPPORTED.
  *   - All tensors are dense, row-major, caller-owned DEVICE memory.  q, k,
  *     v, log_alpha, o and the states are 16-byte aligned; beta, cu_seqlens,
  *     state_indices and device_status 4-byte aligned; the prefill workspace
- *     256-byte aligned.  The library allocates nothing, keeps no state between
- *     calls, never synchronises the host, and enqueues all work on `stream`
- *     (a cudaStream_t; NULL = the legacy default stream).
+ *     256-byte aligned.  The library allocates no device memory, never
+ *     synchronises the host, and enqueues all work on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream).  The two-pass prefill
+ *     may also run part of its work on a library-owned stream per device
+ *     (created on first use), ordered with `stream` by events: the call's
+ *     work still completes before later work on `stream` starts.
  *   - Argument errors are returned synchronously before anything is
  *     enqueued.  Data-dependent errors found on the device are OR-ed into
  *     *device_status (if non-NULL) as KDA_DEV_* bits; the affected sequences
@@ -73,6 +77,35 @@ typedef enum {
 #define KDA_DEV_BAD_SLOT 0x2        /* state_indices entry outside [0, num_slots) */
 #define KDA_DEV_TIMEOUT 0x4         /* an on-chip wait hit its iteration limit */
 #define KDA_DEV_BAD_SNAPSHOT 0x8    /* kda_prefill_snapshots: a (sequence, position) entry is invalid */
+
+/*
+ * Fused prologue / epilogue (kda_prefill_ex, kda_decode_step_ex): the
+ * elementwise steps around the recurrence that "kimi delta attn from first
+ * principles" (aryagxr) lists -- q and k L2-normalised ("KDA Architecture"),
+ * the update gate beta as a sigmoid of its projection, and the output gate
+ * (RMSNorm of o_t, then an elementwise product with g_t) ("KDA has three
+ * gates").  Done inside the kernels, they save the caller a pass over HBM.
+ *
+ *   KDA_FUSE_L2NORM_QK   q, k <- x / sqrt(sum_c x_c^2 + l2_eps), per (token, head)
+ *   KDA_FUSE_BETA_SIGMOID  beta holds logits b; beta = 1 / (1 + exp(-b)) is used
+ *   KDA_FUSE_OUT_GATE    the output is y = o / sqrt(mean_c o_c^2 + rms_eps)
+ *                        * rms_weight * out_gate instead of o
+ *
+ * rms_weight: [dv] fp32 device (NULL = all ones); out_gate: [tokens, H, dv]
+ * in qkv_dtype, device, 16-byte aligned (required with KDA_FUSE_OUT_GATE;
+ * tokens = total_tokens for prefill, N for decode).  l2_eps, rms_eps >= 0.
+ * The state and S_final are those of the normalised q, k and sigmoid beta.
+ */
+#define KDA_FUSE_L2NORM_QK 0x1u
+#define KDA_FUSE_BETA_SIGMOID 0x2u
+#define KDA_FUSE_OUT_GATE 0x4u
+typedef struct {
+    uint32_t flags;
+    float l2_eps;
+    float rms_eps;
+    const float *rms_weight;
+    const void *out_gate;
+} kda_fusion;
 
 /* Version of this header the library was built from. */
 KDA_API int32_t kda_abi_version(void);
@@ -176,6 +209,20 @@ KDA_API kda_status kda_prefill_snapshots(const void *q, const void *k, const voi
                                  int32_t *device_status, kda_stream_t stream);
 
 /*
+ * kda_prefill_ex -- kda_prefill with the fused prologue / epilogue of
+ * `fusion` (host pointer; NULL or flags = 0 is kda_prefill).  With any flag
+ * set the two-pass workspace is required (>= kda_prefill_workspace_bytes),
+ * else KDA_ERR_WORKSPACE.  Unknown flags, a missing out_gate, or a negative
+ * eps return KDA_ERR_INVALID_ARG; out_gate overlapping o returns it too.
+ */
+KDA_API kda_status kda_prefill_ex(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                          const float *log_alpha, const float *beta, const float *S0,
+                          const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                          int32_t H, int32_t dk, int32_t dv, void *o, float *S_final,
+                          const kda_fusion *fusion, void *workspace, size_t workspace_bytes,
+                          int32_t *device_status, kda_stream_t stream);
+
+/*
  * kda_decode_step -- one fused recurrent step for N sequences
  * ("Understanding Kimi Delta Attention" (pyshine), section "The Chunkwise
  * DPLR Algorithm": the step-by-step "fused recurrent mode" for decode).
@@ -195,6 +242,17 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                            int32_t num_slots, const int32_t *state_indices, int32_t N,
                            int32_t H, int32_t dk, int32_t dv, void *o,
                            int32_t *device_status, kda_stream_t stream);
+
+/*
+ * kda_decode_step_ex -- kda_decode_step with the fused prologue / epilogue
+ * of `fusion` (host pointer; NULL or flags = 0 is kda_decode_step).  Errors
+ * as kda_prefill_ex; out_gate is [N, H, dv].
+ */
+KDA_API kda_status kda_decode_step_ex(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                              const float *log_alpha, const float *beta, float *S,
+                              int32_t num_slots, const int32_t *state_indices, int32_t N,
+                              int32_t H, int32_t dk, int32_t dv, void *o, const kda_fusion *fusion,
+                              int32_t *device_status, kda_stream_t stream);
 
 /*
  * kda_decode_multi -- T consecutive tokens per sequence in one launch: a

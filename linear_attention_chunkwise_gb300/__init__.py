@@ -14,15 +14,21 @@ from ._binding import (  # noqa: F401
     KDA_DEV_TIMEOUT,
     KDA_DTYPE_BF16,
     KDA_DTYPE_F32,
+    KDA_FUSE_BETA_SIGMOID,
+    KDA_FUSE_L2NORM_QK,
+    KDA_FUSE_OUT_GATE,
     KDA_ERR_CUDA,
     KDA_ERR_INVALID_ARG,
     KDA_ERR_UNSUPPORTED,
     KDA_ERR_WORKSPACE,
     KDA_OK,
+    Fusion,
     KdaError,
     kda_decode_multi,
     kda_decode_step,
+    kda_decode_step_ex,
     kda_prefill,
+    kda_prefill_ex,
     kda_prefill_min_workspace_bytes,
     kda_prefill_snapshots,
     kda_prefill_workspace_bytes,

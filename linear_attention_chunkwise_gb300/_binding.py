@@ -27,10 +27,40 @@ KDA_DEV_BAD_CU_SEQLENS = 0x1
 KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
 KDA_DEV_BAD_SNAPSHOT = 0x8
+KDA_FUSE_L2NORM_QK = 0x1
+KDA_FUSE_BETA_SIGMOID = 0x2
+KDA_FUSE_OUT_GATE = 0x4
+
+
+class _KdaFusion(ctypes.Structure):
+    """Mirror of the C struct kda_fusion (include/kda.h)."""
+    _fields_ = [("flags", ctypes.c_uint32), ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("rms_weight", ctypes.c_void_p), ("out_gate", ctypes.c_void_p)]
+
+
+class Fusion:
+    """Fused prologue / epilogue of the _ex entry points.
+
+    l2norm_qk: q, k <- x / sqrt(sum x^2 + l2_eps) per (token, head); beta_sigmoid: beta holds logits;
+    out_gate: [tokens, H, 128] tensor (dtype of q) -> output y = RMSNorm(o) * rms_weight * out_gate.
+    """
+
+    def __init__(self, l2norm_qk=False, beta_sigmoid=False, l2_eps=1e-6, out_gate=None, rms_weight=None,
+                 rms_eps=1e-6):
+        self.l2norm_qk, self.beta_sigmoid, self.l2_eps = l2norm_qk, beta_sigmoid, l2_eps
+        self.out_gate, self.rms_weight, self.rms_eps = out_gate, rms_weight, rms_eps
+
+    def c_struct(self):
+        flags = (KDA_FUSE_L2NORM_QK if self.l2norm_qk else 0) | (KDA_FUSE_BETA_SIGMOID if self.beta_sigmoid else 0)
+        if self.out_gate is not None:
+            flags |= KDA_FUSE_OUT_GATE
+        return _KdaFusion(flags, float(self.l2_eps), float(self.rms_eps),
+                          None if self.rms_weight is None else self.rms_weight.data_ptr(),
+                          None if self.out_gate is None else self.out_gate.data_ptr())
 
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
-                    "kda_prefill_noalloc", "kda_prefill_snapshots")
+                    "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +99,12 @@ def load_library(path: str | None = None):
         lib.kda_prefill_snapshots.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
                                               P, P, i32, P, P, sz, P, P]
         lib.kda_prefill_snapshots.restype = ctypes.c_int
+        FP = ctypes.POINTER(_KdaFusion)
+        lib.kda_prefill_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P, FP, P, sz,
+                                       P, P]
+        lib.kda_prefill_ex.restype = ctypes.c_int
+        lib.kda_decode_step_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, FP, P, P]
+        lib.kda_decode_step_ex.restype = ctypes.c_int
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -223,6 +259,80 @@ def kda_prefill_snapshots(q, k, v, log_alpha, beta, cu_seqlens, snap_seq, snap_p
     if st != KDA_OK:
         raise KdaError("kda_prefill_snapshots", st, kda_status_string(st))
     return o, S_final, S_snap
+
+
+def _check_fusion(fusion, q, tokens):
+    if fusion is None:
+        return None
+    if fusion.out_gate is not None:
+        _check(fusion.out_gate, "out_gate", q.dtype, q.device)
+        if tuple(fusion.out_gate.shape) != (tokens, q.shape[1], 128):
+            raise ValueError("out_gate must be [tokens, H, 128]")
+    if fusion.rms_weight is not None:
+        _check(fusion.rms_weight, "rms_weight", torch.float32, q.device)
+    return fusion.c_struct()
+
+
+def kda_prefill_ex(q, k, v, log_alpha, beta, cu_seqlens, S0=None, *, fusion=None, o=None, S_final=None,
+                   workspace=None, device_status=None, stream=None):
+    """kda_prefill with the fused prologue / epilogue of `fusion` (a Fusion); returns (o, S_final)."""
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    for t, n, dt in ((k, "k", q.dtype), (v, "v", q.dtype), (log_alpha, "log_alpha", torch.float32),
+                     (beta, "beta", torch.float32), (cu_seqlens, "cu_seqlens", torch.int32),
+                     (S0, "S0", torch.float32)):
+        _check(t, n, dt, dev)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    fz = _check_fusion(fusion, q, T)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if S_final is None:
+        S_final = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    _check(o, "o", q.dtype, dev)
+    _check(S_final, "S_final", torch.float32, dev)
+    need = int(lib.kda_prefill_workspace_bytes(code, N, T, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    st = lib.kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                            _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(o), _ptr(S_final),
+                            None if fz is None else ctypes.byref(fz), _ptr(workspace), workspace.numel(),
+                            _ptr(device_status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_ex", st, kda_status_string(st))
+    return o, S_final
+
+
+def kda_decode_step_ex(q, k, v, log_alpha, beta, S, state_indices=None, *, fusion=None, o=None,
+                       device_status=None, stream=None):
+    """kda_decode_step with the fused prologue / epilogue of `fusion` (a Fusion); returns o."""
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    for t, n, dt in ((k, "k", q.dtype), (v, "v", q.dtype), (log_alpha, "log_alpha", torch.float32),
+                     (beta, "beta", torch.float32), (S, "S", torch.float32),
+                     (state_indices, "state_indices", torch.int32)):
+        _check(t, n, dt, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    fz = _check_fusion(fusion, q, N)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    _check(o, "o", q.dtype, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    st = lib.kda_decode_step_ex(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S),
+                                S.shape[0], _ptr(state_indices), N, H, dk, dv, _ptr(o),
+                                None if fz is None else ctypes.byref(fz), _ptr(device_status),
+                                _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_decode_step_ex", st, kda_status_string(st))
+    return o
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None, device_status=None, stream=None):

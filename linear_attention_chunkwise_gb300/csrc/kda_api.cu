@@ -211,6 +211,24 @@ size_t kda_prefill_min_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, in
 
 namespace {
 
+// Fusion options: validated copy (flags 0 when `f` is NULL).  Returns false on
+// unknown flags, a negative eps, a missing / misaligned out_gate or weight.
+bool fusion_ok(const kda_fusion* f, kda::DecodeFusion& out) {
+    out = kda::DecodeFusion();
+    if (!f) return true;
+    constexpr uint32_t known = KDA_FUSE_L2NORM_QK | KDA_FUSE_BETA_SIGMOID | KDA_FUSE_OUT_GATE;
+    if (f->flags & ~known) return false;
+    if (!(f->l2_eps >= 0.f) || !(f->rms_eps >= 0.f)) return false;
+    if ((f->flags & KDA_FUSE_OUT_GATE) && (!f->out_gate || !aligned(f->out_gate, 16))) return false;
+    if (f->rms_weight && !aligned(f->rms_weight, 4)) return false;
+    out.flags = f->flags;
+    out.l2_eps = f->l2_eps;
+    out.rms_eps = f->rms_eps;
+    out.rms_weight = f->rms_weight;
+    out.out_gate = f->out_gate;
+    return true;
+}
+
 struct Snapshots {
     const int32_t* seq = nullptr;
     const int32_t* pos = nullptr;
@@ -221,9 +239,11 @@ struct Snapshots {
 kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
                         const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
                         int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
-                        const Snapshots& snap, void* workspace, size_t workspace_bytes, int32_t* device_status,
-                        kda_stream_t stream_) {
+                        const Snapshots& snap, const kda_fusion* fusion, void* workspace, size_t workspace_bytes,
+                        int32_t* device_status, kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    kda::DecodeFusion fz;
+    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -257,6 +277,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         if (!sizes_ok(snap.count, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
         if (!two_pass) return KDA_ERR_WORKSPACE;
     }
+    if (fz.flags && !two_pass) return KDA_ERR_WORKSPACE;
 
     // Overlap rules: outputs overlap nothing (S_final may equal S0 exactly).
     const Range r_o = range_of(o, nqk * es), r_sf = range_of(S_final, S_final ? nst * 4 : 0);
@@ -274,6 +295,11 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     if (have_tokens && (overlap(r_o, r_sf) || overlap(r_o, r_ws) || overlap(r_o, r_s0))) return KDA_ERR_INVALID_ARG;
     if (overlap(r_sf, r_ws) || overlap(r_s0, r_ws)) return KDA_ERR_INVALID_ARG;
     if (S0 && S_final && S0 != S_final && overlap(r_sf, r_s0)) return KDA_ERR_INVALID_ARG;
+    if (fz.flags & KDA_FUSE_OUT_GATE) {  // out_gate is read while o is written
+        const Range r_g = range_of(fz.out_gate, nqk * es);
+        if (have_tokens && overlap(r_g, r_o)) return KDA_ERR_INVALID_ARG;
+        if (overlap(r_g, r_sf) || overlap(r_g, r_ws)) return KDA_ERR_INVALID_ARG;
+    }
     if (snap.count > 0) {  // S_snap is an output: it overlaps nothing
         const Range r_ss = range_of(snap.S, static_cast<size_t>(snap.count) * H * kHeadDim * kHeadDim * 4);
         const Range r_sq = range_of(snap.seq, static_cast<size_t>(snap.count) * 4);
@@ -340,6 +366,11 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     a.snap_pos = snap.pos;
     a.num_snaps = snap.count;
     a.S_snap = snap.S;
+    a.fuse_flags = fz.flags;
+    a.l2_eps = fz.l2_eps;
+    a.rms_eps = fz.rms_eps;
+    a.rms_weight = fz.rms_weight;
+    a.out_gate = fz.out_gate;
     a.total_tokens = total_tokens;
     a.num_seqs = num_seqs;
     a.H = H;
@@ -399,7 +430,16 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, kda_dtype qk
                        int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
                        void* workspace, size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
     return prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv, o,
-                        S_final, Snapshots{}, workspace, workspace_bytes, device_status, stream);
+                        S_final, Snapshots{}, nullptr, workspace, workspace_bytes, device_status, stream);
+}
+
+kda_status kda_prefill_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                          const float* beta, const float* S0, const int32_t* cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t H, int32_t dk, int32_t dv, void* o, float* S_final,
+                          const kda_fusion* fusion, void* workspace, size_t workspace_bytes, int32_t* device_status,
+                          kda_stream_t stream) {
+    return prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv, o,
+                        S_final, Snapshots{}, fusion, workspace, workspace_bytes, device_status, stream);
 }
 
 kda_status kda_prefill_snapshots(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
@@ -414,14 +454,20 @@ kda_status kda_prefill_snapshots(const void* q, const void* k, const void* v, kd
     snap.count = num_snaps;
     snap.S = S_snap;
     return prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv, o,
-                        S_final, snap, workspace, workspace_bytes, device_status, stream);
+                        S_final, snap, nullptr, workspace, workspace_bytes, device_status, stream);
 }
 
-kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
-                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
-                           int32_t H, int32_t dk, int32_t dv, void* o, int32_t* device_status,
-                           kda_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+kda_status decode_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                       const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
+                       int32_t H, int32_t dk, int32_t dv, void* o, const kda_fusion* fusion, int32_t* device_status,
+                       kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    kda::DecodeFusion fz;
+    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -449,13 +495,37 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtyp
     for (const Range& in : inputs)
         if (overlap(r_o, in) || overlap(r_s, in)) return KDA_ERR_INVALID_ARG;
     if (overlap(r_o, r_s)) return KDA_ERR_INVALID_ARG;
+    if (fz.flags & KDA_FUSE_OUT_GATE) {
+        const Range r_g = range_of(fz.out_gate, nio * es);
+        if (overlap(r_g, r_o) || overlap(r_g, r_s)) return KDA_ERR_INVALID_ARG;
+    }
 
     const kda_status dev = check_device();
     if (dev != KDA_OK) return dev;
     if (kda::launch_decode(qkv_dtype == KDA_DTYPE_F32, q, k, v, log_alpha, beta, S, num_slots, state_indices, N, H,
-                           o, device_status, stream) != cudaSuccess)
+                           o, device_status, stream, fz) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
+                           int32_t H, int32_t dk, int32_t dv, void* o, int32_t* device_status,
+                           kda_stream_t stream) {
+    return decode_impl(q, k, v, qkv_dtype, log_alpha, beta, S, num_slots, state_indices, N, H, dk, dv, o, nullptr,
+                       device_status, stream);
+}
+
+kda_status kda_decode_step_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                              const float* log_alpha, const float* beta, float* S, int32_t num_slots,
+                              const int32_t* state_indices, int32_t N, int32_t H, int32_t dk, int32_t dv, void* o,
+                              const kda_fusion* fusion, int32_t* device_status, kda_stream_t stream) {
+    return decode_impl(q, k, v, qkv_dtype, log_alpha, beta, S, num_slots, state_indices, N, H, dk, dv, o, fusion,
+                       device_status, stream);
 }
 
 kda_status kda_decode_multi(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,

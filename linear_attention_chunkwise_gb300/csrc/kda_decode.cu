@@ -38,12 +38,16 @@ __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-template <typename IoT>
+// FUSED adds the prologue / epilogue of DecodeFusion: q, k L2-normalised,
+// beta = sigmoid(logit), output y = RMSNorm(o) * weight * gate (the three
+// gates of "kimi delta attn from first principles" (aryagxr), "KDA has three
+// gates", and its "KDA Architecture" L2 norm).
+template <typename IoT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     kda_decode_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k, const IoT* __restrict__ v,
                       const float* __restrict__ log_alpha, const float* __restrict__ beta, float* S,
                       int32_t num_slots, const int32_t* __restrict__ state_indices, int32_t H,
-                      IoT* __restrict__ o, int32_t* device_status) {
+                      IoT* __restrict__ o, int32_t* device_status, const DecodeFusion fz) {
     const int unit = blockIdx.x;
     const int n = unit / H;
     const int h = unit - n * H;
@@ -60,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ __align__(16) float red_y[kThreads / 32][kHeadDim];
     __shared__ __align__(16) float red_p[kThreads / 32][kHeadDim];
     __shared__ float kq_part[4];
+    __shared__ float kk_part[4], qq_part[4], oo_part[4];
 
     float* Sg = S + (static_cast<size_t>(slot) * H + h) * kHeadDim * kHeadDim;
     const int row0 = warp * kRowsPerWarp;
@@ -81,14 +86,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
         if (lane == 0) kq_part[warp] = kq;
+        if (FUSED && (fz.flags & KDA_FUSE_L2NORM_QK)) {
+            float k2 = kk * kk, q2 = qq * qq;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                k2 += __shfl_xor_sync(0xffffffffu, k2, off);
+                q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+            }
+            if (lane == 0) { kk_part[warp] = k2; qq_part[warp] = q2; }
+        }
     }
     __syncthreads();
+    // L2 norms of k and q (1 without the prologue); the rows below use k/|k|, q/|q|
+    float ik = 1.f, iq = 1.f;
+    if (FUSED && (fz.flags & KDA_FUSE_L2NORM_QK)) {
+        ik = rsqrtf(kk_part[0] + kk_part[1] + kk_part[2] + kk_part[3] + fz.l2_eps);
+        iq = rsqrtf(qq_part[0] + qq_part[1] + qq_part[2] + qq_part[3] + fz.l2_eps);
+    }
 
+    float o_val = 0.f;
     float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
         const int r = row0 + i;
-        const float a = a_s[r], kr = k_s[r], qr = q_s[r];
+        const float a = a_s[r], kr = k_s[r] * ik, qr = q_s[r] * iq;
         s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
         y.x = fmaf(kr, s[i].x, y.x); y.y = fmaf(kr, s[i].y, y.y);
         y.z = fmaf(kr, s[i].z, y.z); y.w = fmaf(kr, s[i].w, y.w);
@@ -106,18 +127,33 @@ __global__ void __launch_bounds__(kThreads, 2)
             yy += red_y[w][tid];
             pp += red_p[w][tid];
         }
-        const float b = beta[tok];
+        float b = beta[tok];
+        if (FUSED && (fz.flags & KDA_FUSE_BETA_SIGMOID)) b = 1.f / (1.f + expf(-b));
         const float u = b * (to_f32(v[tok * kHeadDim + tid]) - yy);
-        const float kq = kq_part[0] + kq_part[1] + kq_part[2] + kq_part[3];
+        const float kq = (kq_part[0] + kq_part[1] + kq_part[2] + kq_part[3]) * (ik * iq);
         u_s[tid] = u;
-        o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
+        o_val = fmaf(kq, u, pp);
+        if (FUSED && (fz.flags & KDA_FUSE_OUT_GATE)) {
+            float o2 = o_val * o_val;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) o2 += __shfl_xor_sync(0xffffffffu, o2, off);
+            if (lane == 0) oo_part[warp] = o2;
+        } else {
+            o[tok * kHeadDim + tid] = from_f32<IoT>(o_val);
+        }
     }
     __syncthreads();
+    if (FUSED && (fz.flags & KDA_FUSE_OUT_GATE) && tid < kHeadDim) {  // y = RMSNorm(o) * weight * gate
+        const float ms = (oo_part[0] + oo_part[1] + oo_part[2] + oo_part[3]) * (1.f / kHeadDim);
+        const float w = fz.rms_weight ? fz.rms_weight[tid] : 1.f;
+        const float g = to_f32(static_cast<const IoT*>(fz.out_gate)[tok * kHeadDim + tid]);
+        o[tok * kHeadDim + tid] = from_f32<IoT>(o_val * rsqrtf(ms + fz.rms_eps) * w * g);
+    }
 
     const float4 uu = reinterpret_cast<const float4*>(u_s)[lane];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-        const float kr = k_s[row0 + i];
+        const float kr = k_s[row0 + i] * ik;
         float4 t = s[i];
         t.x = fmaf(kr, uu.x, t.x); t.y = fmaf(kr, uu.y, t.y);
         t.z = fmaf(kr, uu.z, t.z); t.w = fmaf(kr, uu.w, t.w);
@@ -243,21 +279,29 @@ cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const
     return cudaGetLastError();
 }
 
+template <typename IoT, bool FUSED>
+void launch_decode_t(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta,
+                     float* S, int32_t num_slots, const int32_t* state_indices, int32_t H, void* o,
+                     int32_t* device_status, cudaStream_t stream, const DecodeFusion& fz, dim3 grid) {
+    kda_decode_kernel<IoT, FUSED><<<grid, kThreads, 0, stream>>>(
+        static_cast<const IoT*>(q), static_cast<const IoT*>(k), static_cast<const IoT*>(v), log_alpha, beta, S,
+        num_slots, state_indices, H, static_cast<IoT*>(o), device_status, fz);
+}
+
 cudaError_t launch_decode(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
-                          int32_t N, int32_t H, void* o, int32_t* device_status, cudaStream_t stream) {
+                          int32_t N, int32_t H, void* o, int32_t* device_status, cudaStream_t stream,
+                          const DecodeFusion& fusion) {
     const long long units = static_cast<long long>(N) * H;
     if (units == 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>(units));
+    const bool fused = fusion.flags != 0;
     if (f32_io) {
-        kda_decode_kernel<float><<<grid, kThreads, 0, stream>>>(
-            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), log_alpha,
-            beta, S, num_slots, state_indices, H, static_cast<float*>(o), device_status);
+        (fused ? launch_decode_t<float, true> : launch_decode_t<float, false>)(
+            q, k, v, log_alpha, beta, S, num_slots, state_indices, H, o, device_status, stream, fusion, grid);
     } else {
-        kda_decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-            static_cast<const __nv_bfloat16*>(v), log_alpha, beta, S, num_slots, state_indices, H,
-            static_cast<__nv_bfloat16*>(o), device_status);
+        (fused ? launch_decode_t<__nv_bfloat16, true> : launch_decode_t<__nv_bfloat16, false>)(
+            q, k, v, log_alpha, beta, S, num_slots, state_indices, H, o, device_status, stream, fusion, grid);
     }
     return cudaGetLastError();
 }

@@ -14,9 +14,16 @@ constexpr int kChunk = 64;   // chunk length of the prefill
 constexpr int kHeadDim = 128;  // dk = dv
 
 // ---- decode ----
+struct DecodeFusion {  // KDA_FUSE_* bits and their parameters (see kda_fusion)
+    uint32_t flags = 0;
+    float l2_eps = 0.f, rms_eps = 0.f;
+    const float* rms_weight = nullptr;
+    const void* out_gate = nullptr;
+};
 cudaError_t launch_decode(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                           const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
-                          int32_t N, int32_t H, void* o, int32_t* device_status, cudaStream_t stream);
+                          int32_t N, int32_t H, void* o, int32_t* device_status, cudaStream_t stream,
+                          const DecodeFusion& fusion = DecodeFusion());
 
 cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                                 const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
@@ -48,6 +55,13 @@ struct PrefillArgs {
     const int32_t* snap_pos = nullptr;
     int32_t num_snaps = 0;
     float* S_snap = nullptr;
+    // fused prologue (KDA_FUSE_* bits; pass 1 applies them) and epilogue
+    // (KDA_FUSE_OUT_GATE: pass 2 runs as 2-CTA clusters, one per (sequence, head))
+    uint32_t fuse_flags = 0;
+    float l2_eps = 0.f;
+    float rms_eps = 0.f;
+    const float* rms_weight = nullptr;
+    const void* out_gate = nullptr;
 };
 
 // Bytes per (chunk, head) of the two-pass path's operand images:

@@ -85,7 +85,7 @@ __device__ __forceinline__ float4 fma4(float s, const float4& a, const float4& a
 //   egm/egc/egcm[128] receive exp(gm), exp(gC), exp(gC - gm) per channel
 __device__ __forceinline__ void gate_chunk(const float* la_s, uint8_t* opa, uint8_t* opkb, int Lc, float* red,
                                            float* beta_s, float beta_cur, float* egm, float* egc, float* egcm,
-                                           int tid) {
+                                           int tid, const float* inv_norm = nullptr) {
     const int cp = tid & 63;  // channel pair (2cp, 2cp+1)
     const int rq = tid >> 6;  // rows 16rq .. 16rq+15
     float g0[16], g1[16];
@@ -130,10 +130,30 @@ __device__ __forceinline__ void gate_chunk(const float* la_s, uint8_t* opa, uint
         if (r < Lc) {
             kk = unpack_bf16(*reinterpret_cast<const uint32_t*>(opa + koff));
             qv = unpack_bf16(*reinterpret_cast<const uint32_t*>(opa + qoff));
+            if (inv_norm) {  // fused L2 normalisation of k and q rows
+                const float ik = inv_norm[r], iq = inv_norm[64 + r];
+                kk.x *= ik; kk.y *= ik; qv.x *= iq; qv.y *= iq;
+            }
         }
         *reinterpret_cast<uint32_t*>(opa + koff) = pack_bf16(kk.x * e0, kk.y * e1);
         *reinterpret_cast<uint32_t*>(opa + qoff) = pack_bf16(qv.x * e0, qv.y * e1);
         *reinterpret_cast<uint32_t*>(opkb + sw128_off(r, 2 * cp, 8192)) = pack_bf16(kk.x * f0, kk.y * f1);
+    }
+}
+
+// 1 / sqrt(|x|^2 + eps) of the 128 rows of an operand tile [2 blk][128 rows][128 B]
+// (rows 0..63 k, 64..127 q) into inv[128]; all NT threads, no barrier inside.
+__device__ __forceinline__ void row_inv_norms(const uint8_t* opa, float eps, float* inv, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * warp + i;
+        const uint2 w = *reinterpret_cast<const uint2*>(opa + sw128_off(r, 4 * lane, 16384));
+        const float2 a = unpack_bf16(w.x), b = unpack_bf16(w.y);
+        float ss = a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) inv[r] = rsqrtf(ss + eps);
     }
 }
 

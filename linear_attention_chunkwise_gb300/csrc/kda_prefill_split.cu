@@ -52,6 +52,50 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
                  "r"(smem_u32(src)), "r"(bytes)
                  : "memory");
 }
+// ---- 2-CTA cluster exchange (fused output gate) ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
@@ -135,7 +179,8 @@ struct PrepSmem {
     static constexpr uint32_t BETA = XS + 3072;  // f32 [64]
     static constexpr uint32_t RED = BETA + 256;  // f32 [4][128]
     static constexpr uint32_t EV = RED + 2048;   // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
-    static constexpr uint32_t BARS = EV + 1536;  // 3 x u64
+    static constexpr uint32_t INV = EV + 1536;   // f32 [128]: 1/|row| of k (0..63) and q (64..127)
+    static constexpr uint32_t BARS = INV + 512;  // 3 x u64
     static constexpr uint32_t TMEM_SLOT = BARS + 24;
     static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
@@ -194,7 +239,8 @@ __global__ void __launch_bounds__(NT, 2)
             tma_load_3d(sm + L::OP_A + kh * 16384 + 8192, &tm_q, &bars[1], 64 * kh, h, static_cast<int32_t>(t0));
         }
     }
-    const float beta_cur = (tid < Lc) ? p.beta[(t0 + tid) * H + h] : 0.f;
+    float beta_cur = (tid < Lc) ? p.beta[(t0 + tid) * H + h] : 0.f;
+    if ((p.fuse_flags & KDA_FUSE_BETA_SIGMOID) && tid < Lc) beta_cur = 1.f / (1.f + expf(-beta_cur));
     if (warp == 0) {
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
@@ -207,8 +253,13 @@ __global__ void __launch_bounds__(NT, 2)
     bool ok = mbar_wait(&bars[0], 0, kWaitLimit);
     ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
 
+    float* inv = nullptr;
+    if (p.fuse_flags & KDA_FUSE_L2NORM_QK) {  // read by gate_chunk after its internal barrier
+        inv = reinterpret_cast<float*>(sm + L::INV);
+        row_inv_norms(sm + L::OP_A, p.l2_eps, inv, tid);
+    }
     gate_chunk(reinterpret_cast<const float*>(sm + L::LA), sm + L::OP_A, sm + L::OP_KB, Lc,
-               reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev, ev + 128, ev + 256, tid);
+               reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev, ev + 128, ev + 256, tid, inv);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -302,15 +353,21 @@ struct ScanSmem {
     static constexpr uint32_t OP_SM = 2 * SET;   // [128 rows][128 B]: Sm slice
     static constexpr uint32_t OP_U = OP_SM + 16384;  // [64 rows][128 B]: U slice
     static constexpr uint32_t BARS = OP_U + 8192;    // 5 x u64: load0, load1, c1, c2, fin
-    static constexpr uint32_t TMEM_SLOT = BARS + 40;
+    static constexpr uint32_t RXBAR = BARS + 40;     // 2 x u64: peer's row partials landed (by chunk parity)
+    static constexpr uint32_t TMEM_SLOT = RXBAR + 16;
     static constexpr uint32_t ABORT = TMEM_SLOT + 4;
-    static constexpr uint32_t TOTAL = ABORT + 4;
+    static constexpr uint32_t OSQ = ABORT + 4;       // f32 [2][64]: sum of o^2 per O row, per column half
+    static constexpr uint32_t RX = OSQ + 512;        // f32 [2][64]: the peer CTA's row sums, by chunk parity
+    static constexpr uint32_t TOTAL = RX + 512;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
 static_assert(ScanSmem::ALLOC <= 232448, "scan shared memory over the per-CTA limit");
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 
-template <typename OutT>
+// OG (fused output gate): the two dv slices of a (sequence, head) run as one
+// 2-CTA cluster and swap per-row sums of o^2 through distributed shared
+// memory, so each writes y = o / sqrt(mean o^2 + eps) * weight * gate.
+template <typename OutT, bool OG>
 __global__ void __launch_bounds__(NT, 1)
     kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
     using L = ScanSmem;
@@ -389,9 +446,14 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
     volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
+    uint64_t* rxbar = reinterpret_cast<uint64_t*>(sm + L::RXBAR);
     if (tid == 0) {
         *abort_s = 0;
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        if (OG) {
+            mbar_init(&rxbar[0], 64);  // one arrive per O row of the peer
+            mbar_init(&rxbar[1], 64);
+        }
         fence_mbar_init();
         prefetch_tmap(&tm_v);
     }
@@ -409,6 +471,12 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t tq = tmem + tmem_lane(qw);
     constexpr uint32_t TM_X = 0;    // + 64 * parity
     constexpr uint32_t TM_DS = 128;
+    // fused output gate: peer CTA rank and the shared-memory addresses this CTA writes there
+    const uint32_t peer = OG ? (cluster_ctarank() ^ 1u) : 0u;
+    uint32_t ph_rx[2] = {0, 0};
+    float* osq = reinterpret_cast<float*>(sm + L::OSQ);
+    const float* rx = reinterpret_cast<const float*>(sm + L::RX);
+    if (OG) cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
 
     auto issue_loads = [&](int c) {
         uint8_t* set = sm + (c & 1) * L::SET;
@@ -535,6 +603,33 @@ __global__ void __launch_bounds__(NT, 1)
             float a[32];
             tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
             tmem_ld_wait();
+            if (OG) {
+                // row sum of o^2: this thread's 32 columns, the other column half of this CTA,
+                // then the peer CTA's 64 columns (written into this CTA's RX by the peer)
+                float ps = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ps = fmaf(a[e], a[e], ps);
+                osq[hw * 64 + rr] = ps;
+                bar_sync_named(1, 128);  // the four O warps
+                const float own = osq[rr] + osq[64 + rr];
+                if (hw == 0) {
+                    st_cluster_f32(mapa_shared(smem_u32(sm + L::RX + (b * 64 + rr) * 4), peer), own);
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&rxbar[b]), peer));
+                }
+                if (!mbar_wait_cluster(&rxbar[b], ph_rx[b], kWaitLimit)) *abort_s = 1;
+                ph_rx[b] ^= 1u;
+                const float tot = own + rx[b * 64 + rr];
+                const float sc = rsqrtf(tot * (1.f / D) + p.rms_eps);
+                bar_sync_named(1, 128);  // osq is rewritten next chunk
+                if (rr < Lc) {
+                    const int64_t row = (t0 + rr) * H + h;
+                    const OutT* g = static_cast<const OutT*>(p.out_gate) + row * D + j0 + 32 * hw;
+                    const float* w = p.rms_weight ? p.rms_weight + j0 + 32 * hw : nullptr;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        a[e] = a[e] * sc * (w ? w[e] : 1.f) * static_cast<float>(g[e]);
+                }
+            }
             if (rr < Lc) {
                 OutT* dst = static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + 32 * hw;
 #pragma unroll
@@ -558,6 +653,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+    if (OG) cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
 }
 
 template <typename K>
@@ -602,22 +698,37 @@ cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_
     return launch_chunk_scan(tm_v, a, out_f32, stream);
 }
 
+template <typename OutT, bool OG>
+cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigned ctas, cudaStream_t stream) {
+    static int configured[64];
+    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG>, ScanSmem::ALLOC, configured);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = ScanSmem::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (OG) {  // the two dv slices of a (sequence, head) are adjacent CTAs: one cluster
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG>, tm_v, a);
+}
+
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
-    static int cfg_scan_bf[64], cfg_scan_f[64];
-    cudaError_t err;
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
-    if (out_f32) {
-        err = set_smem(kda_chunk_scan_kernel<float>, ScanSmem::ALLOC, cfg_scan_f);
-        if (err != cudaSuccess) return err;
-        kda_chunk_scan_kernel<float><<<static_cast<unsigned>(scan_ctas), NT, ScanSmem::ALLOC, stream>>>(tm_v, a);
-    } else {
-        err = set_smem(kda_chunk_scan_kernel<__nv_bfloat16>, ScanSmem::ALLOC, cfg_scan_bf);
-        if (err != cudaSuccess) return err;
-        kda_chunk_scan_kernel<__nv_bfloat16>
-            <<<static_cast<unsigned>(scan_ctas), NT, ScanSmem::ALLOC, stream>>>(tm_v, a);
-    }
-    return cudaGetLastError();
+    const unsigned n = static_cast<unsigned>(scan_ctas);
+    const bool og = (a.fuse_flags & KDA_FUSE_OUT_GATE) != 0;
+    if (out_f32)
+        return og ? launch_scan_t<float, true>(tm_v, a, n, stream) : launch_scan_t<float, false>(tm_v, a, n, stream);
+    return og ? launch_scan_t<__nv_bfloat16, true>(tm_v, a, n, stream)
+              : launch_scan_t<__nv_bfloat16, false>(tm_v, a, n, stream);
 }
 
 }  // namespace kda

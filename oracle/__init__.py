@@ -123,3 +123,31 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, nthreads: i
     if rc != 0:
         raise ValueError("oracle_kda_decode_step: slot index out of range")
     return o
+
+
+# ------------------------------------------------------------------------
+# Prologue / epilogue around the recurrence (plain fp64 definitions).  From
+# "kimi delta attn from first principles" (aryagxr): q and k are
+# L2-normalised ("KDA Architecture"), the update gate beta is the sigmoid of
+# its projection, and the output gate multiplies RMSNorm(o_t) elementwise by
+# g_t ("KDA has three gates").  The pages fix no epsilon; both take one.
+
+def l2_normalize(x, eps: float = 0.0) -> np.ndarray:
+    """x / sqrt(sum_c x_c^2 + eps) over the last axis."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def sigmoid(b) -> np.ndarray:
+    """1 / (1 + exp(-b))."""
+    b = np.asarray(b, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-b))
+
+
+def rmsnorm_gate(o, g, w=None, eps: float = 0.0) -> np.ndarray:
+    """o / sqrt(mean_c o_c^2 + eps) * w * g over the last axis (w = ones when None)."""
+    o = np.asarray(o, dtype=np.float64)
+    y = o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    if w is not None:
+        y = y * np.asarray(w, dtype=np.float64)
+    return y * np.asarray(g, dtype=np.float64)

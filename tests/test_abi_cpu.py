@@ -125,6 +125,55 @@ def test_prefill_snapshots_rejects_bad_arguments(lib, over, expect):
     assert _snapshots(lib, **over) == expect
 
 
+def _prefill_ex(lib, fz, **over):
+    T, H, N = 128, 2, 1
+    tok = T * H * 128
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, o=BASE + 12 * tok, Sf=BASE + 14 * tok,
+             ws=BASE + 20 * tok, wsb=1 << 20, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill_ex(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]), P(a["S0"]),
+                              P(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"], P(a["o"]), P(a["Sf"]),
+                              ctypes.byref(fz), P(a["ws"]), a["wsb"], P(a["status"]), None)
+
+
+def _fusion(flags=0, l2_eps=1e-6, rms_eps=1e-6, w=None, g=None):
+    from linear_attention_chunkwise_gb300._binding import _KdaFusion
+    return _KdaFusion(flags, l2_eps, rms_eps, w, g)
+
+
+GATE = BASE + 40 * 128 * 2 * 128  # a gate buffer clear of every other fake range
+
+
+@pytest.mark.parametrize("fz,over,expect", [
+    (dict(flags=0x8), {}, kda.KDA_ERR_INVALID_ARG),                                  # unknown flag
+    (dict(flags=kda.KDA_FUSE_L2NORM_QK, l2_eps=-1.0), {}, kda.KDA_ERR_INVALID_ARG),   # negative eps
+    (dict(flags=kda.KDA_FUSE_OUT_GATE), {}, kda.KDA_ERR_INVALID_ARG),                 # no gate
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GATE + 8), {}, kda.KDA_ERR_INVALID_ARG),     # misaligned gate
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=BASE + 12 * 128 * 2 * 128), {}, kda.KDA_ERR_INVALID_ARG),  # gate = o
+    (dict(flags=kda.KDA_FUSE_L2NORM_QK), dict(wsb=4096), kda.KDA_ERR_WORKSPACE),      # single-pass workspace
+])
+def test_prefill_ex_rejects_bad_fusion(lib, fz, over, expect):
+    assert _prefill_ex(lib, _fusion(**fz), **over) == expect
+
+
+def test_decode_ex_rejects_bad_fusion(lib):
+    N, H = 4, 2
+    io = N * H * 128
+    P = _fake
+    fz = _fusion(flags=0x10)
+    st = lib.kda_decode_step_ex(P(BASE), P(BASE + 2 * io), P(BASE + 4 * io), 0, P(BASE + 6 * io),
+                                P(BASE + 10 * io), P(BASE + 20 * io), N, None, N, H, 128, 128, P(BASE + 12 * io),
+                                ctypes.byref(fz), None, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+    fz = _fusion(flags=kda.KDA_FUSE_OUT_GATE)  # gate missing
+    st = lib.kda_decode_step_ex(P(BASE), P(BASE + 2 * io), P(BASE + 4 * io), 0, P(BASE + 6 * io),
+                                P(BASE + 10 * io), P(BASE + 20 * io), N, None, N, H, 128, 128, P(BASE + 12 * io),
+                                ctypes.byref(fz), None, None)
+    assert st == kda.KDA_ERR_INVALID_ARG
+
+
 def _decode(lib, **over):
     N, H = 4, 2
     io = N * H * 128
