@@ -289,11 +289,54 @@ def bench_prefill(cx: Ctx, args):
     ev1.record(cx.stream)
     cx.barrier()
     e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+
+    # the same call with the fused prologue / epilogue, and with a state snapshot every 1024 tokens
+    g = torch.Generator(device=cx.dev).manual_seed(7 + cx.rank)
+    gate = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
+    wrms = torch.ones(D, dtype=torch.float32, device=cx.dev)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, out_gate=gate, rms_weight=wrms)
+    snap_pos = torch.arange(1024, T + 1, 1024, dtype=torch.int32, device=cx.dev)
+    snap_seq = torch.zeros_like(snap_pos)
+    ss = torch.empty((snap_pos.numel(), H, D, D), dtype=torch.float32, device=cx.dev)
+
+    def variant_us(fn, n=10):
+        for _ in range(3):
+            fn()
+        cx.barrier()
+        ev0.record(cx.stream)
+        for _ in range(n):
+            fn()
+        ev1.record(cx.stream)
+        cx.barrier()
+        return round(cx.max_over_ranks(ev0.elapsed_time(ev1) / n) * 1e3, 1)
+
+    variants = {
+        "plain_us": round(ms * 1e3, 1),
+        "fused_prologue_epilogue_us": variant_us(lambda: kda.kda_prefill_ex(
+            p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, fusion=fz, o=o, S_final=sf, workspace=work,
+            stream=cx.stream)),
+        "fused_prologue_only_us": variant_us(lambda: kda.kda_prefill_ex(
+            p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, fusion=kda.Fusion(l2norm_qk=True, beta_sigmoid=True),
+            o=o, S_final=sf, workspace=work, stream=cx.stream)),
+        "fused_epilogue_only_us": variant_us(lambda: kda.kda_prefill_ex(
+            p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, fusion=kda.Fusion(out_gate=gate, rms_weight=wrms),
+            o=o, S_final=sf, workspace=work, stream=cx.stream)),
+        "snapshots_every_1024_us": variant_us(lambda: kda.kda_prefill_snapshots(
+            p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, snap_seq, snap_pos, None, o=o, S_final=sf,
+            S_snap=ss, workspace=work, stream=cx.stream)),
+    }
+    del gate, ss
+    # kernels per call: schedule + chunk table + (prep + scan) per piece of 64 chunks when the scan
+    # leaves SMs idle (one sequence here), else one prep + one scan
+    chunks = -(-T // 64)
+    sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
+    pieces = -(-chunks // 64) if H * 2 <= sms else 1
     pk = cx.peaks
     return {
         "value": whole_job_mtok_s(T, cx.ws, ms),
         "ms": ms,
-        "launches": 2 * args.steps,  # schedule + prefill kernel per call
+        "launches": (2 + 2 * pieces) * args.steps,
+        "variants": variants,
         "tokens": T,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved_gbs / pk["hbm"], 4),
@@ -375,6 +418,28 @@ def bench_decode(cx: Ctx, args):
                                / (m_ms * 1e-3) / 1e9 / cx.peaks["hbm"], 4)}
     del dm, mq, mk, mv, mla, mb, mo
 
+    # decode step with the fused prologue / epilogue (L2 norm of q, k; sigmoid beta; RMSNorm x gate)
+    gate = torch.randn(od[0].shape, device=cx.dev).to(od.dtype)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, out_gate=gate,
+                    rms_weight=torch.ones(D, dtype=torch.float32, device=cx.dev))
+
+    def fused_step():
+        kda.kda_decode_step_ex(d.q[0], d.k[0], d.v[0], d.log_alpha[0], d.beta[0], d.S, None, fusion=fz, o=od[0],
+                               stream=cx.stream)
+
+    for _ in range(3):
+        fused_step()
+    cx.barrier()
+    ev0.record(cx.stream)
+    for _ in range(50):
+        fused_step()
+    ev1.record(cx.stream)
+    cx.barrier()
+    f_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / 50)
+    fused = {"us_per_step": round(f_ms * 1e3, 2),
+             "state_gbs": round(cx.ws * n_units * 2 * STATE_BYTES / (f_ms * 1e-3) / 1e9, 1)}
+    del gate
+
     # end to end: each step's inputs H2D from pinned memory and its o D2H; the states stay in HBM
     names = ("q", "k", "v", "log_alpha", "beta")
     hq = [getattr(d, n)[0].cpu().pin_memory() for n in names]
@@ -415,6 +480,7 @@ def bench_decode(cx: Ctx, args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         "multi_token": multi,
+        "fused_prologue_epilogue": fused,
     }
 
 
@@ -438,7 +504,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (404 MB read per step), no flush",
                        "parallelism": f"independent problem per GPU x{cx.ws}"},
             "roofline": pf["roofline"], "tensor": pf["tensor"], "e2e": pf["e2e"],
-            "gpu_launches": pf["launches"], "clocks": pf["clocks"],
+            "gpu_launches": pf["launches"], "clocks": pf["clocks"], "prefill_variants": pf["variants"],
         })
     if dc is not None:
         out["decode"] = dc

@@ -349,6 +349,13 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         !make_map(&tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_tokens ? static_cast<const void*>(log_alpha) : dummy,
                   kHeadDim, Hh, T, kHeadDim, kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
         return KDA_ERR_CUDA;
+    // output gate [T, H, dv] in the dtype of o, read by the scan in 128-byte boxes (64 bf16 / 32 fp32 columns)
+    CUtensorMap tm_g;
+    const bool og = (fz.flags & KDA_FUSE_OUT_GATE) != 0;
+    if (og && !make_map(&tm_g, qkv_dtype == KDA_DTYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        es, have_tokens ? fz.out_gate : dummy, kHeadDim, Hh, T, qkv_dtype == KDA_DTYPE_F32 ? 32 : 64,
+                        kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+        return KDA_ERR_CUDA;
 
     if (kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -388,7 +395,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
             cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
             ps = piece_streams();
         if (!ps)
-            return kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, a, max_chunks(num_seqs, total_tokens), out_f32,
+            return kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, og ? &tm_g : nullptr, a,
+                                             max_chunks(num_seqs, total_tokens), out_f32,
                                              stream) == cudaSuccess
                        ? KDA_OK
                        : KDA_ERR_CUDA;
@@ -409,7 +417,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
                      cudaSuccess &&
                  cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
                  cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess &&
-                 kda::launch_chunk_scan(tm_v, a, out_f32, ps->scan) == cudaSuccess;
+                 kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, ps->scan) == cudaSuccess;
         }
         // join even after a failed launch so later work on `stream` stays ordered
         const bool joined = cudaEventRecord(ps->scan_done, ps->scan) == cudaSuccess &&

@@ -64,30 +64,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit_cycles) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (clock64() - t0 > limit_cycles) return false;
-    }
-    return true;
+// Asynchronous 4-byte store into a peer CTA's shared memory that counts its bytes on the peer's
+// mbarrier (complete_tx), the way a TMA load does: the reader needs no release / acquire fences.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar_addr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(bar_addr)
+                 : "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -96,6 +78,23 @@ __device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Bounded spin on an mbarrier phase with test_wait (never suspends the thread): for phases that
+// complete from another CTA, where a suspended try_wait may sleep past the completion.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > limit_cycles) return false;
+    }
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
@@ -360,7 +359,14 @@ struct ScanSmem {
     static constexpr uint32_t RX = OSQ + 512;        // f32 [2][64]: the peer CTA's row sums, by chunk parity
     static constexpr uint32_t TOTAL = RX + 512;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
+    // fused output gate only: the gate tiles of two chunks (TMA, 128B-swizzled rows of 128 B:
+    // one 64-column box for bf16, two 32-column boxes for fp32) and their barriers
+    static constexpr uint32_t GATE = (TOTAL + 1023) / 1024 * 1024;
+    static constexpr uint32_t GBAR = GATE + 2 * 16384;
+    static constexpr uint32_t WRMS = GBAR + 16;      // f32 [64]: RMSNorm weight of this CTA's columns
+    static constexpr uint32_t ALLOC_OG = WRMS + 256 + 1024;
 };
+static_assert(ScanSmem::ALLOC_OG <= 232448, "scan shared memory (output gate) over the per-CTA limit");
 static_assert(ScanSmem::ALLOC <= 232448, "scan shared memory over the per-CTA limit");
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 
@@ -369,7 +375,8 @@ constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 // memory, so each writes y = o / sqrt(mean o^2 + eps) * weight * gate.
 template <typename OutT, bool OG>
 __global__ void __launch_bounds__(NT, 1)
-    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
+    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                          const PrefillArgs p) {
     using L = ScanSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -447,16 +454,22 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
     volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
     uint64_t* rxbar = reinterpret_cast<uint64_t*>(sm + L::RXBAR);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(sm + L::GBAR);
     if (tid == 0) {
         *abort_s = 0;
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         if (OG) {
-            mbar_init(&rxbar[0], 64);  // one arrive per O row of the peer
-            mbar_init(&rxbar[1], 64);
+            mbar_init(&rxbar[0], 1);  // this CTA's arrive.expect_tx + the peer's 64 async stores
+            mbar_init(&rxbar[1], 1);
+            mbar_init(&gbar[0], 1);
+            mbar_init(&gbar[1], 1);
+            prefetch_tmap(&tm_g);
         }
         fence_mbar_init();
         prefetch_tmap(&tm_v);
     }
+    if (OG && tid < NV)
+        reinterpret_cast<float*>(sm + L::WRMS)[tid] = p.rms_weight ? p.rms_weight[slice * NV + tid] : 1.f;
     for (int e = tid; e < 2 * 512; e += NT)  // zero rows of both [Tb | 0 | M] tiles
         reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp == 0) {
@@ -498,6 +511,54 @@ __global__ void __launch_bounds__(NT, 1)
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
         if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
         ph ^= 1u;
+    };
+    // fused output gate: y = o / sqrt(mean o^2 + eps) * weight * gate for chunk cf, whose O rows sit in
+    // X[cf & 1] and whose row sums are own_pending (this CTA) + RX[cf & 1] (the peer's)
+    float own_pending = 0.f;
+    float o_pend[32];  // the O row of the chunk awaiting its output gate (this thread's 32 columns)
+    // gate tile of chunk cf -> GATE[cf & 1] (issued by tid 64 one step before og_finish(cf) reads it)
+    constexpr int kGateBoxes = static_cast<int>(sizeof(OutT) / 2);  // 128-byte boxes per 64 columns
+    uint32_t ph_g[2] = {0, 0};
+    int gate_pending = -1;  // tid 64: the chunk whose gate load is in flight and not yet consumed
+    auto issue_gate = [&](int cf) {
+        uint64_t* bar = &gbar[cf & 1];
+        mbar_arrive_expect_tx(bar, kGateBoxes * 8192);
+        const int32_t z = static_cast<int32_t>(t_begin + static_cast<int64_t>(cf) * C);
+#pragma unroll
+        for (int bx = 0; bx < kGateBoxes; ++bx)
+            tma_load_3d(sm + L::GATE + (cf & 1) * 16384 + bx * 8192, &tm_g, bar, j0 + bx * (64 / kGateBoxes), h, z);
+        gate_pending = cf;
+    };
+    auto og_finish = [&](int cf, int rr) {
+        const int bf = cf & 1;
+        if (tid == 64) mbar_arrive_expect_tx(&rxbar[bf], 64 * 4);  // the peer's 64 row sums
+        if (!mbar_spin(&rxbar[bf], ph_rx[bf], kWaitLimit)) *abort_s = 1;
+        ph_rx[bf] ^= 1u;
+        const float sc = rsqrtf((own_pending + rx[bf * 64 + rr]) * (1.f / D) + p.rms_eps);
+        float* a = o_pend;
+        const int64_t tf = t_begin + static_cast<int64_t>(cf) * C;
+        if (!mbar_wait(&gbar[bf], ph_g[bf], kWaitLimit)) *abort_s = 1;
+        ph_g[bf] ^= 1u;
+        if (tid == 64) gate_pending = -1;
+        if (tf + rr < t_end) {
+            const int64_t row = (tf + rr) * H + h;
+            // this thread's 32 gate values: 64 bytes (bf16, chunks 4hw..4hw+3 of the one box) or
+            // 128 bytes (fp32, box hw): 16-byte chunks of a 128B-swizzled row
+            uint4 gv[4 * kGateBoxes];
+            const uint8_t* grow = sm + L::GATE + bf * 16384 + (kGateBoxes == 2 ? hw * 8192 : 0);
+#pragma unroll
+            for (int i = 0; i < 4 * kGateBoxes; ++i) {
+                const int chunk = kGateBoxes == 2 ? i : 4 * hw + i;
+                gv[i] = *reinterpret_cast<const uint4*>(grow + sw128_chunk(rr, chunk));
+            }
+            const OutT* g = reinterpret_cast<const OutT*>(gv);
+            const float* w = reinterpret_cast<const float*>(sm + L::WRMS) + 32 * hw;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = a[e] * sc * w[e] * static_cast<float>(g[e]);
+            OutT* dst = static_cast<OutT*>(p.o) + row * static_cast<int64_t>(D) + j0 + 32 * hw;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
+        }
     };
     const uint64_t d_sm = sdesc_sw128(smem_u32(sm + L::OP_SM), 8192, 1024);
     const uint64_t d_u = sdesc_sw128(smem_u32(sm + L::OP_U), 8192, 1024);
@@ -600,44 +661,42 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (qw >= 2) {  // O rows -> global
             const int rr = 32 * (qw - 2) + lane;
-            float a[32];
-            tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
-            tmem_ld_wait();
             if (OG) {
-                // row sum of o^2: this thread's 32 columns, the other column half of this CTA,
-                // then the peer CTA's 64 columns (written into this CTA's RX by the peer)
+                // fused output gate, one chunk behind: finish chunk c-1 (its O rows are still in
+                // X[(c-1)&1] and the peer's row sums have had a whole step to arrive), then send
+                // this chunk's row sums of o^2 to the peer without waiting
+                if (c > 0) og_finish(c - 1, rr);
+                if (tid == 64) issue_gate(c);
+                tmem_ld32(tq + TM_X + 64 * b + 32 * hw, o_pend);
+                tmem_ld_wait();
                 float ps = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ps = fmaf(a[e], a[e], ps);
+                for (int e = 0; e < 32; ++e) ps = fmaf(o_pend[e], o_pend[e], ps);
                 osq[hw * 64 + rr] = ps;
                 bar_sync_named(1, 128);  // the four O warps
-                const float own = osq[rr] + osq[64 + rr];
-                if (hw == 0) {
-                    st_cluster_f32(mapa_shared(smem_u32(sm + L::RX + (b * 64 + rr) * 4), peer), own);
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&rxbar[b]), peer));
-                }
-                if (!mbar_wait_cluster(&rxbar[b], ph_rx[b], kWaitLimit)) *abort_s = 1;
-                ph_rx[b] ^= 1u;
-                const float tot = own + rx[b * 64 + rr];
-                const float sc = rsqrtf(tot * (1.f / D) + p.rms_eps);
-                bar_sync_named(1, 128);  // osq is rewritten next chunk
+                own_pending = osq[rr] + osq[64 + rr];
+                if (hw == 0)
+                    st_async_cluster_f32(mapa_shared(smem_u32(sm + L::RX + (b * 64 + rr) * 4), peer), own_pending,
+                                         mapa_shared(smem_u32(&rxbar[b]), peer));
+            } else {
+                float a[32];
+                tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
+                tmem_ld_wait();
                 if (rr < Lc) {
-                    const int64_t row = (t0 + rr) * H + h;
-                    const OutT* g = static_cast<const OutT*>(p.out_gate) + row * D + j0 + 32 * hw;
-                    const float* w = p.rms_weight ? p.rms_weight + j0 + 32 * hw : nullptr;
+                    OutT* dst =
+                        static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + 32 * hw;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        a[e] = a[e] * sc * (w ? w[e] : 1.f) * static_cast<float>(g[e]);
+                    for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
                 }
-            }
-            if (rr < Lc) {
-                OutT* dst = static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + 32 * hw;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
             }
         }
         tc_fence_before();
     }
+    __syncthreads();
+    if (OG && qw >= 2 && *abort_s == 0)  // the last chunk's output gate
+        og_finish(nch - 1, 32 * (qw - 2) + lane);
+    if (OG && tid == 64 && gate_pending >= 0)  // a wind-down left a gate copy in flight: let it land
+        (void)mbar_wait(&gbar[gate_pending & 1], ph_g[gate_pending & 1], kWaitLimit);
     __syncthreads();
     const bool ok = *abort_s == 0;
     if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
@@ -691,22 +750,24 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 }
 
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap& tm_la, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
-                                 cudaStream_t stream) {
+                                 const CUtensorMap& tm_la, const CUtensorMap* tm_g, const PrefillArgs& a,
+                                 int64_t max_chunks, bool out_f32, cudaStream_t stream) {
     const cudaError_t err = launch_chunk_prep(tm_q, tm_k, tm_la, a, max_chunks, stream);
     if (err != cudaSuccess) return err;
-    return launch_chunk_scan(tm_v, a, out_f32, stream);
+    return launch_chunk_scan(tm_v, tm_g, a, out_f32, stream);
 }
 
 template <typename OutT, bool OG>
-cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigned ctas, cudaStream_t stream) {
+cudaError_t launch_scan_t(const CUtensorMap& tm_v, const CUtensorMap& tm_g, const PrefillArgs& a, unsigned ctas,
+                          cudaStream_t stream) {
     static int configured[64];
-    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG>, ScanSmem::ALLOC, configured);
+    const uint32_t smem = OG ? ScanSmem::ALLOC_OG : ScanSmem::ALLOC;
+    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG>, smem, configured);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = ScanSmem::ALLOC;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (OG) {  // the two dv slices of a (sequence, head) are adjacent CTAs: one cluster
@@ -717,18 +778,22 @@ cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigne
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG>, tm_v, a);
+    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG>, tm_v, tm_g, a);
 }
 
-cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
+                              cudaStream_t stream) {
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
     const unsigned n = static_cast<unsigned>(scan_ctas);
     const bool og = (a.fuse_flags & KDA_FUSE_OUT_GATE) != 0;
+    if (og && !tm_g) return cudaErrorInvalidValue;
+    const CUtensorMap& g = og ? *tm_g : tm_v;  // unused without the output gate
     if (out_f32)
-        return og ? launch_scan_t<float, true>(tm_v, a, n, stream) : launch_scan_t<float, false>(tm_v, a, n, stream);
-    return og ? launch_scan_t<__nv_bfloat16, true>(tm_v, a, n, stream)
-              : launch_scan_t<__nv_bfloat16, false>(tm_v, a, n, stream);
+        return og ? launch_scan_t<float, true>(tm_v, g, a, n, stream)
+                  : launch_scan_t<float, false>(tm_v, g, a, n, stream);
+    return og ? launch_scan_t<__nv_bfloat16, true>(tm_v, g, a, n, stream)
+              : launch_scan_t<__nv_bfloat16, false>(tm_v, g, a, n, stream);
 }
 
 }  // namespace kda
