@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(NT, 1)
     constexpr uint32_t TM_DS = 128;
     // fused output gate: peer CTA rank and the shared-memory addresses this CTA writes there
     const uint32_t peer = OG ? (cluster_ctarank() ^ 1u) : 0u;
-    uint32_t ph_rx[2] = {0, 0};
+    uint32_t ph_rx = 0;  // phase parity of rxbar[i] in bit i (registers, not a runtime-indexed array)
     float* osq = reinterpret_cast<float*>(sm + L::OSQ);
     const float* rx = reinterpret_cast<const float*>(sm + L::RX);
     if (OG) cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(NT, 1)
         issue_loads(0);
         if (nch > 1) issue_loads(1);
     }
-    uint32_t ph_load[2] = {0, 0}, ph_c1 = 0, ph_c2 = 0;
+    uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] in bit i
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
         if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
         ph ^= 1u;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(NT, 1)
     float o_pend[32];  // the O row of the chunk awaiting its output gate (this thread's 32 columns)
     // gate tile of chunk cf -> GATE[cf & 1] (issued by tid 64 one step before og_finish(cf) reads it)
     constexpr int kGateBoxes = static_cast<int>(sizeof(OutT) / 2);  // 128-byte boxes per 64 columns
-    uint32_t ph_g[2] = {0, 0};
+    uint32_t ph_g = 0;  // parity of gbar[i] in bit i
     int gate_pending = -1;  // tid 64: the chunk whose gate load is in flight and not yet consumed
     auto issue_gate = [&](int cf) {
         uint64_t* bar = &gbar[cf & 1];
@@ -532,13 +532,13 @@ __global__ void __launch_bounds__(NT, 1)
     auto og_finish = [&](int cf, int rr) {
         const int bf = cf & 1;
         if (tid == 64) mbar_arrive_expect_tx(&rxbar[bf], 64 * 4);  // the peer's 64 row sums
-        if (!mbar_spin(&rxbar[bf], ph_rx[bf], kWaitLimit)) *abort_s = 1;
-        ph_rx[bf] ^= 1u;
+        if (!mbar_spin(&rxbar[bf], (ph_rx >> bf) & 1u, kWaitLimit)) *abort_s = 1;
+        ph_rx ^= 1u << bf;
         const float sc = rsqrtf((own_pending + rx[bf * 64 + rr]) * (1.f / D) + p.rms_eps);
         float* a = o_pend;
         const int64_t tf = t_begin + static_cast<int64_t>(cf) * C;
-        if (!mbar_wait(&gbar[bf], ph_g[bf], kWaitLimit)) *abort_s = 1;
-        ph_g[bf] ^= 1u;
+        if (!mbar_wait(&gbar[bf], (ph_g >> bf) & 1u, kWaitLimit)) *abort_s = 1;
+        ph_g ^= 1u << bf;
         if (tid == 64) gate_pending = -1;
         if (tf + rr < t_end) {
             const int64_t row = (tf + rr) * H + h;
@@ -569,7 +569,8 @@ __global__ void __launch_bounds__(NT, 1)
         const float* evs = reinterpret_cast<const float*>(set + L::S_EV);
         const int64_t t0 = t_begin + static_cast<int64_t>(c) * C;
         const int Lc = static_cast<int>(t_end - t0 < C ? t_end - t0 : C);
-        wait_bar(&bars[b], ph_load[b]);
+        if (!mbar_wait(&bars[b], (ph_load >> b) & 1u, kWaitLimit)) *abort_s = 1;
+        ph_load ^= 1u << b;
         if (Lc < C) {  // rows of v past the sequence end -> 0
             for (int e = tid; e < (C - Lc) * 8; e += NT) {
                 const int r = Lc + (e >> 3);
@@ -696,7 +697,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (OG && qw >= 2 && *abort_s == 0)  // the last chunk's output gate
         og_finish(nch - 1, 32 * (qw - 2) + lane);
     if (OG && tid == 64 && gate_pending >= 0)  // a wind-down left a gate copy in flight: let it land
-        (void)mbar_wait(&gbar[gate_pending & 1], ph_g[gate_pending & 1], kWaitLimit);
+        (void)mbar_wait(&gbar[gate_pending & 1], (ph_g >> (gate_pending & 1)) & 1u, kWaitLimit);
     __syncthreads();
     const bool ok = *abort_s == 0;
     if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
