@@ -226,6 +226,26 @@ class Ctx:
         return E(enable_timing=True), E(enable_timing=True)
 
 
+def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.25):
+    """(pass-1 launches, scan launches) of the library's piecewise prefill schedule for one sequence
+    of seq_chunks chunks: scan pieces of max(min_piece, ceil(n / max_pieces)) chunks, pass 1 a lead
+    of sq + lag * sq * (pieces - 1) chunks, then equal shares."""
+    sq = max(min_piece, -(-seq_chunks // max_pieces))
+    pieces = -(-seq_chunks // sq)
+    if pieces <= 1:
+        return 1, 1
+    lead = min(seq_chunks, sq + int(lag * sq * (pieces - 1) + 0.999))
+    share = (seq_chunks - lead + pieces - 2) // (pieces - 1)
+    prepared, n_prep = 0, 0
+    for j in range(pieces):
+        scan_end = min(seq_chunks, (j + 1) * sq)
+        prep_end = max(lead if j == 0 else min(seq_chunks, lead + j * share), scan_end)
+        if prep_end > prepared:
+            n_prep += 1
+            prepared = prep_end
+    return n_prep, pieces
+
+
 def bench_prefill(cx: Ctx, args):
     """Prefill on the 8k workload: device-resident timing, then end to end from pinned host memory."""
     torch = cx.torch
@@ -326,16 +346,15 @@ def bench_prefill(cx: Ctx, args):
             S_snap=ss, workspace=work, stream=cx.stream)),
     }
     del gate, ss
-    # kernels per call: schedule + chunk table + (prep + scan) per piece of 64 chunks when the scan
-    # leaves SMs idle (one sequence here), else one prep + one scan
-    chunks = -(-T // 64)
+    # kernels per call: schedule + chunk table + the pass-1 and scan launches of the piecewise
+    # schedule (one sequence here, so the scan leaves SMs idle), else one prep + one scan
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
-    pieces = -(-chunks // 64) if H * 2 <= sms else 1
+    n_prep, n_scan = piecewise_launches(-(-T // 64)) if H * 2 <= sms else (1, 1)
     pk = cx.peaks
     return {
         "value": whole_job_mtok_s(T, cx.ws, ms),
         "ms": ms,
-        "launches": (2 + 2 * pieces) * args.steps,
+        "launches": (2 + n_prep + n_scan) * args.steps,
         "variants": variants,
         "tokens": T,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -56,16 +57,21 @@ int sm_count() {
 }
 
 // Piecewise schedule of the two-pass prefill.  When the scan has fewer CTAs
-// than the GPU has SMs (few sequences), the chunks are processed in pieces of
-// kPieceChunks (64) per sequence: pass 1 of piece i+1 runs on the SMs the scan of
-// piece i leaves idle, and pass 2 reads operand images that pass 1 wrote
-// moments earlier (still in L2).  Pass 1 stays on the caller's stream; pass 2
-// runs on a library-owned high-priority stream per device, ordered by events,
-// and the caller's stream waits for the last scan before the call returns.
-// Pass 1 of piece i+1 is held back (a stream wait on a counter the scan CTAs
-// bump as they start) until every scan CTA of piece i is resident, so the
-// prep CTAs cannot take the SMs the scan needs.
-constexpr int kPieceChunks = 64;
+// than the GPU has SMs (few sequences), the scan runs in pieces of 48 or more
+// chunks per sequence (at most 32 pieces) and pass 1 runs ahead of it: a first
+// pass-1 launch prepares a lead of chunks on the whole GPU, and each later one
+// prepares its share while the previous scan piece runs on the SMs it leaves
+// idle (pass 2 then reads images written moments earlier, still in L2).  Pass 1
+// stays on the caller's stream; pass 2 runs on a library-owned high-priority
+// stream per device, ordered by events, and the caller's stream waits for the
+// last scan before the call returns.  A later pass-1 launch is held back (a
+// stream wait on a counter the scan CTAs bump as they start) until every CTA of
+// the running scan piece is resident, so prep CTAs cannot take the SMs the scan
+// needs.  Each piece boundary costs a few microseconds (launch, state carry,
+// first copies), which bounds the piece count.
+constexpr int64_t kScanPieceChunks = 48;  // smallest scan piece (chunks per sequence); each piece costs a few us
+constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
+constexpr double kPrepLag = 0.25;          // lead of pass 1, as a fraction of the chunks scanned after piece 0
 
 struct PieceStreams {
     std::mutex mu;  // one call at a time enqueues record/wait pairs on these
@@ -386,9 +392,10 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, reinterpret_cast<int32_t*>(ws + two.table),
                                     device_status, snap.seq, snap.pos, snap.count, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
-        // chunks of the longest possible sequence bound the number of pieces
+        // chunks of the longest possible sequence bound the pieces
         const int64_t seq_chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
-        const int64_t pieces = (seq_chunks + kPieceChunks - 1) / kPieceChunks;
+        const int64_t sq = std::max<int64_t>(kScanPieceChunks, (seq_chunks + kMaxScanPieces - 1) / kMaxScanPieces);
+        const int64_t pieces = (seq_chunks + sq - 1) / sq;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         PieceStreams* ps = nullptr;
         if (S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
@@ -400,24 +407,40 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
                                              stream) == cudaSuccess
                        ? KDA_OK
                        : KDA_ERR_CUDA;
+        // Scan piece j covers chunks [j sq, (j+1) sq).  Pass 1 runs ahead: its first piece prepares a
+        // lead of L0 chunks on the whole GPU, then its piece j (j >= 1) prepares the next share of the
+        // rest while scan piece j-1 runs; scan piece j starts once pass-1 pieces 0..j are done.
+        // L0 makes up for pass 1 being slower on the SMs the scan leaves than the scan is per chunk.
+        const int64_t lead = std::min<int64_t>(
+            seq_chunks, sq + static_cast<int64_t>(kPrepLag * static_cast<double>(sq * (pieces - 1)) + 0.999));
+        const int64_t share = (seq_chunks - lead + pieces - 2) / (pieces - 1);
         std::lock_guard<std::mutex> g(ps->mu);
         auto wait_value = wait_value_fn();
         uint32_t* started = reinterpret_cast<uint32_t*>(ws + two.table) + num_seqs + 2;
         const uint32_t scan_ctas = static_cast<uint32_t>(num_seqs) * H * 2;
         bool ok = !wait_value || cudaMemsetAsync(started, 0, 4, stream) == cudaSuccess;
-        a.piece_len = kPieceChunks;
         a.started = wait_value ? started : nullptr;
-        for (int64_t i = 0; i < pieces && ok; ++i) {
-            a.piece_begin = static_cast<int32_t>(i * kPieceChunks);
-            if (i > 0 && wait_value)
-                ok = wait_value(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(started),
-                                static_cast<cuuint32_t>(i * scan_ctas), CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
-            ok = ok &&
-                 kda::launch_chunk_prep(tm_q, tm_k, tm_la, a, static_cast<int64_t>(num_seqs) * kPieceChunks, stream) ==
-                     cudaSuccess &&
-                 cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
-                 cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess &&
-                 kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, ps->scan) == cudaSuccess;
+        int64_t prepared = 0;  // chunks [0, prepared) of every sequence have their images
+        for (int64_t j = 0; j < pieces && ok; ++j) {
+            const int64_t scan_end = std::min(seq_chunks, (j + 1) * sq);
+            int64_t prep_end = j == 0 ? lead : std::min(seq_chunks, lead + j * share);
+            prep_end = std::max(prep_end, scan_end);
+            if (prep_end > prepared) {
+                if (j > 0 && wait_value)  // pass 1 starts once every CTA of scan piece j-1 is resident
+                    ok = wait_value(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(started),
+                                    static_cast<cuuint32_t>(j * scan_ctas), CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
+                a.piece_begin = static_cast<int32_t>(prepared);
+                a.piece_len = static_cast<int32_t>(prep_end - prepared);
+                ok = ok &&
+                     kda::launch_chunk_prep(tm_q, tm_k, tm_la, a, static_cast<int64_t>(num_seqs) * a.piece_len,
+                                            stream) == cudaSuccess &&
+                     cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
+                     cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess;
+                prepared = prep_end;
+            }
+            a.piece_begin = static_cast<int32_t>(j * sq);
+            a.piece_len = static_cast<int32_t>(scan_end - j * sq);
+            ok = ok && kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, ps->scan) == cudaSuccess;
         }
         // join even after a failed launch so later work on `stream` stays ordered
         const bool joined = cudaEventRecord(ps->scan_done, ps->scan) == cudaSuccess &&
