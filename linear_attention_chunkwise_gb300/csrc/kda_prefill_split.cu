@@ -52,6 +52,14 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
                  "r"(smem_u32(src)), "r"(bytes)
                  : "memory");
 }
+// PC consecutive TMEM columns of this thread's lane (32x32b shape): 32 or 16.
+template <int PC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* r) {
+    static_assert(PC == 32 || PC == 16, "32 or 16 columns");
+    if (PC == 32) tmem_ld32(taddr, r);
+    else tmem_ld16(taddr, r);
+}
+
 // ---- 2-CTA cluster exchange (fused output gate) ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -373,15 +381,20 @@ constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 // OG (fused output gate): the two dv slices of a (sequence, head) run as one
 // 2-CTA cluster and swap per-row sums of o^2 through distributed shared
 // memory, so each writes y = o / sqrt(mean o^2 + eps) * weight * gate.
-template <typename OutT, bool OG>
-__global__ void __launch_bounds__(NT, 1)
+// NTS threads in NTS/128 column groups (256: two groups of 32 state columns per thread; 512: four
+// of 16).  Thread (warp w): lane quarter qw = w % 4 (state rows 32 qw + lane, the TMEM lanes it may
+// read), column group cq = w / 4.
+template <typename OutT, bool OG, int NTS>
+__global__ void __launch_bounds__(NTS, 1)
     kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                           const PrefillArgs p) {
     using L = ScanSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qw = warp & 3, hw = warp >> 2;
+    constexpr int CQ = NTS / 128;  // column groups
+    constexpr int PC = NV / CQ;    // state columns per thread
+    const int qw = warp & 3, cq = warp >> 2;
     const int H = p.H, N = p.num_seqs;
     const int32_t* co = p.chunk_off;
     constexpr int NSLICE = D / NV;
@@ -427,24 +440,24 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t seq_len = static_cast<int64_t>(p.cu_seqlens[seq + 1]) - p.cu_seqlens[seq];
     int next_snap = si < se ? p.snap_pos[si] : INT_MAX;
 
-    // state: row rho, columns [j0 + 32*hw, +32)
+    // state: row rho, columns [j0 + PC*cq, +PC)
     const int rho = 32 * qw + lane;
-    float S[32];
-    const size_t srow = ((static_cast<size_t>(seq) * H + h) * D + rho) * D + j0 + 32 * hw;
+    float S[PC];
+    const size_t srow = ((static_cast<size_t>(seq) * H + h) * D + rho) * D + j0 + PC * cq;
     if (S_in) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < PC; j += 4) {
             const float4 t = *reinterpret_cast<const float4*>(S_in + srow + j);
             S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = 0.f;
+        for (int j = 0; j < PC; ++j) S[j] = 0.f;
     }
     if (nch == 0) {
         if (p.S_final) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
+            for (int j = 0; j < PC; j += 4)
                 *reinterpret_cast<float4*>(p.S_final + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
         return;
@@ -470,7 +483,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (OG && tid < NV)
         reinterpret_cast<float*>(sm + L::WRMS)[tid] = p.rms_weight ? p.rms_weight[slice * NV + tid] : 1.f;
-    for (int e = tid; e < 2 * 512; e += NT)  // zero rows of both [Tb | 0 | M] tiles
+    for (int e = tid; e < 2 * 512; e += NTS)  // zero rows of both [Tb | 0 | M] tiles
         reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp == 0) {
         tmem_alloc(tmem_slot, 256);
@@ -515,7 +528,7 @@ __global__ void __launch_bounds__(NT, 1)
     // fused output gate: y = o / sqrt(mean o^2 + eps) * weight * gate for chunk cf, whose O rows sit in
     // X[cf & 1] and whose row sums are own_pending (this CTA) + RX[cf & 1] (the peer's)
     float own_pending = 0.f;
-    float o_pend[32];  // the O row of the chunk awaiting its output gate (this thread's 32 columns)
+    float o_pend[PC];  // the O row of the chunk awaiting its output gate (this thread's PC columns)
     // gate tile of chunk cf -> GATE[cf & 1] (issued by tid 64 one step before og_finish(cf) reads it)
     constexpr int kGateBoxes = static_cast<int>(sizeof(OutT) / 2);  // 128-byte boxes per 64 columns
     uint32_t ph_g = 0;  // parity of gbar[i] in bit i
@@ -542,22 +555,23 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 64) gate_pending = -1;
         if (tf + rr < t_end) {
             const int64_t row = (tf + rr) * H + h;
-            // this thread's 32 gate values: 64 bytes (bf16, chunks 4hw..4hw+3 of the one box) or
-            // 128 bytes (fp32, box hw): 16-byte chunks of a 128B-swizzled row
-            uint4 gv[4 * kGateBoxes];
-            const uint8_t* grow = sm + L::GATE + bf * 16384 + (kGateBoxes == 2 ? hw * 8192 : 0);
+            // this thread's PC gate values (columns c0 .. c0+PC-1 of the slice): 16-byte chunks of a
+            // 128B-swizzled 128-byte row (one 64-column box for bf16, two 32-column boxes for fp32)
+            constexpr int kPerChunk = static_cast<int>(16 / sizeof(OutT));
+            constexpr int kBoxCols = 64 / kGateBoxes;
+            const int c0 = PC * cq;
+            uint4 gv[PC / kPerChunk];
+            const uint8_t* grow = sm + L::GATE + bf * 16384 + (c0 / kBoxCols) * 8192;
 #pragma unroll
-            for (int i = 0; i < 4 * kGateBoxes; ++i) {
-                const int chunk = kGateBoxes == 2 ? i : 4 * hw + i;
-                gv[i] = *reinterpret_cast<const uint4*>(grow + sw128_chunk(rr, chunk));
-            }
+            for (int i = 0; i < PC / kPerChunk; ++i)
+                gv[i] = *reinterpret_cast<const uint4*>(grow + sw128_chunk(rr, (c0 % kBoxCols) / kPerChunk + i));
             const OutT* g = reinterpret_cast<const OutT*>(gv);
-            const float* w = reinterpret_cast<const float*>(sm + L::WRMS) + 32 * hw;
+            const float* w = reinterpret_cast<const float*>(sm + L::WRMS) + c0;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = a[e] * sc * w[e] * static_cast<float>(g[e]);
-            OutT* dst = static_cast<OutT*>(p.o) + row * static_cast<int64_t>(D) + j0 + 32 * hw;
+            for (int e = 0; e < PC; ++e) a[e] = a[e] * sc * w[e] * static_cast<float>(g[e]);
+            OutT* dst = static_cast<OutT*>(p.o) + row * static_cast<int64_t>(D) + j0 + c0;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
+            for (int ch = 0; ch < PC / 8; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
         }
     };
     const uint64_t d_sm = sdesc_sw128(smem_u32(sm + L::OP_SM), 8192, 1024);
@@ -572,19 +586,19 @@ __global__ void __launch_bounds__(NT, 1)
         if (!mbar_wait(&bars[b], (ph_load >> b) & 1u, kWaitLimit)) *abort_s = 1;
         ph_load ^= 1u << b;
         if (Lc < C) {  // rows of v past the sequence end -> 0
-            for (int e = tid; e < (C - Lc) * 8; e += NT) {
+            for (int e = tid; e < (C - Lc) * 8; e += NTS) {
                 const int r = Lc + (e >> 3);
                 *reinterpret_cast<uint4*>(set + L::S_V + sw128_chunk(r, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks 4hw..4hw+3)
+        {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks PC*cq/8 ..)
             const float sc = evs[rho];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < PC / 8; ++ch) {
                 float m8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) m8[e] = sc * S[8 * ch + e];
-                *reinterpret_cast<uint4*>(sm + L::OP_SM + sw128_chunk(rho, 4 * hw + ch)) = pack8(m8);
+                *reinterpret_cast<uint4*>(sm + L::OP_SM + sw128_chunk(rho, PC * cq / 8 + ch)) = pack8(m8);
             }
         }
         fence_async_smem();
@@ -613,14 +627,14 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 32 && c >= 1 && c + 1 < nch) issue_loads(c + 1);
         wait_bar(&bars[2], ph_c1);
         tc_fence_after();
-        if (qw < 2) {  // U -> OP_U (row r, chunks 4hw..4hw+3)
+        if (qw < 2) {  // U -> OP_U (row r, chunks PC*cq/8 ..)
             const int r = 32 * qw + lane;
-            float a[32];
-            tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
+            float a[PC];
+            tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
             tmem_ld_wait();
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                *reinterpret_cast<uint4*>(sm + L::OP_U + sw128_chunk(r, 4 * hw + ch)) = pack8(a + 8 * ch);
+            for (int ch = 0; ch < PC / 8; ++ch)
+                *reinterpret_cast<uint4*>(sm + L::OP_U + sw128_chunk(r, PC * cq / 8 + ch)) = pack8(a + 8 * ch);
         }
         fence_async_smem();
         tc_fence_before();
@@ -641,19 +655,19 @@ __global__ void __launch_bounds__(NT, 1)
         tc_fence_after();
         {
             const float dc = evs[128 + rho], dcm = evs[256 + rho];
-            float a[32];
-            tmem_ld32(tq + TM_DS + 32 * hw, a);
+            float a[PC];
+            tmem_ld_cols<PC>(tq + TM_DS + PC * cq, a);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) S[e] = fmaf(dc, S[e], dcm * a[e]);
+            for (int e = 0; e < PC; ++e) S[e] = fmaf(dc, S[e], dcm * a[e]);
         }
         {  // state snapshots at the end of this chunk (positions are sequence-relative)
             const int64_t done = min(static_cast<int64_t>(cb + c + 1) * C, seq_len);
             while (next_snap <= done) {
                 if (next_snap == done) {
-                    float* dst = p.S_snap + ((static_cast<size_t>(si) * H + h) * D + rho) * D + j0 + 32 * hw;
+                    float* dst = p.S_snap + ((static_cast<size_t>(si) * H + h) * D + rho) * D + j0 + PC * cq;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
+                    for (int j = 0; j < PC; j += 4)
                         *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
                 }
                 ++si;
@@ -668,26 +682,28 @@ __global__ void __launch_bounds__(NT, 1)
                 // this chunk's row sums of o^2 to the peer without waiting
                 if (c > 0) og_finish(c - 1, rr);
                 if (tid == 64) issue_gate(c);
-                tmem_ld32(tq + TM_X + 64 * b + 32 * hw, o_pend);
+                tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, o_pend);
                 tmem_ld_wait();
                 float ps = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ps = fmaf(o_pend[e], o_pend[e], ps);
-                osq[hw * 64 + rr] = ps;
-                bar_sync_named(1, 128);  // the four O warps
-                own_pending = osq[rr] + osq[64 + rr];
-                if (hw == 0)
+                for (int e = 0; e < PC; ++e) ps = fmaf(o_pend[e], o_pend[e], ps);
+                osq[cq * 64 + rr] = ps;
+                bar_sync_named(1, 64 * CQ);  // the O warps
+                own_pending = 0.f;
+#pragma unroll
+                for (int q2 = 0; q2 < CQ; ++q2) own_pending += osq[q2 * 64 + rr];
+                if (cq == 0)
                     st_async_cluster_f32(mapa_shared(smem_u32(sm + L::RX + (b * 64 + rr) * 4), peer), own_pending,
                                          mapa_shared(smem_u32(&rxbar[b]), peer));
             } else {
-                float a[32];
-                tmem_ld32(tq + TM_X + 64 * b + 32 * hw, a);
+                float a[PC];
+                tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
                 tmem_ld_wait();
                 if (rr < Lc) {
                     OutT* dst =
-                        static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + 32 * hw;
+                        static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + PC * cq;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
+                    for (int ch = 0; ch < PC / 8; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
                 }
             }
         }
@@ -707,7 +723,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (p.S_final && ok) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
+        for (int j = 0; j < PC; j += 4)
             *reinterpret_cast<float4*>(p.S_final + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     tc_fence_before();
@@ -761,13 +777,14 @@ cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_
 template <typename OutT, bool OG>
 cudaError_t launch_scan_t(const CUtensorMap& tm_v, const CUtensorMap& tm_g, const PrefillArgs& a, unsigned ctas,
                           cudaStream_t stream) {
+    constexpr int NTS = 256;  // 512 threads (16 columns each) measured no faster: the chunk is not epilogue-bound
     static int configured[64];
     const uint32_t smem = OG ? ScanSmem::ALLOC_OG : ScanSmem::ALLOC;
-    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG>, smem, configured);
+    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG, NTS>, smem, configured);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(NT);
+    cfg.blockDim = dim3(NTS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -779,7 +796,7 @@ cudaError_t launch_scan_t(const CUtensorMap& tm_v, const CUtensorMap& tm_g, cons
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG>, tm_v, tm_g, a);
+    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG, NTS>, tm_v, tm_g, a);
 }
 
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,

@@ -173,3 +173,24 @@ def test_prefill_config4_long_two_heads():
     g = torch.Generator().manual_seed(4)
     heads = [sorted(torch.randperm(p.q.shape[1], generator=g)[:2].tolist())]
     check_against_oracle(p, o, sf, heads)
+
+
+@pytest.mark.parametrize("alias", [False, True])
+def test_prefill_piecewise_two_sequences(alias):
+    # two sequences of different lengths, few heads: the scan runs piecewise (pass 1 ahead of it
+    # on another stream); the short sequence ends inside the first piece, the long one spans four.
+    # With alias, S_final is S0 itself (the carry between pieces then lives in S0's memory).
+    p = synth.prefill_inputs([7000, 3500], 4, s0_std=0.02, seed=631, device="cuda")
+    S0_copy = p.S0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sf_out = p.S0 if alias else None
+    o, sf = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, S_final=sf_out,
+                            device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    p.S0 = S0_copy  # the oracle starts from the original states
+    check_against_oracle(p, o, sf, [[0, 3], [1, 2]])
+    # the same batch in one launch pair (no S_final -> no piecewise schedule) gives the same o
+    o1, _ = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, S0_copy, return_final=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o1)
