@@ -164,9 +164,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 // T consecutive tokens per sequence in one launch (a speculative-decoding
 // verify step, or a short prefill): the state stays in registers across the
 // tokens, so it is read once and written once per launch.  The per-token
-// arithmetic is the single-step kernel's, token after token.  The small
-// per-token vectors are double-buffered by token parity so one barrier at the
-// top of each token separates its writes from the previous token's reads.
+// arithmetic is the single-step kernel's, token after token.  The inputs of up
+// to kTokBatch tokens are fetched into shared memory up front (together with
+// the state read), so no token waits on a global load: each token costs two
+// block barriers (column partial sums, then u).
+constexpr int kTokBatch = 8;
+
 template <typename IoT>
 __global__ void __launch_bounds__(kThreads, 2)
     kda_decode_multi_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k, const IoT* __restrict__ v,
@@ -184,11 +187,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     }
 
-    __shared__ float a_s[2][kHeadDim], k_s[2][kHeadDim], q_s[2][kHeadDim];
-    __shared__ __align__(16) float u_s[2][kHeadDim];
+    __shared__ float a_s[kTokBatch][kHeadDim], k_s[kTokBatch][kHeadDim], q_s[kTokBatch][kHeadDim];
+    __shared__ float v_s[kTokBatch][kHeadDim], b_s[kTokBatch];
+    __shared__ __align__(16) float u_s[kHeadDim];
     __shared__ __align__(16) float red_y[kThreads / 32][kHeadDim];
     __shared__ __align__(16) float red_p[kThreads / 32][kHeadDim];
-    __shared__ float kq_part[2][4];
+    __shared__ float kq_part[4];
 
     float* Sg = S + (static_cast<size_t>(slot) * H + h) * kHeadDim * kHeadDim;
     const int row0 = warp * kRowsPerWarp;
@@ -197,59 +201,67 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int i = 0; i < kRowsPerWarp; ++i)
         s[i] = __ldcs(reinterpret_cast<const float4*>(Sg + static_cast<size_t>(row0 + i) * kHeadDim) + lane);
 
-    for (int t = 0; t < T; ++t) {
-        const int b = t & 1;
-        const size_t tok = (static_cast<size_t>(n) * T + t) * H + h;
-        if (tid < kHeadDim) {
-            const float kk = to_f32(k[tok * kHeadDim + tid]);
-            const float qq = to_f32(q[tok * kHeadDim + tid]);
-            k_s[b][tid] = kk;
-            q_s[b][tid] = qq;
-            a_s[b][tid] = expf(log_alpha[tok * kHeadDim + tid]);
-            float kq = kk * qq;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-            if (lane == 0) kq_part[b][warp] = kq;
+    for (int tb0 = 0; tb0 < T; tb0 += kTokBatch) {
+        const int nb = min(kTokBatch, T - tb0);
+        if (tb0 > 0) __syncthreads();  // the previous batch's vectors are no longer read
+        for (int e = tid; e < nb * kHeadDim; e += kThreads) {
+            const int tt = e / kHeadDim, ch = e - tt * kHeadDim;
+            const size_t tok = (static_cast<size_t>(n) * T + tb0 + tt) * H + h;
+            k_s[tt][ch] = to_f32(k[tok * kHeadDim + ch]);
+            q_s[tt][ch] = to_f32(q[tok * kHeadDim + ch]);
+            a_s[tt][ch] = expf(log_alpha[tok * kHeadDim + ch]);
+            v_s[tt][ch] = to_f32(v[tok * kHeadDim + ch]);
         }
+        if (tid < nb) b_s[tid] = beta[(static_cast<size_t>(n) * T + tb0 + tid) * H + h];
         __syncthreads();
 
-        float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
+        for (int tt = 0; tt < nb; ++tt) {
+            const int t = tb0 + tt;
+            const size_t tok = (static_cast<size_t>(n) * T + t) * H + h;
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const int r = row0 + i;
-            const float a = a_s[b][r], kr = k_s[b][r], qr = q_s[b][r];
-            s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
-            y.x = fmaf(kr, s[i].x, y.x); y.y = fmaf(kr, s[i].y, y.y);
-            y.z = fmaf(kr, s[i].z, y.z); y.w = fmaf(kr, s[i].w, y.w);
-            p.x = fmaf(qr, s[i].x, p.x); p.y = fmaf(qr, s[i].y, p.y);
-            p.z = fmaf(qr, s[i].z, p.z); p.w = fmaf(qr, s[i].w, p.w);
-        }
-        reinterpret_cast<float4*>(red_y[warp])[lane] = y;
-        reinterpret_cast<float4*>(red_p[warp])[lane] = p;
-        __syncthreads();
-
-        if (tid < kHeadDim) {
-            float yy = 0.f, pp = 0.f;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
-                yy += red_y[w][tid];
-                pp += red_p[w][tid];
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const int r = row0 + i;
+                const float a = a_s[tt][r], kr = k_s[tt][r], qr = q_s[tt][r];
+                s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+                y.x = fmaf(kr, s[i].x, y.x); y.y = fmaf(kr, s[i].y, y.y);
+                y.z = fmaf(kr, s[i].z, y.z); y.w = fmaf(kr, s[i].w, y.w);
+                p.x = fmaf(qr, s[i].x, p.x); p.y = fmaf(qr, s[i].y, p.y);
+                p.z = fmaf(qr, s[i].z, p.z); p.w = fmaf(qr, s[i].w, p.w);
             }
-            const float u = beta[tok] * (to_f32(v[tok * kHeadDim + tid]) - yy);
-            const float kq = kq_part[b][0] + kq_part[b][1] + kq_part[b][2] + kq_part[b][3];
-            u_s[b][tid] = u;
-            o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
-        }
-        __syncthreads();
-
-        const float4 uu = reinterpret_cast<const float4*>(u_s[b])[lane];
-        float* Ss = S_steps ? S_steps + tok * kHeadDim * kHeadDim : nullptr;
+            reinterpret_cast<float4*>(red_y[warp])[lane] = y;
+            reinterpret_cast<float4*>(red_p[warp])[lane] = p;
+            if (tid < kHeadDim) {
+                float kq = k_s[tt][tid] * q_s[tt][tid];
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const float kr = k_s[b][row0 + i];
-            s[i].x = fmaf(kr, uu.x, s[i].x); s[i].y = fmaf(kr, uu.y, s[i].y);
-            s[i].z = fmaf(kr, uu.z, s[i].z); s[i].w = fmaf(kr, uu.w, s[i].w);
-            if (Ss) __stcs(reinterpret_cast<float4*>(Ss + static_cast<size_t>(row0 + i) * kHeadDim) + lane, s[i]);
+                for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                if (lane == 0) kq_part[warp] = kq;
+            }
+            __syncthreads();
+
+            if (tid < kHeadDim) {
+                float yy = 0.f, pp = 0.f;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    yy += red_y[w][tid];
+                    pp += red_p[w][tid];
+                }
+                const float u = b_s[tt] * (v_s[tt][tid] - yy);
+                const float kq = kq_part[0] + kq_part[1] + kq_part[2] + kq_part[3];
+                u_s[tid] = u;
+                o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
+            }
+            __syncthreads();
+
+            const float4 uu = reinterpret_cast<const float4*>(u_s)[lane];
+            float* Ss = S_steps ? S_steps + tok * kHeadDim * kHeadDim : nullptr;
+#pragma unroll
+            for (int i = 0; i < kRowsPerWarp; ++i) {
+                const float kr = k_s[tt][row0 + i];
+                s[i].x = fmaf(kr, uu.x, s[i].x); s[i].y = fmaf(kr, uu.y, s[i].y);
+                s[i].z = fmaf(kr, uu.z, s[i].z); s[i].w = fmaf(kr, uu.w, s[i].w);
+                if (Ss) __stcs(reinterpret_cast<float4*>(Ss + static_cast<size_t>(row0 + i) * kHeadDim) + lane, s[i]);
+            }
         }
     }
 #pragma unroll
