@@ -194,3 +194,24 @@ def test_prefill_piecewise_two_sequences(alias):
     o1, _ = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, S0_copy, return_final=False)
     torch.cuda.synchronize()
     assert torch.equal(o, o1)
+
+
+def test_prefill_in_cuda_graph():
+    # under stream capture the library runs one prep + one scan on the capturing stream (no
+    # library-owned stream); the replayed graph gives the eager result bit for bit
+    p = synth.prefill_inputs([5000, 300], 2, s0_std=0.02, seed=641, device="cuda")
+    o_ref, sf_ref = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0)
+    T, H, _ = p.q.shape
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(torch.bfloat16, 2, T, H), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(o_ref)
+    sf = torch.empty_like(sf_ref)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf, workspace=ws,
+                        stream=s)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(sf, sf_ref)
