@@ -79,9 +79,10 @@ typedef enum {
 #define KDA_DEV_BAD_SNAPSHOT 0x8    /* kda_prefill_snapshots: a (sequence, position) entry is invalid */
 
 /*
- * Fused prologue / epilogue (kda_prefill_ex, kda_decode_step_ex): the
- * elementwise steps around the recurrence that "kimi delta attn from first
- * principles" (aryagxr) lists -- q and k L2-normalised ("KDA Architecture"),
+ * Fused prologue / epilogue (kda_prefill_ex, kda_decode_step_ex,
+ * kda_decode_multi_ex): the elementwise steps around the recurrence that
+ * "kimi delta attn from first principles" (aryagxr) lists -- q and k
+ * L2-normalised ("KDA Architecture"),
  * the update gate beta as a sigmoid of its projection, and the output gate
  * (RMSNorm of o_t, then an elementwise product with g_t) ("KDA has three
  * gates").  Done inside the kernels, they save the caller a pass over HBM.
@@ -93,7 +94,8 @@ typedef enum {
  *
  * rms_weight: [dv] fp32 device (NULL = all ones); out_gate: [tokens, H, dv]
  * in qkv_dtype, device, 16-byte aligned (required with KDA_FUSE_OUT_GATE;
- * tokens = total_tokens for prefill, N for decode).  l2_eps, rms_eps >= 0.
+ * tokens = total_tokens for prefill, N for a decode step, N x T for
+ * kda_decode_multi_ex).  l2_eps, rms_eps >= 0.
  * The state and S_final are those of the normalised q, k and sigmoid beta.
  */
 #define KDA_FUSE_L2NORM_QK 0x1u
@@ -278,6 +280,17 @@ KDA_API kda_status kda_decode_multi(const void *q, const void *k, const void *v,
                                     int32_t num_slots, const int32_t *state_indices, int32_t N,
                                     int32_t T, int32_t H, int32_t dk, int32_t dv, void *o,
                                     float *S_steps, int32_t *device_status, kda_stream_t stream);
+
+/*
+ * kda_decode_multi_ex -- kda_decode_multi with the fused prologue / epilogue
+ * of `fusion` per token (host pointer; NULL or flags = 0 is kda_decode_multi).
+ * Errors as kda_prefill_ex; out_gate is [N, T, H, dv].
+ */
+KDA_API kda_status kda_decode_multi_ex(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                               const float *log_alpha, const float *beta, float *S,
+                               int32_t num_slots, const int32_t *state_indices, int32_t N,
+                               int32_t T, int32_t H, int32_t dk, int32_t dv, void *o, float *S_steps,
+                               const kda_fusion *fusion, int32_t *device_status, kda_stream_t stream);
 
 /*
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     Fusion,
     KdaError,
     kda_decode_multi,
+    kda_decode_multi_ex,
     kda_decode_step,
     kda_decode_step_ex,
     kda_prefill,

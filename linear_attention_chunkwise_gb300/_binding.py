@@ -60,7 +60,8 @@ class Fusion:
 
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
-                    "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex")
+                    "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex",
+                    "kda_decode_multi_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -105,6 +106,9 @@ def load_library(path: str | None = None):
         lib.kda_prefill_ex.restype = ctypes.c_int
         lib.kda_decode_step_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, FP, P, P]
         lib.kda_decode_step_ex.restype = ctypes.c_int
+        lib.kda_decode_multi_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P,
+                                            FP, P, P]
+        lib.kda_decode_multi_ex.restype = ctypes.c_int
         lib.kda_prefill.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -373,6 +377,19 @@ def kda_decode_multi(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None,
     state_indices: int32 [N] or None.  Returns o [N, T, H, 128], or (o, S_steps) when
     return_steps (S_steps [N, T, H, 128, 128] fp32: the state after each token).
     """
+    return _decode_multi(q, k, v, log_alpha, beta, S, state_indices, None, o, S_steps, return_steps,
+                         device_status, stream)
+
+
+def kda_decode_multi_ex(q, k, v, log_alpha, beta, S, state_indices=None, *, fusion=None, o=None, S_steps=None,
+                        return_steps=False, device_status=None, stream=None):
+    """kda_decode_multi with the fused prologue / epilogue of `fusion` (a Fusion; out_gate [N, T, H, 128])."""
+    return _decode_multi(q, k, v, log_alpha, beta, S, state_indices, fusion, o, S_steps, return_steps,
+                         device_status, stream)
+
+
+def _decode_multi(q, k, v, log_alpha, beta, S, state_indices, fusion, o, S_steps, return_steps, device_status,
+                  stream):
     lib = load_library()
     dev = q.device
     _check(q, "q", device=dev)
@@ -394,9 +411,23 @@ def kda_decode_multi(q, k, v, log_alpha, beta, S, state_indices=None, *, o=None,
     if S_steps is None and return_steps:
         S_steps = torch.empty((N, T, H, dk, dv), dtype=torch.float32, device=dev)
     _check(S_steps, "S_steps", torch.float32, dev)
-    st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S), S.shape[0],
-                              _ptr(state_indices), N, T, H, dk, dv, _ptr(o), _ptr(S_steps), _ptr(device_status),
-                              _stream_handle(stream))
+    if fusion is None:
+        st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S),
+                                  S.shape[0], _ptr(state_indices), N, T, H, dk, dv, _ptr(o), _ptr(S_steps),
+                                  _ptr(device_status), _stream_handle(stream))
+        name = "kda_decode_multi"
+    else:
+        if fusion.out_gate is not None and tuple(fusion.out_gate.shape) != (N, T, H, dv):
+            raise ValueError("out_gate must be [N, T, H, 128]")
+        fz = fusion.c_struct()
+        if fusion.out_gate is not None:
+            _check(fusion.out_gate, "out_gate", q.dtype, dev)
+        if fusion.rms_weight is not None:
+            _check(fusion.rms_weight, "rms_weight", torch.float32, dev)
+        st = lib.kda_decode_multi_ex(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S),
+                                     S.shape[0], _ptr(state_indices), N, T, H, dk, dv, _ptr(o), _ptr(S_steps),
+                                     ctypes.byref(fz), _ptr(device_status), _stream_handle(stream))
+        name = "kda_decode_multi_ex"
     if st != KDA_OK:
-        raise KdaError("kda_decode_multi", st, kda_status_string(st))
+        raise KdaError(name, st, kda_status_string(st))
     return (o, S_steps) if return_steps else o

@@ -559,11 +559,18 @@ kda_status kda_decode_step_ex(const void* q, const void* k, const void* v, kda_d
                        device_status, stream);
 }
 
-kda_status kda_decode_multi(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
-                            const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
-                            int32_t T, int32_t H, int32_t dk, int32_t dv, void* o, float* S_steps,
-                            int32_t* device_status, kda_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+kda_status decode_multi_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                             const float* log_alpha, const float* beta, float* S, int32_t num_slots,
+                             const int32_t* state_indices, int32_t N, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                             void* o, float* S_steps, const kda_fusion* fusion, int32_t* device_status,
+                             kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    kda::DecodeFusion fz;
+    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (N < 0 || T < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -593,13 +600,38 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, kda_dty
     for (const Range& in : inputs)
         if (overlap(r_o, in) || overlap(r_s, in) || overlap(r_st, in)) return KDA_ERR_INVALID_ARG;
     if (overlap(r_o, r_s) || overlap(r_o, r_st) || overlap(r_s, r_st)) return KDA_ERR_INVALID_ARG;
+    if (fz.flags & KDA_FUSE_OUT_GATE) {
+        const Range r_g = range_of(fz.out_gate, nio * es);
+        if (overlap(r_g, r_o) || overlap(r_g, r_s) || overlap(r_g, r_st)) return KDA_ERR_INVALID_ARG;
+    }
 
     const kda_status dev = check_device();
     if (dev != KDA_OK) return dev;
     if (kda::launch_decode_multi(qkv_dtype == KDA_DTYPE_F32, q, k, v, log_alpha, beta, S, num_slots, state_indices,
-                                 N, T, H, o, S_steps, device_status, stream) != cudaSuccess)
+                                 N, T, H, o, S_steps, device_status, stream, fz) != cudaSuccess)
         return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_multi(const void* q, const void* k, const void* v, kda_dtype qkv_dtype, const float* log_alpha,
+                            const float* beta, float* S, int32_t num_slots, const int32_t* state_indices, int32_t N,
+                            int32_t T, int32_t H, int32_t dk, int32_t dv, void* o, float* S_steps,
+                            int32_t* device_status, kda_stream_t stream) {
+    return decode_multi_impl(q, k, v, qkv_dtype, log_alpha, beta, S, num_slots, state_indices, N, T, H, dk, dv, o,
+                             S_steps, nullptr, device_status, stream);
+}
+
+kda_status kda_decode_multi_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                               const float* log_alpha, const float* beta, float* S, int32_t num_slots,
+                               const int32_t* state_indices, int32_t N, int32_t T, int32_t H, int32_t dk, int32_t dv,
+                               void* o, float* S_steps, const kda_fusion* fusion, int32_t* device_status,
+                               kda_stream_t stream) {
+    return decode_multi_impl(q, k, v, qkv_dtype, log_alpha, beta, S, num_slots, state_indices, N, T, H, dk, dv, o,
+                             S_steps, fusion, device_status, stream);
 }
 
 }  // extern "C"

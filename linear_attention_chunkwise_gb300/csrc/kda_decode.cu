@@ -170,12 +170,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 // block barriers (column partial sums, then u).
 constexpr int kTokBatch = 8;
 
-template <typename IoT>
+// FUSED: the prologue / epilogue of DecodeFusion, per token (as kda_decode_kernel's).
+template <typename IoT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     kda_decode_multi_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k, const IoT* __restrict__ v,
                             const float* __restrict__ log_alpha, const float* __restrict__ beta, float* S,
                             int32_t num_slots, const int32_t* __restrict__ state_indices, int32_t T, int32_t H,
-                            IoT* __restrict__ o, float* S_steps, int32_t* device_status) {
+                            IoT* __restrict__ o, float* S_steps, int32_t* device_status, const DecodeFusion fz) {
     const int unit = blockIdx.x;
     const int n = unit / H;
     const int h = unit - n * H;
@@ -193,6 +194,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ __align__(16) float red_y[kThreads / 32][kHeadDim];
     __shared__ __align__(16) float red_p[kThreads / 32][kHeadDim];
     __shared__ float kq_part[4];
+    __shared__ float g_s[FUSED ? kTokBatch : 1][FUSED ? kHeadDim : 1];  // output gates of the batch
+    __shared__ float oo_part[4];
+    const bool l2n = FUSED && (fz.flags & KDA_FUSE_L2NORM_QK);
+    const bool og = FUSED && (fz.flags & KDA_FUSE_OUT_GATE);
 
     float* Sg = S + (static_cast<size_t>(slot) * H + h) * kHeadDim * kHeadDim;
     const int row0 = warp * kRowsPerWarp;
@@ -211,11 +216,39 @@ __global__ void __launch_bounds__(kThreads, 2)
             q_s[tt][ch] = to_f32(q[tok * kHeadDim + ch]);
             a_s[tt][ch] = expf(log_alpha[tok * kHeadDim + ch]);
             v_s[tt][ch] = to_f32(v[tok * kHeadDim + ch]);
+            if (og) g_s[tt][ch] = to_f32(static_cast<const IoT*>(fz.out_gate)[tok * kHeadDim + ch]);
         }
-        if (tid < nb) b_s[tid] = beta[(static_cast<size_t>(n) * T + tb0 + tid) * H + h];
+        if (tid < nb) {
+            float bb = beta[(static_cast<size_t>(n) * T + tb0 + tid) * H + h];
+            if (FUSED && (fz.flags & KDA_FUSE_BETA_SIGMOID)) bb = 1.f / (1.f + expf(-bb));
+            b_s[tid] = bb;
+        }
         __syncthreads();
+        if (l2n) {  // warp tt normalises token tt's k and q rows in place
+            if (warp < nb) {
+                float k2 = 0.f, q2 = 0.f;
+#pragma unroll
+                for (int c = lane; c < kHeadDim; c += 32) {
+                    k2 = fmaf(k_s[warp][c], k_s[warp][c], k2);
+                    q2 = fmaf(q_s[warp][c], q_s[warp][c], q2);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    k2 += __shfl_xor_sync(0xffffffffu, k2, off);
+                    q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+                }
+                const float ik = rsqrtf(k2 + fz.l2_eps), iq = rsqrtf(q2 + fz.l2_eps);
+#pragma unroll
+                for (int c = lane; c < kHeadDim; c += 32) {
+                    k_s[warp][c] *= ik;
+                    q_s[warp][c] *= iq;
+                }
+            }
+            __syncthreads();
+        }
 
         for (int tt = 0; tt < nb; ++tt) {
+            float o_val = 0.f;
             const int t = tb0 + tt;
             const size_t tok = (static_cast<size_t>(n) * T + t) * H + h;
             float4 y = make_float4(0.f, 0.f, 0.f, 0.f), p = y;
@@ -249,9 +282,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float u = b_s[tt] * (v_s[tt][tid] - yy);
                 const float kq = kq_part[0] + kq_part[1] + kq_part[2] + kq_part[3];
                 u_s[tid] = u;
-                o[tok * kHeadDim + tid] = from_f32<IoT>(fmaf(kq, u, pp));
+                o_val = fmaf(kq, u, pp);
+                if (og) {
+                    float o2 = o_val * o_val;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) o2 += __shfl_xor_sync(0xffffffffu, o2, off);
+                    if (lane == 0) oo_part[warp] = o2;
+                } else {
+                    o[tok * kHeadDim + tid] = from_f32<IoT>(o_val);
+                }
             }
             __syncthreads();
+            if (og && tid < kHeadDim) {  // y = RMSNorm(o) * weight * gate; oo_part is rewritten only after
+                                         // the next token's first barrier
+                const float ms = (oo_part[0] + oo_part[1] + oo_part[2] + oo_part[3]) * (1.f / kHeadDim);
+                const float w = fz.rms_weight ? fz.rms_weight[tid] : 1.f;
+                o[tok * kHeadDim + tid] = from_f32<IoT>(o_val * rsqrtf(ms + fz.rms_eps) * w * g_s[tt][tid]);
+            }
 
             const float4 uu = reinterpret_cast<const float4*>(u_s)[lane];
             float* Ss = S_steps ? S_steps + tok * kHeadDim * kHeadDim : nullptr;
@@ -271,23 +318,31 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
+template <typename IoT, bool FUSED>
+void launch_multi_t(const void* q, const void* k, const void* v, const float* log_alpha, const float* beta, float* S,
+                    int32_t num_slots, const int32_t* state_indices, int32_t T, int32_t H, void* o, float* S_steps,
+                    int32_t* device_status, cudaStream_t stream, const DecodeFusion& fz, dim3 grid) {
+    kda_decode_multi_kernel<IoT, FUSED><<<grid, kThreads, 0, stream>>>(
+        static_cast<const IoT*>(q), static_cast<const IoT*>(k), static_cast<const IoT*>(v), log_alpha, beta, S,
+        num_slots, state_indices, T, H, static_cast<IoT*>(o), S_steps, device_status, fz);
+}
+
 cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                                 const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
                                 int32_t N, int32_t T, int32_t H, void* o, float* S_steps, int32_t* device_status,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const DecodeFusion& fusion) {
     const long long units = static_cast<long long>(N) * H;
     if (units == 0 || T == 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>(units));
-    if (f32_io) {
-        kda_decode_multi_kernel<float><<<grid, kThreads, 0, stream>>>(
-            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), log_alpha,
-            beta, S, num_slots, state_indices, T, H, static_cast<float*>(o), S_steps, device_status);
-    } else {
-        kda_decode_multi_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-            static_cast<const __nv_bfloat16*>(v), log_alpha, beta, S, num_slots, state_indices, T, H,
-            static_cast<__nv_bfloat16*>(o), S_steps, device_status);
-    }
+    const bool fused = fusion.flags != 0;
+    if (f32_io)
+        (fused ? launch_multi_t<float, true> : launch_multi_t<float, false>)(
+            q, k, v, log_alpha, beta, S, num_slots, state_indices, T, H, o, S_steps, device_status, stream, fusion,
+            grid);
+    else
+        (fused ? launch_multi_t<__nv_bfloat16, true> : launch_multi_t<__nv_bfloat16, false>)(
+            q, k, v, log_alpha, beta, S, num_slots, state_indices, T, H, o, S_steps, device_status, stream, fusion,
+            grid);
     return cudaGetLastError();
 }
 

@@ -28,7 +28,7 @@ cudaError_t launch_decode(bool f32_io, const void* q, const void* k, const void*
 cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const void* v, const float* log_alpha,
                                 const float* beta, float* S, int32_t num_slots, const int32_t* state_indices,
                                 int32_t N, int32_t T, int32_t H, void* o, float* S_steps, int32_t* device_status,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const DecodeFusion& fusion = DecodeFusion());
 
 // ---- prefill ----
 struct PrefillArgs {
