@@ -50,6 +50,8 @@ def load_library(path: str):
     lib.oracle_kda_prefill.restype = ctypes.c_int
     lib.oracle_kda_decode_step.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, P, i32]
     lib.oracle_kda_decode_step.restype = ctypes.c_int
+    lib.oracle_kda_prefill_backward.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32]
+    lib.oracle_kda_prefill_backward.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = [i32]
     lib.oracle_num_threads.restype = i32
     return lib
@@ -102,6 +104,31 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, nthreads: int = 0
     if rc != 0:
         raise ValueError("oracle_kda_prefill: malformed cu_seqlens or allocation failure")
     return o, sf
+
+
+def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, S0, dO, dS_final=None, nthreads: int = 0, lib=None):
+    """Reverse-mode gradient of kda_prefill for L = <o, dO> + <S_final, dS_final>.
+
+    Same inputs as kda_prefill plus dO [T, H, dv] and dS_final [N, H, dk, dv] (None = 0).
+    Returns (dq, dk, dv, dlog_alpha, dbeta, dS0), float64, shaped like the inputs.
+    """
+    q, k, v, la, b = (_f32(x) for x in (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    s0 = None if S0 is None else _f32(S0)
+    do = np.ascontiguousarray(np.asarray(dO, dtype=np.float64))
+    dsf = None if dS_final is None else np.ascontiguousarray(np.asarray(dS_final, dtype=np.float64))
+    assert do.shape == (T, H, dv)
+    out = [np.zeros((T, H, dk)), np.zeros((T, H, dk)), np.zeros((T, H, dv)), np.zeros((T, H, dk)),
+           np.zeros((T, H)), np.zeros((N, H, dk, dv))]
+    rc = (lib or _load()).oracle_kda_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0), _ptr(cu), N, H, dk, dv, _ptr(do), _ptr(dsf),
+        *(_ptr(x) for x in out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_kda_prefill_backward: malformed cu_seqlens or allocation failure")
+    return tuple(out)
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S, state_indices=None, nthreads: int = 0, lib=None):

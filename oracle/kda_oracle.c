@@ -183,3 +183,127 @@ int32_t oracle_num_threads(int32_t requested) {
     return 1;
 #endif
 }
+
+
+/*
+ * Reverse-mode gradient of the prefill above, for a loss
+ *   L = sum_t <o_t, dO_t> + sum_n <S_final_n, dS_final_n>,
+ * taken through the same literal update, step by step in reverse:
+ *   S_t = Sd - beta k (Sd^T k)^T + beta k v^T,  Sd = Diag(exp(log_alpha)) S_{t-1},
+ *   o_t = S_t^T q.
+ * The adjoint of S (Sbar, dk x dv) starts at dS_final and is carried back to
+ * dS0.  Forward states are kept for every token of the sequence (test sizes).
+ *   dO, dS_final : double, shapes as o and S_final (dS_final may be NULL = 0)
+ *   dq, dk, dlog_alpha : [T_total, H, dk] double (out); dv : [T_total, H, dv]
+ *   dbeta : [T_total, H] double (out);  dS0 : [N, H, dk, dv] double or NULL
+ * Returns 0, or -1 on a malformed cu_seqlens / allocation failure.
+ */
+int oracle_kda_prefill_backward(const float *q, const float *k, const float *v,
+                                const float *log_alpha, const float *beta, const float *S0,
+                                const int32_t *cu_seqlens, int32_t N, int32_t H,
+                                int32_t dk, int32_t dv, const double *dO, const double *dS_final,
+                                double *dq, double *dkk, double *dvv, double *dla, double *dbeta,
+                                double *dS0, int32_t nthreads) {
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (N > 0 && cu_seqlens[0] != 0) return -1;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    int err = 0;
+    long units = (long)N * H;
+    const size_t M = (size_t)dk * dv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+#endif
+    for (long u = 0; u < units; ++u) {
+        int n = (int)(u / H), h = (int)(u % H);
+        int64_t t0 = cu_seqlens[n], L = cu_seqlens[n + 1] - t0;
+        double *Sall = (double *)malloc(sizeof(double) * M * (size_t)(L + 1)); /* S_{-1} .. S_{L-1} */
+        double *Sd = (double *)malloc(sizeof(double) * M);
+        double *Sb = (double *)malloc(sizeof(double) * M);  /* adjoint of S_t */
+        double *Sdb = (double *)malloc(sizeof(double) * M); /* adjoint of Sd */
+        double *kS = (double *)malloc(sizeof(double) * dv);
+        double *kSb = (double *)malloc(sizeof(double) * dv);
+        if (!Sall || !Sd || !Sb || !Sdb || !kS || !kSb) {
+            err |= 1;
+        } else {
+            size_t sidx = ((size_t)n * H + h) * M;
+            for (size_t e = 0; e < M; ++e) Sall[e] = S0 ? (double)S0[sidx + e] : 0.0;
+            /* forward, keeping every state */
+            for (int64_t i = 0; i < L; ++i) {
+                size_t th = (size_t)(t0 + i) * H + h;
+                double *Sp = Sall + (size_t)i * M, *Sn = Sall + (size_t)(i + 1) * M;
+                memcpy(Sn, Sp, sizeof(double) * M);
+                kda_token(Sn, Sd, kS, dk, dv, q + th * dk, k + th * dk, v + th * dv, log_alpha + th * dk,
+                          (double)beta[th], NULL);
+            }
+            for (size_t e = 0; e < M; ++e) Sb[e] = dS_final ? dS_final[sidx + e] : 0.0;
+            /* reverse */
+            for (int64_t i = L - 1; i >= 0; --i) {
+                size_t th = (size_t)(t0 + i) * H + h;
+                const float *qt = q + th * dk, *kt = k + th * dk, *vt = v + th * dv, *lat = log_alpha + th * dk;
+                const double *ob = dO + th * dv;
+                const double b = (double)beta[th];
+                const double *Sp = Sall + (size_t)i * M, *St = Sall + (size_t)(i + 1) * M;
+                /* recompute Sd and kS = Sd^T k of this token */
+                for (int r = 0; r < dk; ++r) {
+                    double a = exp((double)lat[r]);
+                    for (int j = 0; j < dv; ++j) Sd[(size_t)r * dv + j] = a * Sp[(size_t)r * dv + j];
+                }
+                for (int j = 0; j < dv; ++j) kS[j] = 0.0;
+                for (int r = 0; r < dk; ++r)
+                    for (int j = 0; j < dv; ++j) kS[j] += (double)kt[r] * Sd[(size_t)r * dv + j];
+                /* o = S_t^T q: Sbar += q obar^T, qbar = S_t obar */
+                for (int r = 0; r < dk; ++r) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j) {
+                        Sb[(size_t)r * dv + j] += (double)qt[r] * ob[j];
+                        acc += St[(size_t)r * dv + j] * ob[j];
+                    }
+                    dq[th * dk + r] = acc;
+                }
+                /* S_t = Sd - b k kS^T + b k v^T */
+                double betabar = 0.0;
+                for (int r = 0; r < dk; ++r) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j) acc += Sb[(size_t)r * dv + j] * ((double)vt[j] - kS[j]);
+                    dkk[th * dk + r] = b * acc;          /* from the k of the outer products */
+                    betabar += (double)kt[r] * acc;
+                }
+                dbeta[th] = betabar;
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dk; ++r) acc += Sb[(size_t)r * dv + j] * (double)kt[r];
+                    kSb[j] = -b * acc;                   /* adjoint of kS */
+                    dvv[th * dv + j] = b * acc;
+                }
+                /* Sd: direct term plus kS = Sd^T k */
+                for (int r = 0; r < dk; ++r) {
+                    double acc = 0.0;
+                    for (int j = 0; j < dv; ++j) {
+                        Sdb[(size_t)r * dv + j] = Sb[(size_t)r * dv + j] + (double)kt[r] * kSb[j];
+                        acc += Sd[(size_t)r * dv + j] * kSb[j];
+                    }
+                    dkk[th * dk + r] += acc;
+                }
+                /* Sd = Diag(exp(log_alpha)) S_{t-1} */
+                for (int r = 0; r < dk; ++r) {
+                    double a = exp((double)lat[r]), acc = 0.0;
+                    for (int j = 0; j < dv; ++j) {
+                        acc += Sdb[(size_t)r * dv + j] * Sd[(size_t)r * dv + j];
+                        Sb[(size_t)r * dv + j] = a * Sdb[(size_t)r * dv + j];
+                    }
+                    dla[th * dk + r] = acc;
+                }
+            }
+            if (dS0) memcpy(dS0 + sidx, Sb, sizeof(double) * M);
+        }
+        free(Sall);
+        free(Sd);
+        free(Sb);
+        free(Sdb);
+        free(kS);
+        free(kSb);
+    }
+    return err ? -1 : 0;
+}
