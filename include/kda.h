@@ -225,6 +225,51 @@ KDA_API kda_status kda_prefill_ex(const void *q, const void *k, const void *v, k
                           int32_t *device_status, kda_stream_t stream);
 
 /*
+ * kda_prefill_backward -- reverse-mode gradient of kda_prefill (plain
+ * inputs; no fusion) for the scalar loss
+ *     L = sum_{t,h,j} o[t,h,j] grad_o[t,h,j] + sum_{n,h,i,j} S_final grad_S_final,
+ * i.e. the vector-Jacobian product of the recurrence of "Understanding Kimi
+ * Delta Attention" (pyshine), section "The KDA Recurrence", read in the
+ * erase-then-write order of "kimi delta attn from first principles"
+ * (aryagxr), section "KDA".  The pages train the layer but print no
+ * backward; this is the exact derivative of that update, per token.
+ *
+ *   q, k, v, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H,
+ *   dk, dv     the forward's inputs, as kda_prefill (S0 may be NULL = zeros)
+ *   grad_o        [total_tokens, H, dv] qkv_dtype, device (dL/do)
+ *   grad_S_final  [num_seqs, H, dk, dv] fp32 device, or NULL (zeros)
+ *   grad_q, grad_k, grad_v, grad_log_alpha  [total_tokens, H, 128] fp32 out
+ *   grad_beta     [total_tokens, H] fp32 out
+ *   grad_S0       [num_seqs, H, dk, dv] fp32 out, or NULL (not computed)
+ *
+ * The library reruns the chunkwise forward inside the call, recording the
+ * state after every 64-token chunk, then walks each (sequence, head) back in
+ * fp32, recomputing the per-token states of one chunk at a time.  The
+ * gradients are those of the fp32 recurrence on the given inputs; the only
+ * bf16 step is the chunkwise forward that supplies the chunk-start states.
+ * When the heads leave SMs idle a head's state columns are split over CTAs
+ * and the row sums (grad_q, grad_k, grad_log_alpha, grad_beta) are added
+ * atomically, so the last bits of those may differ from run to run.
+ *
+ * Workspace: >= kda_prefill_backward_workspace_bytes(...) device bytes,
+ * 256-byte aligned (KDA_ERR_WORKSPACE below it).  Pointers: 16-byte aligned
+ * (beta, grad_beta: 4).  The outputs overlap nothing: not each other, the
+ * inputs or the workspace (KDA_ERR_INVALID_ARG).  Other errors are
+ * kda_prefill's; a malformed cu_seqlens sets KDA_DEV_BAD_CU_SEQLENS and leaves
+ * the gradients unspecified.  Asynchronous on `stream`.
+ */
+KDA_API size_t kda_prefill_backward_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens,
+                                                    int32_t H, int32_t dk, int32_t dv);
+KDA_API kda_status kda_prefill_backward(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                        const float *log_alpha, const float *beta, const float *S0,
+                                        const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                        int32_t H, int32_t dk, int32_t dv, const void *grad_o,
+                                        const float *grad_S_final, float *grad_q, float *grad_k, float *grad_v,
+                                        float *grad_log_alpha, float *grad_beta, float *grad_S0,
+                                        void *workspace, size_t workspace_bytes, int32_t *device_status,
+                                        kda_stream_t stream);
+
+/*
  * kda_decode_step -- one fused recurrent step for N sequences
  * ("Understanding Kimi Delta Attention" (pyshine), section "The Chunkwise
  * DPLR Algorithm": the step-by-step "fused recurrent mode" for decode).

@@ -61,7 +61,7 @@ class Fusion:
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
                     "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex",
-                    "kda_decode_multi_ex")
+                    "kda_decode_multi_ex", "kda_prefill_backward_workspace_bytes", "kda_prefill_backward")
 
 _lock = threading.Lock()
 _lib = None
@@ -110,6 +110,11 @@ def load_library(path: str | None = None):
                                             FP, P, P]
         lib.kda_decode_multi_ex.restype = ctypes.c_int
         lib.kda_prefill.restype = ctypes.c_int
+        lib.kda_prefill_backward_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
+        lib.kda_prefill_backward_workspace_bytes.restype = sz
+        lib.kda_prefill_backward.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
+                                             P, P, P, P, P, P, P, sz, P, P]
+        lib.kda_prefill_backward.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_multi.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P, P, P]
@@ -263,6 +268,61 @@ def kda_prefill_snapshots(q, k, v, log_alpha, beta, cu_seqlens, snap_seq, snap_p
     if st != KDA_OK:
         raise KdaError("kda_prefill_snapshots", st, kda_status_string(st))
     return o, S_final, S_snap
+
+
+def kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: int, dk: int = 128,
+                                         dv: int = 128) -> int:
+    code = qkv_dtype if isinstance(qkv_dtype, int) else _dtype_code(qkv_dtype)
+    return int(load_library().kda_prefill_backward_workspace_bytes(code, int(num_seqs), int(total_tokens), int(H),
+                                                                   int(dk), int(dv)))
+
+
+def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, grad_S_final=None, *,
+                         need_grad_S0=True, grads=None, workspace=None, device_status=None, stream=None):
+    """Gradient of kda_prefill for L = <o, grad_o> + <S_final, grad_S_final> (see include/kda.h).
+
+    grad_o: [T, H, 128] in the dtype of q; grad_S_final: fp32 [N, H, 128, 128] or None (zeros).
+    Returns (grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0), all fp32; grad_S0 is None
+    when need_grad_S0 is False.  `grads` may pass those six output tensors in.
+    """
+    lib = load_library()
+    dev = q.device
+    _check(q, "q", device=dev)
+    code = _dtype_code(q.dtype)
+    for t, n, dt in ((k, "k", q.dtype), (v, "v", q.dtype), (log_alpha, "log_alpha", torch.float32),
+                     (beta, "beta", torch.float32), (cu_seqlens, "cu_seqlens", torch.int32),
+                     (S0, "S0", torch.float32), (grad_o, "grad_o", q.dtype),
+                     (grad_S_final, "grad_S_final", torch.float32)):
+        _check(t, n, dt, dev)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, dk]")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    if N < 0:
+        raise ValueError("cu_seqlens must have at least one entry")
+    if grads is None:
+        f32 = dict(dtype=torch.float32, device=dev)
+        grads = (torch.empty((T, H, dk), **f32), torch.empty((T, H, dk), **f32), torch.empty((T, H, dv), **f32),
+                 torch.empty((T, H, dk), **f32), torch.empty((T, H), **f32),
+                 torch.empty((N, H, dk, dv), **f32) if need_grad_S0 else None)
+    if len(grads) != 6:
+        raise ValueError("grads must hold six tensors (the last may be None)")
+    for t, n in zip(grads, ("grad_q", "grad_k", "grad_v", "grad_log_alpha", "grad_beta", "grad_S0")):
+        _check(t, n, torch.float32, dev)
+    need = int(lib.kda_prefill_backward_workspace_bytes(code, N, T, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    gq, gk, gv, gla, gb, gs0 = grads
+    st = lib.kda_prefill_backward(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                                  _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(grad_o), _ptr(grad_S_final), _ptr(gq),
+                                  _ptr(gk), _ptr(gv), _ptr(gla), _ptr(gb), _ptr(gs0), _ptr(workspace),
+                                  workspace.numel(), _ptr(device_status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError("kda_prefill_backward", st, kda_status_string(st))
+    return gq, gk, gv, gla, gb, gs0
 
 
 def _check_fusion(fusion, q, tokens):

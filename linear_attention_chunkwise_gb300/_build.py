@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libkda.so")
-SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_prefill.cu", "kda_prefill_split.cu", "kda_noalloc.cu"]
+SOURCES = ["kda_api.cu", "kda_decode.cu", "kda_prefill.cu", "kda_prefill_split.cu", "kda_noalloc.cu",
+           "kda_backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -488,6 +488,169 @@ kda_status kda_prefill_snapshots(const void* q, const void* k, const void* v, kd
                         S_final, snap, nullptr, workspace, workspace_bytes, device_status, stream);
 }
 
+
+}  // extern "C"
+
+namespace {
+
+// Backward workspace: [two-pass prefill workspace][o scratch][snapshot seq][snapshot pos]
+// [state after every chunk][work counter][per-CTA scratch slabs].
+constexpr int32_t kBwdMaxCtas = 256;  // slabs the workspace holds (more than one CTA per SM of a GB300)
+struct BwdLayout {
+    size_t o = 0, seq = 0, pos = 0, snap = 0, work = 0, slab = 0, total = 0;
+    int64_t entries = 0;
+};
+BwdLayout bwd_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
+    BwdLayout b;
+    b.entries = max_chunks(N, T);
+    b.o = round_up(split_layout(t, N, T, H).total, kAlign);
+    b.seq = b.o + round_up(static_cast<size_t>(T) * H * kHeadDim * esize_of(t), kAlign);
+    b.pos = b.seq + round_up(static_cast<size_t>(b.entries) * 4, kAlign);
+    b.snap = b.pos + round_up(static_cast<size_t>(b.entries) * 4, kAlign);
+    b.work = b.snap + static_cast<size_t>(b.entries) * H * kHeadDim * kHeadDim * 4;
+    b.slab = b.work + kAlign;
+    const int64_t units = static_cast<int64_t>(N) * H;
+    b.total = b.slab + static_cast<size_t>(std::min<int64_t>(units, kBwdMaxCtas)) * kda::backward_slab_bytes(kHeadDim);
+    return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_backward_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                            int32_t dk, int32_t dv) {
+    if (!ws_args_ok(qkv_dtype, num_seqs, total_tokens, H, dk, dv)) return 0;
+    if (!sizes_ok(max_chunks(num_seqs, total_tokens), H, kHeadDim * kHeadDim, 4)) return 0;
+    return bwd_layout(qkv_dtype, num_seqs, total_tokens, H).total;
+}
+
+kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                const float* log_alpha, const float* beta, const float* S0,
+                                const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
+                                float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
+                                float* grad_beta, float* grad_S0, void* workspace, size_t workspace_bytes,
+                                int32_t* device_status, kda_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
+    if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
+    const size_t need = kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
+    if (need == 0 || !sizes_ok(num_seqs, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
+    const bool have_tokens = total_tokens > 0;
+    if (have_tokens && (!q || !k || !v || !log_alpha || !beta || !grad_o || !grad_q || !grad_k || !grad_v ||
+                        !grad_log_alpha || !grad_beta))
+        return KDA_ERR_INVALID_ARG;
+    if (have_tokens && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+                        !aligned(beta, 4) || !aligned(grad_o, 16) || !aligned(grad_q, 16) || !aligned(grad_k, 16) ||
+                        !aligned(grad_v, 16) || !aligned(grad_log_alpha, 16) || !aligned(grad_beta, 4)))
+        return KDA_ERR_INVALID_ARG;
+    if ((S0 && !aligned(S0, 16)) || (grad_S_final && !aligned(grad_S_final, 16)) ||
+        (grad_S0 && !aligned(grad_S0, 16)) || !aligned(workspace, kAlign) || !aligned(cu_seqlens, 4) ||
+        (device_status && !aligned(device_status, 4)))
+        return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+
+    // Overlap rules: the gradients overlap nothing (each other, the inputs, the workspace).
+    const size_t es = esize_of(qkv_dtype);
+    const size_t nqk = static_cast<size_t>(total_tokens) * H * kHeadDim;
+    const size_t nst = static_cast<size_t>(num_seqs) * H * kHeadDim * kHeadDim;
+    const size_t nb = static_cast<size_t>(total_tokens) * H;
+    const Range ins[] = {range_of(q, nqk * es),
+                         range_of(k, nqk * es),
+                         range_of(v, nqk * es),
+                         range_of(log_alpha, nqk * 4),
+                         range_of(beta, nb * 4),
+                         range_of(S0, S0 ? nst * 4 : 0),
+                         range_of(cu_seqlens, static_cast<size_t>(num_seqs + 1) * 4),
+                         range_of(grad_o, nqk * es),
+                         range_of(grad_S_final, grad_S_final ? nst * 4 : 0),
+                         range_of(device_status, device_status ? 4 : 0)};
+    const Range r_ws = range_of(workspace, need);
+    const Range outs[] = {range_of(grad_q, have_tokens ? nqk * 4 : 0),
+                          range_of(grad_k, have_tokens ? nqk * 4 : 0),
+                          range_of(grad_v, have_tokens ? nqk * 4 : 0),
+                          range_of(grad_log_alpha, have_tokens ? nqk * 4 : 0),
+                          range_of(grad_beta, have_tokens ? nb * 4 : 0),
+                          range_of(grad_S0, grad_S0 ? nst * 4 : 0),
+                          r_ws};
+    constexpr size_t n_outs = sizeof(outs) / sizeof(outs[0]);
+    for (size_t i = 0; i < n_outs; ++i) {
+        for (const Range& in : ins)
+            if (overlap(outs[i], in)) return KDA_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < n_outs; ++j)
+            if (overlap(outs[i], outs[j])) return KDA_ERR_INVALID_ARG;
+    }
+
+    const kda_status dev = check_device();
+    if (dev != KDA_OK) return dev;
+
+    // 1. chunk table (validates cu_seqlens into device_status) and a snapshot entry at every chunk end
+    const WsLayout fwd = split_layout(qkv_dtype, num_seqs, total_tokens, H);
+    const BwdLayout lay = bwd_layout(qkv_dtype, num_seqs, total_tokens, H);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws + fwd.table);
+    int32_t* snap_seq = reinterpret_cast<int32_t*>(ws + lay.seq);
+    int32_t* snap_pos = reinterpret_cast<int32_t*>(ws + lay.pos);
+    float* ckpt = reinterpret_cast<float*>(ws + lay.snap);
+    if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, chunk_off, device_status, nullptr, nullptr, 0,
+                                stream) != cudaSuccess ||
+        kda::launch_ckpt_entries(cu_seqlens, chunk_off, num_seqs, static_cast<int32_t>(lay.entries), snap_seq,
+                                 snap_pos, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    // 2. the chunkwise prefill records those states (its own table pass rebuilds the same chunk table)
+    Snapshots snap;
+    snap.seq = snap_seq;
+    snap.pos = snap_pos;
+    snap.count = static_cast<int32_t>(lay.entries);
+    snap.S = ckpt;
+    const kda_status fs = prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens,
+                                       H, dk, dv, ws + lay.o, nullptr, snap, nullptr, workspace, fwd.total, nullptr,
+                                       stream_);
+    if (fs != KDA_OK) return fs;
+    // 3. the reverse walk: state columns split over CTAs when the heads alone leave SMs idle
+    const int sms = sm_count();
+    const int64_t units = static_cast<int64_t>(num_seqs) * H;
+    const int32_t cols = units * 4 <= sms ? 32 : units * 2 <= sms ? 64 : 128;
+    const int64_t work_units = units * (kHeadDim / cols);
+    const int32_t ctas = static_cast<int32_t>(std::min<int64_t>({work_units, sms, kBwdMaxCtas}));
+    kda::BackwardArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.log_alpha = log_alpha;
+    a.beta = beta;
+    a.S0 = S0;
+    a.cu_seqlens = cu_seqlens;
+    a.order = reinterpret_cast<const int32_t*>(ws);  // the prefill's schedule
+    a.chunk_off = chunk_off;
+    a.ckpt = ckpt;
+    a.dO = grad_o;
+    a.dS_final = grad_S_final;
+    a.dq = grad_q;
+    a.dk = grad_k;
+    a.dv = grad_v;
+    a.dla = grad_log_alpha;
+    a.dbeta = grad_beta;
+    a.dS0 = grad_S0;
+    a.scratch = reinterpret_cast<float*>(ws + lay.slab);
+    a.work = reinterpret_cast<int32_t*>(ws + lay.work);
+    a.num_seqs = num_seqs;
+    a.H = H;
+    if (cudaMemsetAsync(a.work, 0, 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cols < kHeadDim && have_tokens) {  // row sums are accumulated over the slices
+        if (cudaMemsetAsync(grad_q, 0, nqk * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(grad_k, 0, nqk * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(grad_log_alpha, 0, nqk * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(grad_beta, 0, nb * 4, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    return kda::launch_backward(a, qkv_dtype == KDA_DTYPE_F32, cols, ctas, stream) == cudaSuccess ? KDA_OK
+                                                                                                 : KDA_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace {

@@ -97,4 +97,39 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
                               cudaStream_t stream);
 
+// Reverse-mode gradient of the prefill (kda_backward.cu).  Gradients are fp32,
+// [T, H, 128] for q/k/v/log_alpha, [T, H] for beta, [N, H, 128, 128] for S0.
+struct BackwardArgs {
+    const void* q = nullptr;
+    const void* k = nullptr;
+    const void* v = nullptr;
+    const float* log_alpha = nullptr;
+    const float* beta = nullptr;
+    const float* S0 = nullptr;
+    const int32_t* cu_seqlens = nullptr;
+    const int32_t* order = nullptr;      // sequences, longest first
+    const int32_t* chunk_off = nullptr;  // chunk table
+    const float* ckpt = nullptr;         // state after every chunk: entry chunk_off[n] + c
+    const void* dO = nullptr;
+    const float* dS_final = nullptr;
+    float* dq = nullptr;
+    float* dk = nullptr;
+    float* dv = nullptr;
+    float* dla = nullptr;
+    float* dbeta = nullptr;
+    float* dS0 = nullptr;
+    float* scratch = nullptr;  // per-CTA slab of backward_slab_bytes(cols)
+    int32_t* work = nullptr;   // work counter, zero before the launch
+    int32_t num_seqs = 0;
+    int32_t H = 0;
+};
+// Scratch slab of one backward CTA that owns `cols` columns of a head's state.
+size_t backward_slab_bytes(int cols);
+// Snapshot entries at every chunk end (and sentinels up to max_entries) from the chunk table.
+cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_off, int32_t N, int32_t max_entries,
+                                int32_t* snap_seq, int32_t* snap_pos, cudaStream_t stream);
+// cols = 128, 64 or 32 state columns per CTA; with fewer than 128 the row sums
+// (dq, dk, dla, dbeta) are added atomically and must be zeroed first.
+cudaError_t launch_backward(const BackwardArgs& a, bool f32_io, int32_t cols, int32_t ctas, cudaStream_t stream);
+
 }  // namespace kda

@@ -227,3 +227,55 @@ def _decode_multi(lib, **over):
 ])
 def test_decode_multi_rejects_bad_arguments(lib, over, expect):
     assert _decode_multi(lib, **over) == expect
+
+
+def test_backward_workspace_bytes(lib):
+    # two-pass prefill workspace, o scratch, snapshot entries (ceil(T/64) + N per head, 64 KB each),
+    # a work counter and one 4 MB slab per (sequence, head) up to 256
+    T, H, N = 128, 2, 1
+    fwd = 256 + 256 + (2 + 1) * H * BLOB
+    want = fwd + T * H * 128 * 2 + 256 + 256 + (2 + 1) * H * 65536 + 256 + N * H * 64 * 128 * 128 * 4
+    assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H) == want
+    big = kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32)
+    assert big > 256 * 64 * 128 * 128 * 4  # slabs capped at 256
+    assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
+    assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, 1, 10, 2, 64, 128) == 0
+
+
+def _backward(lib, **over):
+    T, H, N = 128, 2, 1
+    tok = T * H * 128
+    need = kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H)
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, dO=BASE + 12 * tok, dSf=None,
+             gq=BASE + 20 * tok, gk=BASE + 24 * tok, gv=BASE + 28 * tok, gla=BASE + 32 * tok, gb=BASE + 36 * tok,
+             gs0=BASE + 40 * tok, ws=BASE + 64 * tok, wsb=need, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill_backward(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]),
+                                    P(a["S0"]), P(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"], P(a["dO"]),
+                                    P(a["dSf"]), P(a["gq"]), P(a["gk"]), P(a["gv"]), P(a["gla"]), P(a["gb"]),
+                                    P(a["gs0"]), P(a["ws"]), a["wsb"], P(a["status"]), None)
+
+
+TOK = 128 * 2 * 128
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dtype=5), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dO=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(gq=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(gb=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(gk=BASE + 24 * TOK + 8), kda.KDA_ERR_INVALID_ARG),       # misaligned
+    (dict(ws=BASE + 64 * TOK + 16), kda.KDA_ERR_INVALID_ARG),      # workspace not 256-aligned
+    (dict(wsb=1 << 20), kda.KDA_ERR_WORKSPACE),
+    (dict(gv=BASE + 20 * TOK + 4096), kda.KDA_ERR_INVALID_ARG),    # grad_v overlaps grad_q
+    (dict(gla=BASE + 12 * TOK), kda.KDA_ERR_INVALID_ARG),          # grad_log_alpha overlaps grad_o
+    (dict(gs0=BASE + 70 * TOK), kda.KDA_ERR_INVALID_ARG),          # grad_S0 inside the workspace
+    (dict(gq=BASE), kda.KDA_ERR_INVALID_ARG),                      # grad_q overlaps q
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+])
+def test_backward_rejects_bad_arguments(lib, over, expect):
+    assert _backward(lib, **over) == expect
