@@ -39,6 +39,9 @@ H, D = 32, 128
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2          # 1540
 PREFILL_FLOPS_PER_TOKEN_HEAD = 10 * 64 * D + 6 * D * D                  # 180,224 (full 64x64 tiles)
 STATE_BYTES = D * D * 4                                                 # 65,536
+# backward: reads q, k, v, grad_o (bf16), log_alpha, beta; writes fp32 grad_q, grad_k, grad_v,
+# grad_log_alpha and grad_beta
+BACKWARD_BYTES_PER_TOKEN_HEAD = 4 * D * 2 + D * 4 + 4 + 4 * D * 4 + 4   # 3,592
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + PREFILL_BYTES_PER_TOKEN_HEAD  # 132,612
 METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s & % HBM (H=32, d=128)"
 # sources whose ncu DRAM counters profiles/ncu_traffic.json records (null once they change)
@@ -503,12 +506,68 @@ def bench_decode(cx: Ctx, args):
     }
 
 
+def bench_backward(cx: Ctx, args):
+    """Prefill backward on the 8k workload (grad_o ~ N(0,1) bf16, grad_S_final ~ N(0, 0.01)): one call
+    reruns the chunkwise forward with a snapshot per chunk and walks every head back."""
+    torch = cx.torch
+    import linear_attention_chunkwise_gb300 as kda
+    from linear_attention_chunkwise_gb300 import synth
+
+    c = synth.CONFIGS[PREFILL_CFG]
+    p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
+                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+    T = p.total_tokens
+    g = torch.Generator(device=cx.dev).manual_seed(11 + cx.rank)
+    dO = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
+    dSf = torch.randn((1, H, D, D), generator=g, device=cx.dev) * 0.1
+    f32 = dict(dtype=torch.float32, device=cx.dev)
+    grads = (torch.empty((T, H, D), **f32), torch.empty((T, H, D), **f32), torch.empty((T, H, D), **f32),
+             torch.empty((T, H, D), **f32), torch.empty((T, H), **f32), torch.empty((1, H, D, D), **f32))
+    wsb = kda.kda_prefill_backward_workspace_bytes(torch.bfloat16, 1, T, H)
+    work = torch.empty(wsb, dtype=torch.uint8, device=cx.dev)
+
+    def call():
+        kda.kda_prefill_backward(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, None, dSf, grads=grads,
+                                 workspace=work, stream=cx.stream)
+
+    n = max(3, min(args.steps, 10))
+    for _ in range(max(3, args.warmup)):
+        call()
+    cx.barrier()
+    ev0, ev1 = cx.events()
+    with ClockSampler(cx.dev) as clk:
+        ev0.record(cx.stream)
+        for _ in range(n):
+            call()
+        ev1.record(cx.stream)
+        cx.barrier()
+    ms_local = ev0.elapsed_time(ev1) / n
+    ms = cx.max_over_ranks(ms_local)
+    bytes_per_call = T * H * BACKWARD_BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES  # + grad_S_final, grad_S0
+    achieved = bytes_per_call / (ms_local * 1e-3) / 1e9
+    pk = cx.peaks
+    del work, grads
+    return {
+        "workload": "KDA prefill backward B=1 H=32 T=8192 d=128, bf16 q/k/v/grad_o, fp32 gates, S0=0, "
+                    "grad_S_final given; fp32 gradients of q, k, v, log_alpha, beta, S0",
+        "value": round(T * cx.ws / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms_per_call": round(ms, 3),
+        "calls": n,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "kernel": "kda_prefill_backward call (chunkwise forward with per-chunk snapshots + "
+                               "reverse walk)",
+                     "peak_source": pk["src"] + " burst copy", "bytes_per_launch": bytes_per_call},
+        "clocks": clk.summary(),
+    }
+
+
 def run_ours(args):
     from linear_attention_chunkwise_gb300 import _build
     _build.build()
     cx = Ctx()
     pf = bench_prefill(cx, args) if args.only in ("all", "prefill") else None
     dc = bench_decode(cx, args) if args.only in ("all", "decode") else None
+    bw = bench_backward(cx, args) if args.only in ("all", "backward") else None
     out = {"metric": METRIC}
     if pf is not None:
         out.update({
@@ -527,6 +586,8 @@ def run_ours(args):
         })
     if dc is not None:
         out["decode"] = dc
+    if bw is not None:
+        out["backward"] = bw
     if cx.rank == 0 and not args.no_cpu_baseline and pf is not None:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if cx.rank == 0:
@@ -625,7 +686,7 @@ def main(argv=None):
     ap.add_argument("--decode-reps", type=int, default=5, help="replays of the 100-step decode graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward"], default="all",
                     help="profiling aid: run only one workload (the JSON line then lacks the other)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
