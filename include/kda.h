@@ -243,13 +243,12 @@ KDA_API kda_status kda_prefill_ex(const void *q, const void *k, const void *v, k
  *   grad_S0       [num_seqs, H, dk, dv] fp32 out, or NULL (not computed)
  *
  * The library reruns the chunkwise forward inside the call, recording the
- * state after every 64-token chunk, then walks each (sequence, head) back in
- * fp32, recomputing the per-token states of one chunk at a time.  The
+ * state after every 64-token chunk, then computes the gradient chunkwise in
+ * fp32: one walk of the state's adjoint back over the chunks of each
+ * (sequence, head), and dense per-chunk products for everything else.  The
  * gradients are those of the fp32 recurrence on the given inputs; the only
  * bf16 step is the chunkwise forward that supplies the chunk-start states.
- * When the heads leave SMs idle a head's state columns are split over CTAs
- * and the row sums (grad_q, grad_k, grad_log_alpha, grad_beta) are added
- * atomically, so the last bits of those may differ from run to run.
+ * Results are bitwise repeatable.  grad_q doubles as scratch during the call.
  *
  * Workspace: >= kda_prefill_backward_workspace_bytes(...) device bytes,
  * 256-byte aligned (KDA_ERR_WORKSPACE below it).  Pointers: 16-byte aligned

@@ -493,24 +493,25 @@ kda_status kda_prefill_snapshots(const void* q, const void* k, const void* v, kd
 
 namespace {
 
-// Backward workspace: [two-pass prefill workspace][o scratch][snapshot seq][snapshot pos]
-// [state after every chunk][work counter][per-CTA scratch slabs].
-constexpr int32_t kBwdMaxCtas = 256;  // slabs the workspace holds (more than one CTA per SM of a GB300)
+// Backward workspace: [schedule][chunk table][forward's bf16 copies and operand images, later the
+// backward's per-chunk records][o scratch][snapshot seq][snapshot pos][state after every chunk]
+// [adjoint after every chunk].
 struct BwdLayout {
-    size_t o = 0, seq = 0, pos = 0, snap = 0, work = 0, slab = 0, total = 0;
+    size_t o = 0, seq = 0, pos = 0, snap = 0, xbuf = 0, total = 0;
     int64_t entries = 0;
 };
 BwdLayout bwd_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
     BwdLayout b;
+    const WsLayout f = split_layout(t, N, T, H);
     b.entries = max_chunks(N, T);
-    b.o = round_up(split_layout(t, N, T, H).total, kAlign);
+    const size_t per_state = static_cast<size_t>(b.entries) * H * kHeadDim * kHeadDim * 4;
+    const size_t recs = static_cast<size_t>(b.entries) * H * kda::backward_record_bytes();
+    b.o = round_up(std::max(f.total, f.copies + recs), kAlign);
     b.seq = b.o + round_up(static_cast<size_t>(T) * H * kHeadDim * esize_of(t), kAlign);
     b.pos = b.seq + round_up(static_cast<size_t>(b.entries) * 4, kAlign);
     b.snap = b.pos + round_up(static_cast<size_t>(b.entries) * 4, kAlign);
-    b.work = b.snap + static_cast<size_t>(b.entries) * H * kHeadDim * kHeadDim * 4;
-    b.slab = b.work + kAlign;
-    const int64_t units = static_cast<int64_t>(N) * H;
-    b.total = b.slab + static_cast<size_t>(std::min<int64_t>(units, kBwdMaxCtas)) * kda::backward_slab_bytes(kHeadDim);
+    b.xbuf = b.snap + per_state;
+    b.total = b.xbuf + per_state;
     return b;
 }
 
@@ -610,12 +611,7 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
                                        H, dk, dv, ws + lay.o, nullptr, snap, nullptr, workspace, fwd.total, nullptr,
                                        stream_);
     if (fs != KDA_OK) return fs;
-    // 3. the reverse walk: state columns split over CTAs when the heads alone leave SMs idle
-    const int sms = sm_count();
-    const int64_t units = static_cast<int64_t>(num_seqs) * H;
-    const int32_t cols = units * 4 <= sms ? 32 : units * 2 <= sms ? 64 : 128;
-    const int64_t work_units = units * (kHeadDim / cols);
-    const int32_t ctas = static_cast<int32_t>(std::min<int64_t>({work_units, sms, kBwdMaxCtas}));
+    // 3. prep, scan of the adjoint over chunks, value and key kernels
     kda::BackwardArgs a;
     a.q = q;
     a.k = k;
@@ -635,20 +631,13 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
     a.dla = grad_log_alpha;
     a.dbeta = grad_beta;
     a.dS0 = grad_S0;
-    a.scratch = reinterpret_cast<float*>(ws + lay.slab);
-    a.work = reinterpret_cast<int32_t*>(ws + lay.work);
+    a.rec = reinterpret_cast<float*>(ws + fwd.copies);  // the forward's copies and images are dead now
+    a.xbuf = reinterpret_cast<float*>(ws + lay.xbuf);
+    a.u_scratch = grad_q;
     a.num_seqs = num_seqs;
     a.H = H;
-    if (cudaMemsetAsync(a.work, 0, 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (cols < kHeadDim && have_tokens) {  // row sums are accumulated over the slices
-        if (cudaMemsetAsync(grad_q, 0, nqk * 4, stream) != cudaSuccess ||
-            cudaMemsetAsync(grad_k, 0, nqk * 4, stream) != cudaSuccess ||
-            cudaMemsetAsync(grad_log_alpha, 0, nqk * 4, stream) != cudaSuccess ||
-            cudaMemsetAsync(grad_beta, 0, nb * 4, stream) != cudaSuccess)
-            return KDA_ERR_CUDA;
-    }
-    return kda::launch_backward(a, qkv_dtype == KDA_DTYPE_F32, cols, ctas, stream) == cudaSuccess ? KDA_OK
-                                                                                                 : KDA_ERR_CUDA;
+    return kda::launch_backward(a, qkv_dtype == KDA_DTYPE_F32, lay.entries, stream) == cudaSuccess ? KDA_OK
+                                                                                                  : KDA_ERR_CUDA;
 }
 
 }  // extern "C"

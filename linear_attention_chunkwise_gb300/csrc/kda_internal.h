@@ -109,7 +109,7 @@ struct BackwardArgs {
     const int32_t* cu_seqlens = nullptr;
     const int32_t* order = nullptr;      // sequences, longest first
     const int32_t* chunk_off = nullptr;  // chunk table
-    const float* ckpt = nullptr;         // state after every chunk: entry chunk_off[n] + c
+    const float* ckpt = nullptr;         // state after every chunk: entry (chunk_off[n] + c) x H + h
     const void* dO = nullptr;
     const float* dS_final = nullptr;
     float* dq = nullptr;
@@ -118,18 +118,17 @@ struct BackwardArgs {
     float* dla = nullptr;
     float* dbeta = nullptr;
     float* dS0 = nullptr;
-    float* scratch = nullptr;  // per-CTA slab of backward_slab_bytes(cols)
-    int32_t* work = nullptr;   // work counter, zero before the launch
+    float* rec = nullptr;        // per-(chunk, head) records of the prep kernel (backward_record_bytes each)
+    float* xbuf = nullptr;       // adjoint of the state after every chunk, indexed like ckpt
+    float* u_scratch = nullptr;  // [T, H, 128] rows u_t between the value and key kernels (may be dq)
     int32_t num_seqs = 0;
     int32_t H = 0;
 };
-// Scratch slab of one backward CTA that owns `cols` columns of a head's state.
-size_t backward_slab_bytes(int cols);
+size_t backward_record_bytes();
 // Snapshot entries at every chunk end (and sentinels up to max_entries) from the chunk table.
 cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_off, int32_t N, int32_t max_entries,
                                 int32_t* snap_seq, int32_t* snap_pos, cudaStream_t stream);
-// cols = 128, 64 or 32 state columns per CTA; with fewer than 128 the row sums
-// (dq, dk, dla, dbeta) are added atomically and must be zeroed first.
-cudaError_t launch_backward(const BackwardArgs& a, bool f32_io, int32_t cols, int32_t ctas, cudaStream_t stream);
+// prep, scan, value and key kernels; chunk_slots bounds the batch's chunk count.
+cudaError_t launch_backward(const BackwardArgs& a, bool f32_io, int64_t chunk_slots, cudaStream_t stream);
 
 }  // namespace kda

@@ -230,14 +230,19 @@ def test_decode_multi_rejects_bad_arguments(lib, over, expect):
 
 
 def test_backward_workspace_bytes(lib):
-    # two-pass prefill workspace, o scratch, snapshot entries (ceil(T/64) + N per head, 64 KB each),
-    # a work counter and one 4 MB slab per (sequence, head) up to 256
-    T, H, N = 128, 2, 1
-    fwd = 256 + 256 + (2 + 1) * H * BLOB
-    want = fwd + T * H * 128 * 2 + 256 + 256 + (2 + 1) * H * 65536 + 256 + N * H * 64 * 128 * 128 * 4
-    assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H) == want
-    big = kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32)
-    assert big > 256 * 64 * 128 * 128 * 4  # slabs capped at 256
+    # schedule + chunk table, then the larger of the forward's operand images and the backward's
+    # per-chunk records (147,968 B per chunk-head), o scratch, snapshot entries, and two states
+    # (the state and its adjoint) per chunk slot and head; chunk slots = ceil(T/64) + N
+    REC = 147968
+    for T, H, N in ((128, 2, 1), (1000, 32, 16)):
+        slots = -(-T // 64) + N
+        o = max(512 + slots * H * BLOB, 512 + slots * H * REC) if N == 1 else \
+            max(256 * ((N * 4 + 255) // 256) + 256 * (((N + 3) * 4 + 255) // 256) + slots * H * BLOB,
+                256 * ((N * 4 + 255) // 256) + 256 * (((N + 3) * 4 + 255) // 256) + slots * H * REC)
+        o = -(-o // 256) * 256
+        ent = -(-(slots * 4) // 256) * 256
+        want = o + -(-(T * H * 128 * 2) // 256) * 256 + 2 * ent + 2 * slots * H * 128 * 128 * 4
+        assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H) == want
     assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
     assert kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, 1, 10, 2, 64, 128) == 0
 

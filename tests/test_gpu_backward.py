@@ -4,10 +4,9 @@ The oracle's gradient (oracle.kda_prefill_backward) is itself pinned by
 finite differences of the forward oracle (tests/test_oracle_backward_pins.py).
 Here the CUDA path is compared with it element by element, all six gradients
 (q, k, v, log_alpha, beta, S0) at rel-L2 <= 1e-2, on the same seeded inputs:
-varlen batches with empty, one-token and ragged sequences; each of the three
-column splits of the state (the CTA count depends on heads x sequences
-against the SM count); fp32 and bf16 inputs; no grad_S_final; and the 8k-token
-32-head workload on two sampled heads (heads are independent, so the oracle on
+varlen batches with empty, one-token and ragged sequences; several head
+counts; fp32 and bf16 inputs; no grad_S_final; bitwise repeatability; and the
+8k-token 32-head workload on two sampled heads (heads are independent, so the oracle on
 those heads alone gives their exact gradients).
 """
 import numpy as np
@@ -73,12 +72,9 @@ def test_backward_varlen_matches_oracle(dtype):
     _compare(got, _oracle(p, dO, dSf))
 
 
-@pytest.mark.parametrize("slices", [4, 2, 1])
-def test_backward_each_column_split(slices):
-    """heads chosen so the library splits each state over 4, 2 or 1 CTAs on this GPU."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    H = {4: max(1, sms // 4), 2: sms // 2, 1: sms}[slices]
-    p = synth.prefill_inputs([150], H=H, s0_std=0.02, seed=43 + slices)
+@pytest.mark.parametrize("H", [1, 5, 40])
+def test_backward_head_counts(H):
+    p = synth.prefill_inputs([150], H=H, s0_std=0.02, seed=43 + H)
     dO, dSf = _cotangents(p, 44)
     _compare(_gpu(p, dO, dSf), _oracle(p, dO, dSf))
 
@@ -103,10 +99,9 @@ def test_backward_no_tokens_passes_final_gradient_through():
     assert all(g.numel() == 0 for g in got[:5])
 
 
-def test_backward_repeatable_single_split():
-    """With one CTA per head (no atomics) two calls give identical bits."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    p = synth.prefill_inputs([100], H=sms, s0_std=0.02, seed=48)
+def test_backward_is_deterministic():
+    """No atomics anywhere: two calls give identical bits."""
+    p = synth.prefill_inputs([100, 300], H=4, s0_std=0.02, seed=48)
     dO, dSf = _cotangents(p, 49)
     a = _gpu(p, dO, dSf)
     b = _gpu(p, dO, dSf)
