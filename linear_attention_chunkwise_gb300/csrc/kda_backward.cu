@@ -51,13 +51,13 @@ constexpr int NCS = 32;       // state columns per scan CTA
 constexpr int kSlices = D / NCS;
 
 // per-(chunk, head) record of the prep kernel (fp32)
-constexpr int kRecWbc = 0;        // [64][128] Tb^T Kb Diag(e^{gC-gm})
-constexpr int kRecDY0 = 8192;     // [64][128] -Tb^T Mm^T dO
-constexpr int kRecQhm = 16384;    // [64][128] Qh Diag(e^{gm})
-constexpr int kRecKhm = 24576;    // [64][128] Kh Diag(e^{gm})
-constexpr int kRecTb = 32768;     // [64][64]  Tb
-constexpr int kRecGam = 36864;    // [128]     e^{gC}
-constexpr int kRecFloats = 36992;
+constexpr int kRecWbc = 0;        // [64][128]  Tb^T Kb Diag(e^{gC-gm})
+constexpr int kRecDY0 = 8192;     // [64][128]  -Tb^T Mm^T dO
+constexpr int kRecKhm = 16384;    // [64][128]  Kh Diag(e^{gm})
+constexpr int kRecP = 24576;      // [128][128] Diag(e^{gm}) Qh^T dO
+constexpr int kRecTb = 40960;     // [64][64]   Tb
+constexpr int kRecGam = 45056;    // [128]      e^{gC}
+constexpr int kRecFloats = 45184;
 
 template <typename T>
 __device__ __forceinline__ float4 ld4(const T* p);
@@ -80,110 +80,135 @@ __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) { re
 __device__ __forceinline__ float comp(const float4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
 // ---- products on shared tiles ---------------------------------------------------------------
-// Every product accumulates a 64-row output in the same thread layout: thread (rb = tid >> 4,
-// cb = tid & 15) owns rows 4 rb + y (y < 4) and columns cb + 16 x (x < NX).
-//   nn: C += A B     A[m][k] (k contiguous), B[k][n] (n contiguous)
-//   tn: C += At^T B  At[k][m], B[k][n]
-//   nt: C += A Bt^T  A[m][k], Bt[n][k]   (Bt's stride = 4 mod 32 floats)
-template <int NX>
-__device__ __forceinline__ void g_nn(float (&acc)[4][NX], const float* A, int lda, const float* B, int ldb, int K,
-                                     int rb, int cb) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[4];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) a[y] = *reinterpret_cast<const float4*>(A + (4 * rb + y) * lda + k);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            float b[NX];
-#pragma unroll
-            for (int x = 0; x < NX; ++x) b[x] = B[(k + kk) * ldb + cb + 16 * x];
-#pragma unroll
-            for (int y = 0; y < 4; ++y)
-#pragma unroll
-                for (int x = 0; x < NX; ++x) acc[y][x] = fmaf(comp(a[y], kk), b[x], acc[y][x]);
-        }
-    }
-}
-template <int NX>
-__device__ __forceinline__ void g_tn(float (&acc)[4][NX], const float* At, int lda, const float* B, int ldb, int K,
-                                     int rb, int cb) {
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        const float4 a = *reinterpret_cast<const float4*>(At + k * lda + 4 * rb);
-        float b[NX];
-#pragma unroll
-        for (int x = 0; x < NX; ++x) b[x] = B[k * ldb + cb + 16 * x];
-#pragma unroll
-        for (int x = 0; x < NX; ++x) {
-            acc[0][x] = fmaf(a.x, b[x], acc[0][x]);
-            acc[1][x] = fmaf(a.y, b[x], acc[1][x]);
-            acc[2][x] = fmaf(a.z, b[x], acc[2][x]);
-            acc[3][x] = fmaf(a.w, b[x], acc[3][x]);
-        }
-    }
-}
-template <int NX>
-__device__ __forceinline__ void g_nt(float (&acc)[4][NX], const float* A, int lda, const float* Bt, int ldb, int K,
-                                     int rb, int cb) {
-#pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
-        float4 a[4], b[NX];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) a[y] = *reinterpret_cast<const float4*>(A + (4 * rb + y) * lda + k);
-#pragma unroll
-        for (int x = 0; x < NX; ++x) b[x] = *reinterpret_cast<const float4*>(Bt + (cb + 16 * x) * ldb + k);
-#pragma unroll
-        for (int y = 0; y < 4; ++y)
-#pragma unroll
-            for (int x = 0; x < NX; ++x) {
-                float s = acc[y][x];
-                s = fmaf(a[y].x, b[x].x, s);
-                s = fmaf(a[y].y, b[x].y, s);
-                s = fmaf(a[y].z, b[x].z, s);
-                s = fmaf(a[y].w, b[x].w, s);
-                acc[y][x] = s;
-            }
-    }
-}
-template <int NX>
-__device__ __forceinline__ void zero(float (&acc)[4][NX]) {
-#pragma unroll
-    for (int y = 0; y < 4; ++y)
-#pragma unroll
-        for (int x = 0; x < NX; ++x) acc[y][x] = 0.f;
+// Tensor-core products of fp32 shared tiles: operands rounded to tf32 (cvt.rna), fp32 accumulate,
+// mma.sync m16n8k8.  One warp owns 16 output rows from r0 and NT 8-column tiles from c0; its
+// accumulator acc[j][e] holds row r0 + g + 8 (e >> 1), column c0 + 8 j + 2 t + (e & 1)
+// (g = lane >> 2, t = lane & 3).  Operand element addressing:
+//   AR: A(m, k) = A[m * lda + k]     AC: A(m, k) = A[k * lda + m]
+//   BK: B(k, n) = B[k * ldb + n]     BN: B(k, n) = B[n * ldb + k]
+enum { AR = 0, AC = 1, BK = 0, BN = 1 };
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int NT, int AM, int BM>
+__device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int lda, const float* B, int ldb, int K,
+                                      int r0, int c0, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t a[4];
+        if (AM == AR) {
+            a[0] = to_tf32(A[(r0 + g) * lda + k0 + t]);
+            a[1] = to_tf32(A[(r0 + g + 8) * lda + k0 + t]);
+            a[2] = to_tf32(A[(r0 + g) * lda + k0 + t + 4]);
+            a[3] = to_tf32(A[(r0 + g + 8) * lda + k0 + t + 4]);
+        } else {
+            a[0] = to_tf32(A[(k0 + t) * lda + r0 + g]);
+            a[1] = to_tf32(A[(k0 + t) * lda + r0 + g + 8]);
+            a[2] = to_tf32(A[(k0 + t + 4) * lda + r0 + g]);
+            a[3] = to_tf32(A[(k0 + t + 4) * lda + r0 + g + 8]);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int n = c0 + 8 * j + g;
+            const uint32_t b0 = to_tf32(BM == BK ? B[(k0 + t) * ldb + n] : B[n * ldb + k0 + t]);
+            const uint32_t b1 = to_tf32(BM == BK ? B[(k0 + t + 4) * ldb + n] : B[n * ldb + k0 + t + 4]);
+            mma_tf32(acc[j], a, b0, b1);
+        }
+    }
+}
+template <int NT>
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+}
+// coordinates of accumulator element (j, e)
+__device__ __forceinline__ int frow(int r0, int lane, int e) { return r0 + (lane >> 2) + 8 * (e >> 1); }
+__device__ __forceinline__ int fcol(int c0, int lane, int j, int e) { return c0 + 8 * j + 2 * (lane & 3) + (e & 1); }
+
 // ---- loads ------------------------------------------------------------------------------------
-// rows [t0, t0 + L) of a [T, H, 128] tensor, head h -> fp32 tile (stride LDW), rows >= L zero
+// rows [t0, t0 + L) of a [T, H, 128] tensor, head h -> fp32 tile (stride LDW), rows >= L zero.
+// Constant trip counts: every thread's loads are in flight together.
 template <typename T>
 __device__ __forceinline__ void load_tile(float* dst, const T* src, int64_t t0, int L, int H, int h, int tid,
                                           float scale = 1.f) {
-    for (int e = tid; e < C * (D / 4); e += BT) {
-        const int r = e >> 5, c4 = (e & 31) * 4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < L) {
-            v = ld4(src + (static_cast<size_t>(t0 + r) * H + h) * D + c4);
-            v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
-        }
-        *reinterpret_cast<float4*>(dst + r * LDW + c4) = v;
+    constexpr int IT = C * (D / 4) / BT;  // 8
+    float4 v[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
+        v[it] = r < L ? ld4(src + (static_cast<size_t>(t0 + r) * H + h) * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
+        *reinterpret_cast<float4*>(dst + r * LDW + c4) =
+            make_float4(v[it].x * scale, v[it].y * scale, v[it].z * scale, v[it].w * scale);
     }
 }
-// [64][128] fp32 record section -> tile (stride LDW)
-__device__ __forceinline__ void load_rec(float* dst, const float* src, int tid) {
-    for (int e = tid; e < C * (D / 4); e += BT) {
-        const int r = e >> 5, c4 = (e & 31) * 4;
-        *reinterpret_cast<float4*>(dst + r * LDW + c4) = *reinterpret_cast<const float4*>(src + r * D + c4);
+// ROWS x 128 fp32 rows of a state (stride 128) starting at row i0, each row scaled by sc[row],
+// -> tile (stride LDW)
+template <int ROWS>
+__device__ __forceinline__ void load_state_rows(float* dst, const float* S, int i0, const float* sc, int tid) {
+    constexpr int IT = ROWS * (D / 4) / BT;
+    float4 v[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT;
+        v[it] = *reinterpret_cast<const float4*>(S + (i0 + (e >> 5)) * D + (e & 31) * 4);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, r = e >> 5;
+        const float f = sc[i0 + r];
+        *reinterpret_cast<float4*>(dst + r * LDW + (e & 31) * 4) =
+            make_float4(v[it].x * f, v[it].y * f, v[it].z * f, v[it].w * f);
+    }
+}
+// 32 columns j0 .. j0+31 of all 128 rows of a state, row i scaled by sc[i] -> [128][LDS] tile
+__device__ __forceinline__ void load_state_cols(float* dst, const float* S, int j0, const float* sc, int tid) {
+    constexpr int IT = D * 8 / BT;  // 4
+    float4 v[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT;
+        v[it] = *reinterpret_cast<const float4*>(S + (e >> 3) * D + j0 + (e & 7) * 4);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, i = e >> 3;
+        const float f = sc[i];
+        *reinterpret_cast<float4*>(dst + i * LDS + (e & 7) * 4) =
+            make_float4(v[it].x * f, v[it].y * f, v[it].z * f, v[it].w * f);
     }
 }
 
-// cumulative log-decay of the chunk (rows >= L hold gC), by 128 threads; e^{gm}, e^{gC - gm} to vectors
+// Cumulative log-decay of the chunk into G (rows >= L hold gC): log_alpha staged through G, then
+// summed down the rows by 128 threads.  e^{gm}, e^{gC - gm} (and e^{gC}) to vectors.  Contains a
+// barrier: every thread of the CTA calls it.
 __device__ __forceinline__ void chunk_gates(float* G, const float* la, int64_t t0, int L, int H, int h, int tid,
                                             float* egm, float* egcm, float* egc) {
+    load_tile(G, la, t0, L, H, h, tid);
+    __syncthreads();
     if (tid < D) {
         float s = 0.f, gm = 0.f;
+#pragma unroll 8
         for (int r = 0; r < C; ++r) {
-            if (r < L) s += la[(static_cast<size_t>(t0 + r) * H + h) * D + tid];
+            s += G[r * LDW + tid];
             G[r * LDW + tid] = s;
             if (r == C / 2 - 1) gm = s;
         }
@@ -240,7 +265,8 @@ template <typename IoT>
 __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs a) {
     extern __shared__ __align__(16) float sm[];
     using L = PrepL;
-    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
     const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
     ChunkPos p;
     if (!chunk_pos(a, gc, p)) return;
@@ -270,24 +296,35 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
         float ak[4][4], aq[4][4];
         zero(ak);
         zero(aq);
-        g_nt<4>(ak, KH, LDW, KB, LDW, D, rb, cb);
-        g_nt<4>(aq, QH, LDW, KB, LDW, D, rb, cb);
+        mma16<4, AR, BN>(ak, KH, LDW, KB, LDW, D, r0, c64, lane);
+        mma16<4, AR, BN>(aq, QH, LDW, KB, LDW, D, r0, c64, lane);
         __syncthreads();  // g scratch (over NF..MM) is dead
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int r = 4 * rb + y, s = cb + 16 * x;
-                pf::m1(NF, r, s) = s < r ? bet[r] * ak[y][x] : 0.f;
-                MM[r * LDN + s] = s <= r ? aq[y][x] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(r0, lane, e), s = fcol(c64, lane, j, e);
+                pf::m1(NF, r, s) = s < r ? bet[r] * ak[j][e] : 0.f;
+                MM[r * LDN + s] = s <= r ? aq[j][e] : 0.f;
             }
     }
-    for (int e = tid; e < C * D; e += BT) {  // Qh, Kh scaled by e^{gm} for the scan
+    for (int e = tid; e < C * D; e += BT) {  // Kh Diag(e^{gm}) for the scan
         const int r = e >> 7, i = e & 127;
-        rec[kRecQhm + e] = QH[r * LDW + i] * egm[i];
         rec[kRecKhm + e] = KH[r * LDW + i] * egm[i];
     }
     if (tid < D) rec[kRecGam + tid] = egc[tid];
+    for (int half = 0; half < 2; ++half) {  // P = Diag(e^{gm}) Qh^T dO (128 x 128)
+        float acc[8][4];
+        zero(acc);
+        mma16<8, AC, BK>(acc, QH + 64 * half, LDW, DO, LDW, C, r0, c128, lane);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 64 * half + frow(r0, lane, e), col = fcol(c128, lane, j, e);
+                rec[kRecP + i * D + col] = egm[i] * acc[j][e];
+            }
+    }
     __syncthreads();
     pf::lower_inverse(NF, TF, XS, tid);  // T = (I + N)^-1, ends synchronised
     for (int e = tid; e < C * C; e += BT) {
@@ -298,133 +335,149 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
     }
     __syncthreads();
     {   // Wbc = Tb^T Kb Diag(e^{gC-gm});  MdO = Mm^T dO (into QH)
-        float acc[4][8], md[4][8];
+        float acc[8][4], md[8][4];
         zero(acc);
         zero(md);
-        g_tn<8>(acc, TB, LDN, KB, LDW, C, rb, cb);
-        g_tn<8>(md, MM, LDN, DO, LDW, C, rb, cb);
+        mma16<8, AC, BK>(acc, TB, LDN, KB, LDW, C, r0, c128, lane);
+        mma16<8, AC, BK>(md, MM, LDN, DO, LDW, C, r0, c128, lane);
         __syncthreads();  // QH is read no more
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const int r = 4 * rb + y, i = cb + 16 * x;
-                rec[kRecWbc + r * D + i] = acc[y][x] * egcm[i];
-                QH[r * LDW + i] = md[y][x];
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
+                rec[kRecWbc + r * D + i] = acc[j][e] * egcm[i];
+                QH[r * LDW + i] = md[j][e];
             }
     }
     __syncthreads();
     {   // dY0 = -Tb^T MdO
-        float acc[4][8];
+        float acc[8][4];
         zero(acc);
-        g_tn<8>(acc, TB, LDN, QH, LDW, C, rb, cb);
+        mma16<8, AC, BK>(acc, TB, LDN, QH, LDW, C, r0, c128, lane);
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int x = 0; x < 8; ++x) rec[kRecDY0 + (4 * rb + y) * D + cb + 16 * x] = -acc[y][x];
+            for (int e = 0; e < 4; ++e)
+                rec[kRecDY0 + frow(r0, lane, e) * D + fcol(c128, lane, j, e)] = -acc[j][e];
     }
 }
 
 // ================================================================ scan ==========
+// Per chunk (from the prep record): dY = dY0 - Wbc X;  X <- Diag(e^{gC}) X + P + Khm^T dY.
+// The next chunk's record slices are prefetched (cp.async) while this one is computed.
 struct ScanL {
     static constexpr int WB = 0;                 // [64][LDW]   Wbc
-    static constexpr int QK = TILE;              // [128][LDW]  [Qhm; Khm]
-    static constexpr int BB = QK + 2 * TILE;     // [128][LDS]  [dO; dY] (this CTA's columns)
-    static constexpr int Y0 = BB + 128 * LDS;    // [64][LDS]   dY0
-    static constexpr int XS = Y0 + 64 * LDS;     // [128][LDS]  X
-    static constexpr int GM = XS + 128 * LDS;    // [128]       e^{gC}
-    static constexpr int FLOATS = GM + 128;
+    static constexpr int KM = TILE;              // [64][LDW]   Khm
+    static constexpr int PS = 2 * TILE;          // [128][LDS]  P, this CTA's columns
+    static constexpr int Y0 = PS + 128 * LDS;    // [64][LDS]   dY0, this CTA's columns
+    static constexpr int GM = Y0 + 64 * LDS;     // [128]       e^{gC}
+    static constexpr int STAGE = GM + 128;
+    static constexpr int XS = 2 * STAGE;         // [128][LDS]  X
+    static constexpr int DY = XS + 128 * LDS;    // [64][LDS]   dY
+    static constexpr int FLOATS = DY + 64 * LDS;
 };
+
+__device__ __forceinline__ void cp16(float* dst, const float* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void scan_fetch(float* st, const float* rec, int c0, int tid) {
+    for (int e = tid; e < C * (D / 4); e += BT) {
+        const int r = e >> 5, c4 = (e & 31) * 4;
+        cp16(st + ScanL::WB + r * LDW + c4, rec + kRecWbc + r * D + c4);
+        cp16(st + ScanL::KM + r * LDW + c4, rec + kRecKhm + r * D + c4);
+    }
+    for (int e = tid; e < D * (NCS / 4); e += BT) {
+        const int r = e >> 3, c4 = (e & 7) * 4;
+        cp16(st + ScanL::PS + r * LDS + c4, rec + kRecP + r * D + c0 + c4);
+        if (r < C) cp16(st + ScanL::Y0 + r * LDS + c4, rec + kRecDY0 + r * D + c0 + c4);
+    }
+    if (tid < D / 4) cp16(st + ScanL::GM + 4 * tid, rec + kRecGam + 4 * tid);
+}
 
 template <typename IoT>
 __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs a) {
     extern __shared__ __align__(16) float sm[];
     using L = ScanL;
-    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, N = a.num_seqs;
     if (a.chunk_off[N + 1] == 0) return;
     const int unit = blockIdx.x;  // (rank of the sequence, longest first) x H x slices
     const int n = a.order[unit / (H * kSlices)], h = (unit / kSlices) % H, c0 = (unit % kSlices) * NCS;
-    float *WB = sm + L::WB, *QK = sm + L::QK, *BB = sm + L::BB, *Y0 = sm + L::Y0, *XS = sm + L::XS,
-          *GM = sm + L::GM;
+    float *XS = sm + L::XS, *DY = sm + L::DY;
     const size_t sidx = (static_cast<size_t>(n) * H + h) * D * D;
-    float X[2][4][2];  // rows 64 z + 4 rb + y, columns c0 + cb + 16 x
+    // X rows 16 warp + g (+8), columns 8 j + 2 t (+1) of this CTA's slice
+    float X[4][4];
 #pragma unroll
-    for (int z = 0; z < 2; ++z)
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-                X[z][y][x] = a.dS_final ? a.dS_final[sidx + (64 * z + 4 * rb + y) * D + c0 + cb + 16 * x] : 0.f;
+        for (int e = 0; e < 4; ++e)
+            X[j][e] = a.dS_final ? a.dS_final[sidx + frow(16 * warp, lane, e) * D + c0 + fcol(0, lane, j, e)] : 0.f;
     const int base = a.chunk_off[n], nch = a.chunk_off[n + 1] - base;
     const int64_t tb = a.cu_seqlens[n], te = a.cu_seqlens[n + 1];
-    for (int c = nch - 1; c >= 0; --c) {
+    auto rec_of = [&](int c) { return a.rec + (static_cast<size_t>(base + c) * H + h) * kRecFloats; };
+    if (nch > 0) scan_fetch(sm, rec_of(nch - 1), c0, tid);
+    cp_commit();
+    for (int c = nch - 1, s = 0; c >= 0; --c, s ^= 1) {
         const int gc = base + c;
         const int64_t t0 = tb + static_cast<int64_t>(c) * C;
         const int Lr = static_cast<int>(te - t0 < C ? te - t0 : C);
-        const float* rec = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats;
-        __syncthreads();  // the previous chunk's shared data is read no more
+        float* st = sm + s * L::STAGE;
+        __syncthreads();  // the other stage and XS / DY are read no more
+        if (c > 0) scan_fetch(sm + (s ^ 1) * L::STAGE, rec_of(c - 1), c0, tid);
+        cp_commit();
         float* xo = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
 #pragma unroll
-        for (int z = 0; z < 2; ++z)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int y = 0; y < 4; ++y)
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int r = 64 * z + 4 * rb + y, col = cb + 16 * x;
-                    XS[r * LDS + col] = X[z][y][x];
-                    xo[r * D + c0 + col] = X[z][y][x];
-                }
-        load_rec(WB, rec + kRecWbc, tid);
-        load_rec(QK, rec + kRecQhm, tid);
-        load_rec(QK + TILE, rec + kRecKhm, tid);
-        for (int e = tid; e < C * (NCS / 4); e += BT) {
-            const int r = e >> 3, c4 = (e & 7) * 4;
-            *reinterpret_cast<float4*>(Y0 + r * LDS + c4) =
-                *reinterpret_cast<const float4*>(rec + kRecDY0 + r * D + c0 + c4);
-            float4 d = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < Lr) d = ld4(static_cast<const IoT*>(a.dO) + (static_cast<size_t>(t0 + r) * H + h) * D + c0 + c4);
-            *reinterpret_cast<float4*>(BB + r * LDS + c4) = d;
-        }
-        if (tid < D) GM[tid] = rec[kRecGam + tid];
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(16 * warp, lane, e), col = fcol(0, lane, j, e);
+                XS[r * LDS + col] = X[j][e];
+                xo[r * D + c0 + col] = X[j][e];
+            }
+        cp_wait<1>();  // this chunk's stage has landed
         __syncthreads();
-        {   // dY = dY0 - Wbc X
-            float acc[4][2];
+        {   // dY = dY0 - Wbc X  (64 x 32: warp rows 16 (warp & 3), columns 16 (warp >> 2))
+            const int r0 = 16 * (warp & 3), cc = 16 * (warp >> 2);
+            float acc[2][4];
             zero(acc);
-            g_nn<2>(acc, WB, LDW, XS, LDS, D, rb, cb);
+            mma16<2, AR, BK>(acc, st + L::WB, LDW, XS, LDS, D, r0, cc, lane);
 #pragma unroll
-            for (int y = 0; y < 4; ++y)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int r = 4 * rb + y, col = cb + 16 * x;
-                    const float dy = Y0[r * LDS + col] - acc[y][x];
-                    BB[(C + r) * LDS + col] = dy;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(r0, lane, e), col = fcol(cc, lane, j, e);
+                    const float dy = st[L::Y0 + r * LDS + col] - acc[j][e];
+                    DY[r * LDS + col] = dy;
                     if (r < Lr) a.dv[(static_cast<size_t>(t0 + r) * H + h) * D + c0 + col] = -dy;
                 }
         }
         __syncthreads();
-        {   // X <- Diag(e^{gC}) X + [Qhm; Khm]^T [dO; dY]
-            float lo[4][2], hi[4][2];
-            zero(lo);
-            zero(hi);
-            g_tn<2>(lo, QK, LDW, BB, LDS, 2 * C, rb, cb);
-            g_tn<2>(hi, QK + 64, LDW, BB, LDS, 2 * C, rb, cb);
+        {   // X <- Diag(e^{gC}) X + P + Khm^T dY
+            float acc[4][4];
+            zero(acc);
+            mma16<4, AC, BK>(acc, st + L::KM, LDW, DY, LDS, C, 16 * warp, 0, lane);
 #pragma unroll
-            for (int y = 0; y < 4; ++y)
+            for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    X[0][y][x] = fmaf(GM[4 * rb + y], X[0][y][x], lo[y][x]);
-                    X[1][y][x] = fmaf(GM[64 + 4 * rb + y], X[1][y][x], hi[y][x]);
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(16 * warp, lane, e), col = fcol(0, lane, j, e);
+                    X[j][e] = fmaf(st[L::GM + r], X[j][e], st[L::PS + r * LDS + col] + acc[j][e]);
                 }
         }
     }
+    cp_wait<0>();
     if (a.dS0) {
 #pragma unroll
-        for (int z = 0; z < 2; ++z)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int y = 0; y < 4; ++y)
-#pragma unroll
-                for (int x = 0; x < 2; ++x) a.dS0[sidx + (64 * z + 4 * rb + y) * D + c0 + cb + 16 * x] = X[z][y][x];
+            for (int e = 0; e < 4; ++e)
+                a.dS0[sidx + frow(16 * warp, lane, e) * D + c0 + fcol(0, lane, j, e)] = X[j][e];
     }
 }
 
@@ -433,8 +486,8 @@ struct ValueL {
     static constexpr int T0 = 0, T1 = TILE, T2 = 2 * TILE, T3 = 3 * TILE;
     static constexpr int P0 = 4 * TILE, P1 = P0 + PTILE;
     static constexpr int ST = P1 + PTILE;        // [32][LDW] state slab, or Tb [64][LDN]
-    static constexpr int VB = ST + PTILE;        // egm[128], egcm[128]
-    static constexpr int FLOATS = VB + 256;
+    static constexpr int VB = ST + PTILE;        // egm[128], egcm[128], dbeta halves [2][64]
+    static constexpr int FLOATS = VB + 384;
 };
 static_assert(32 * LDW <= PTILE, "state slab fits the Tb slot");
 
@@ -442,12 +495,13 @@ template <typename IoT>
 __global__ void __launch_bounds__(BT, 1) kda_bwd_value_kernel(const BackwardArgs a) {
     extern __shared__ __align__(16) float sm[];
     using L = ValueL;
-    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
     const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
     ChunkPos p;
     if (!chunk_pos(a, gc, p)) return;
     float *T0 = sm + L::T0, *T1 = sm + L::T1, *T2 = sm + L::T2, *T3 = sm + L::T3, *P0 = sm + L::P0,
-          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128;
+          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128, *dbh = egcm + 128;
     const IoT* k = static_cast<const IoT*>(a.k);
 
     load_tile(T1, k, p.t0, p.L, H, h, tid);
@@ -467,109 +521,106 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_kernel(const BackwardArgs
         float al[4][4], am[4][4];
         zero(al);
         zero(am);
-        g_nt<4>(al, T0, LDW, T1, LDW, D, rb, cb);
-        g_nt<4>(am, T2, LDW, T1, LDW, D, rb, cb);
+        mma16<4, AR, BN>(al, T0, LDW, T1, LDW, D, r0, c64, lane);
+        mma16<4, AR, BN>(am, T2, LDW, T1, LDW, D, r0, c64, lane);
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int r = 4 * rb + y, s = cb + 16 * x;
-                P0[r * LDN + s] = s < r ? al[y][x] : 0.f;
-                P1[r * LDN + s] = s <= r ? am[y][x] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(r0, lane, e), s = fcol(c64, lane, j, e);
+                P0[r * LDN + s] = s < r ? al[j][e] : 0.f;
+                P1[r * LDN + s] = s <= r ? am[j][e] : 0.f;
             }
     }
     // Kh Sm, the start state streamed in 32-row slabs
-    float acc[4][8];
+    float acc[8][4];
     zero(acc);
     const float* S = chunk_start_state(a, p, gc, h);
     if (S) {
         for (int i0 = 0; i0 < D; i0 += 32) {
             __syncthreads();
-            for (int e = tid; e < 32 * (D / 4); e += BT) {
-                const int r = e >> 5, c4 = (e & 31) * 4;
-                float4 v = *reinterpret_cast<const float4*>(S + (i0 + r) * D + c4);
-                const float s = egm[i0 + r];
-                v.x *= s; v.y *= s; v.z *= s; v.w *= s;
-                *reinterpret_cast<float4*>(ST + r * LDW + c4) = v;
-            }
+            load_state_rows<32>(ST, S, i0, egm, tid);
             __syncthreads();
-            g_nn<8>(acc, T0 + i0, LDW, ST, LDW, 32, rb, cb);
+            mma16<8, AR, BK>(acc, T0 + i0, LDW, ST, LDW, 32, r0, c128, lane);
         }
     }
     __syncthreads();  // T2 (Qh) and ST are read no more
     load_tile(T2, static_cast<const IoT*>(a.v), p.t0, p.L, H, h, tid);
     {
         const float* tbg = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats + kRecTb;
-        for (int e = tid; e < C * (C / 4); e += BT) {
-            const int r = e >> 4, c4 = (e & 15) * 4;
+#pragma unroll
+        for (int it = 0; it < C * (C / 4) / BT; ++it) {
+            const int e = tid + it * BT, r = e >> 4, c4 = (e & 15) * 4;
             *reinterpret_cast<float4*>(ST + r * LDN + c4) = *reinterpret_cast<const float4*>(tbg + r * C + c4);
         }
     }
     __syncthreads();
-    float rr[4][8];  // Y1 = V - Kh Sm (own elements), later R
+    float rr[8][4];  // Y1 = V - Kh Sm (own elements), later R
 #pragma unroll
-    for (int y = 0; y < 4; ++y)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int r = 4 * rb + y, i = cb + 16 * x;
-            rr[y][x] = T2[r * LDW + i] - acc[y][x];
+        for (int e = 0; e < 4; ++e) {
+            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
+            rr[j][e] = T2[r * LDW + i] - acc[j][e];
         }
     __syncthreads();
 #pragma unroll
-    for (int y = 0; y < 4; ++y)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) T2[(4 * rb + y) * LDW + cb + 16 * x] = rr[y][x];
+        for (int e = 0; e < 4; ++e) T2[frow(r0, lane, e) * LDW + fcol(c128, lane, j, e)] = rr[j][e];
     __syncthreads();
     zero(acc);
-    g_nn<8>(acc, ST, LDN, T2, LDW, C, rb, cb);  // U = Tb Y1
+    mma16<8, AR, BK>(acc, ST, LDN, T2, LDW, C, r0, c128, lane);  // U = Tb Y1
 #pragma unroll
-    for (int y = 0; y < 4; ++y)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int r = 4 * rb + y, i = cb + 16 * x;
-            T3[r * LDW + i] = acc[y][x];
-            if (r < p.L) a.u_scratch[(static_cast<size_t>(p.t0 + r) * H + h) * D + i] = acc[y][x];
+        for (int e = 0; e < 4; ++e) {
+            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
+            T3[r * LDW + i] = acc[j][e];
+            if (r < p.L) a.u_scratch[(static_cast<size_t>(p.t0 + r) * H + h) * D + i] = acc[j][e];
         }
     __syncthreads();
     zero(acc);
-    g_nn<8>(acc, P0, LDN, T3, LDW, C, rb, cb);  // Lm U
+    mma16<8, AR, BK>(acc, P0, LDN, T3, LDW, C, r0, c128, lane);  // Lm U
 #pragma unroll
-    for (int y = 0; y < 4; ++y)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) rr[y][x] -= acc[y][x];  // R
+        for (int e = 0; e < 4; ++e) rr[j][e] -= acc[j][e];  // R
     __syncthreads();  // T2, T3 and ST are read no more
     load_tile(T2, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
     load_tile(T3, a.dv, p.t0, p.L, H, h, tid, -1.f);  // dY = -dv
     __syncthreads();
     zero(acc);
-    g_tn<8>(acc, P1, LDN, T2, LDW, C, rb, cb);  // Mm^T dO
-    g_tn<8>(acc, P0, LDN, T3, LDW, C, rb, cb);  // + Lm^T dY
+    mma16<8, AC, BK>(acc, P1, LDN, T2, LDW, C, r0, c128, lane);  // Mm^T dO
+    mma16<8, AC, BK>(acc, P0, LDN, T3, LDW, C, r0, c128, lane);  // + Lm^T dY
     {   // + Kb Xc, X streamed in 32-row slabs
         const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
         for (int i0 = 0; i0 < D; i0 += 32) {
             __syncthreads();
-            for (int e = tid; e < 32 * (D / 4); e += BT) {
-                const int r = e >> 5, c4 = (e & 31) * 4;
-                float4 v = *reinterpret_cast<const float4*>(X + (i0 + r) * D + c4);
-                const float s = egcm[i0 + r];
-                v.x *= s; v.y *= s; v.z *= s; v.w *= s;
-                *reinterpret_cast<float4*>(ST + r * LDW + c4) = v;
-            }
+            load_state_rows<32>(ST, X, i0, egcm, tid);
             __syncthreads();
-            g_nn<8>(acc, T1 + i0, LDW, ST, LDW, 32, rb, cb);
+            mma16<8, AR, BK>(acc, T1 + i0, LDW, ST, LDW, 32, r0, c128, lane);
         }
     }
-    // dbeta_t = <du_t, r_t>: the 16 threads of a row group share the rows
+    // dbeta_t = <du_t, r_t>: rows g, g + 8 of the warp; columns over the 4 threads of a group
+    // and the two warps (warp, warp + 4) that share the rows
+    float s_lo = 0.f, s_hi = 0.f;
 #pragma unroll
-    for (int y = 0; y < 4; ++y) {
-        float s = 0.f;
-#pragma unroll
-        for (int x = 0; x < 8; ++x) s = fmaf(acc[y][x], rr[y][x], s);
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        const int r = 4 * rb + y;
-        if (cb == 0 && r < p.L) a.dbeta[(p.t0 + r) * H + h] = s;
+    for (int j = 0; j < 8; ++j) {
+        s_lo = fmaf(acc[j][0], rr[j][0], fmaf(acc[j][1], rr[j][1], s_lo));
+        s_hi = fmaf(acc[j][2], rr[j][2], fmaf(acc[j][3], rr[j][3], s_hi));
     }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, off);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, off);
+    }
+    if ((lane & 3) == 0) {
+        dbh[(warp >> 2) * 64 + frow(r0, lane, 0)] = s_lo;
+        dbh[(warp >> 2) * 64 + frow(r0, lane, 2)] = s_hi;
+    }
+    __syncthreads();
+    if (tid < p.L) a.dbeta[(p.t0 + tid) * H + h] = dbh[tid] + dbh[64 + tid];
 }
 
 // ================================================================ key ===========
@@ -585,7 +636,8 @@ template <typename IoT>
 __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a) {
     extern __shared__ __align__(16) float sm[];
     using L = KeyL;
-    const int tid = threadIdx.x, rb = tid >> 4, cb = tid & 15;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
     const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
     ChunkPos p;
     if (!chunk_pos(a, gc, p)) return;
@@ -603,6 +655,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
         const float* Sn = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D;
         const int i = tid >> 1, j0 = (tid & 1) * 64;
         float s = 0.f;
+#pragma unroll
         for (int j = 0; j < 64; j += 4) {
             const float4 sv = *reinterpret_cast<const float4*>(Sn + i * D + j0 + j);
             const float4 xv = *reinterpret_cast<const float4*>(X + i * D + j0 + j);
@@ -616,18 +669,18 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
         float a0[4][4], a1[4][4];
         zero(a0);
         zero(a1);
-        g_nt<4>(a0, T0, LDW, T1, LDW, D, rb, cb);
-        g_nt<4>(a1, T1, LDW, T2, LDW, D, rb, cb);
+        mma16<4, AR, BN>(a0, T0, LDW, T1, LDW, D, r0, c64, lane);
+        mma16<4, AR, BN>(a1, T1, LDW, T2, LDW, D, r0, c64, lane);
 #pragma unroll
-        for (int y = 0; y < 4; ++y)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int r = 4 * rb + y, s = cb + 16 * x;
-                P0[r * LDN + s] = s <= r ? a0[y][x] : 0.f;
-                P1[r * LDN + s] = s > r ? a1[y][x] : 0.f;
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(r0, lane, e), s = fcol(c64, lane, j, e);
+                P0[r * LDN + s] = s <= r ? a0[j][e] : 0.f;
+                P1[r * LDN + s] = s > r ? a1[j][e] : 0.f;
             }
     }
-    float aq[4][8], aka[4][8], akb[4][8];
+    float aq[8][4], aka[8][4], akb[8][4];
     zero(aq);
     zero(aka);
     zero(akb);
@@ -638,19 +691,13 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
         const float* sc = pass == 0 ? egm : egcm;
         for (int j0 = 0; j0 < D; j0 += 32) {
             __syncthreads();
-            for (int e = tid; e < D * 8; e += BT) {
-                const int i = e >> 3, c4 = (e & 7) * 4;
-                float4 v = *reinterpret_cast<const float4*>(M + i * D + j0 + c4);
-                const float s = sc[i];
-                v.x *= s; v.y *= s; v.z *= s; v.w *= s;
-                *reinterpret_cast<float4*>(ST + i * LDS + c4) = v;
-            }
+            load_state_cols(ST, M, j0, sc, tid);
             __syncthreads();
             if (pass == 0) {
-                g_nt<8>(aq, T0 + j0, LDW, ST, LDS, 32, rb, cb);
-                g_nt<8>(akb, T2 + j0, LDW, ST, LDS, 32, rb, cb);
+                mma16<8, AR, BN>(aq, T0 + j0, LDW, ST, LDS, 32, r0, c128, lane);
+                mma16<8, AR, BN>(akb, T2 + j0, LDW, ST, LDS, 32, r0, c128, lane);
             } else {
-                g_nt<8>(aka, T1 + j0, LDW, ST, LDS, 32, rb, cb);
+                mma16<8, AR, BN>(aka, T1 + j0, LDW, ST, LDS, 32, r0, c128, lane);
             }
         }
     }
@@ -667,19 +714,19 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
         T1[r * LDW + i] *= ep;
     }
     __syncthreads();
-    g_nn<8>(aq, P0, LDN, T2, LDW, C, rb, cb);   // tril(dO U^T) Kb
-    g_tn<8>(aka, P0, LDN, T1, LDW, C, rb, cb);  // triu(U dO^T) Qh
-    g_nn<8>(aka, P1, LDN, T0, LDW, C, rb, cb);  // striu(U dY^T) Kh
-    g_tn<8>(akb, P1, LDN, T2, LDW, C, rb, cb);  // stril(dY U^T) Kb
+    mma16<8, AR, BK>(aq, P0, LDN, T2, LDW, C, r0, c128, lane);   // tril(dO U^T) Kb
+    mma16<8, AC, BK>(aka, P0, LDN, T1, LDW, C, r0, c128, lane);  // triu(U dO^T) Qh
+    mma16<8, AR, BK>(aka, P1, LDN, T0, LDW, C, r0, c128, lane);  // striu(U dY^T) Kh
+    mma16<8, AC, BK>(akb, P1, LDN, T2, LDW, C, r0, c128, lane);  // stril(dY U^T) Kb
     __syncthreads();  // T0 takes dg
 #pragma unroll
-    for (int y = 0; y < 4; ++y)
+    for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int r = 4 * rb + y, i = cb + 16 * x;
+        for (int e = 0; e < 4; ++e) {
+            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
             const float gx = T3[r * LDW + i] - T3[(C / 2 - 1) * LDW + i];
             const float eq = expf(gx), eb = expf(-gx);
-            const float dq = eq * aq[y][x], dka = eb * aka[y][x], dkb = eq * akb[y][x];
+            const float dq = eq * aq[j][e], dka = eb * aka[j][e], dkb = eq * akb[j][e];
             float dg = 0.f;
             if (r < p.L) {
                 const size_t o = (static_cast<size_t>(p.t0 + r) * H + h) * D + i;

@@ -231,9 +231,9 @@ def test_decode_multi_rejects_bad_arguments(lib, over, expect):
 
 def test_backward_workspace_bytes(lib):
     # schedule + chunk table, then the larger of the forward's operand images and the backward's
-    # per-chunk records (147,968 B per chunk-head), o scratch, snapshot entries, and two states
+    # per-chunk records (180,736 B per chunk-head), o scratch, snapshot entries, and two states
     # (the state and its adjoint) per chunk slot and head; chunk slots = ceil(T/64) + N
-    REC = 147968
+    REC = 180736
     for T, H, N in ((128, 2, 1), (1000, 32, 16)):
         slots = -(-T // 64) + N
         o = max(512 + slots * H * BLOB, 512 + slots * H * REC) if N == 1 else \
