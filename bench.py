@@ -42,11 +42,19 @@ STATE_BYTES = D * D * 4                                                 # 65,536
 # backward: reads q, k, v, grad_o (bf16), log_alpha, beta; writes fp32 grad_q, grad_k, grad_v,
 # grad_log_alpha and grad_beta
 BACKWARD_BYTES_PER_TOKEN_HEAD = 4 * D * 2 + D * 4 + 4 + 4 * D * 4 + 4   # 3,592
+# tensor-core work of the chunkwise backward per (chunk, head), multiply-adds: prep 3.67M (Grams,
+# Qh^T dO, Tb^T Kb, Mm^T dO, Tb^T MdO), adjoint scan 2.10M, value 5.24M, key 6.29M
+BACKWARD_MACS_PER_CHUNK_HEAD = (2 * 64 * 64 * 128 + 128 * 128 * 64 + 3 * 64 * 128 * 64
+                                + 2 * 64 * 128 * 128
+                                + 2 * 64 * 64 * 128 + 2 * 64 * 128 * 128 + 4 * 64 * 128 * 64
+                                + 2 * 64 * 64 * 128 + 3 * 64 * 128 * 128 + 4 * 64 * 128 * 64)
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rate
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + PREFILL_BYTES_PER_TOKEN_HEAD  # 132,612
 METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s & % HBM (H=32, d=128)"
 # sources whose ncu DRAM counters profiles/ncu_traffic.json records (null once they change)
 PREFILL_SOURCES = ["kda_api.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh"]
 DECODE_SOURCES = ["kda_decode.cu"]
+BACKWARD_SOURCES = ["kda_api.cu", "kda_backward.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh"]
 
 
 def dist_env():
@@ -545,6 +553,8 @@ def bench_backward(cx: Ctx, args):
     ms = cx.max_over_ranks(ms_local)
     bytes_per_call = T * H * BACKWARD_BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES  # + grad_S_final, grad_S0
     achieved = bytes_per_call / (ms_local * 1e-3) / 1e9
+    flops_per_call = 2 * BACKWARD_MACS_PER_CHUNK_HEAD * (-(-T // 64)) * H
+    achieved_tf = flops_per_call / (ms_local * 1e-3) / 1e12
     pk = cx.peaks
     del work, grads
     return {
@@ -553,10 +563,16 @@ def bench_backward(cx: Ctx, args):
         "value": round(T * cx.ws / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms_per_call": round(ms, 3),
         "calls": n,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm"], 4),
+                     "traffic": ncu_traffic("kda_prefill_backward", BACKWARD_SOURCES),
                      "kernel": "kda_prefill_backward call (chunkwise forward with per-chunk snapshots + "
                                "reverse walk)",
                      "peak_source": pk["src"] + " burst copy", "bytes_per_launch": bytes_per_call},
+        "tensor": {"achieved": round(achieved_tf, 2), "peak": round(pk["bf16"] * TF32_OVER_BF16, 1),
+                   "unit": "TFLOP/s", "frac": round(achieved_tf / (pk["bf16"] * TF32_OVER_BF16), 4),
+                   "flops_per_launch": flops_per_call, "dtype": "tf32 (fp32 operands rounded), fp32 accumulate",
+                   "peak_source": pk["src"] + " bf16 burst x nominal tf32/bf16 ratio 1.1/2.25"},
+        "gpu_launches_per_call": 10,
         "clocks": clk.summary(),
     }
 
