@@ -237,6 +237,50 @@ class Ctx:
         return E(enable_timing=True), E(enable_timing=True)
 
 
+class CopyOverlap:
+    """End-to-end steps with the host<->device copies overlapped across steps.  Every step copies
+    all of its inputs from pinned host memory to the device and reads its result back; step i+1's
+    inputs travel (own stream) while step i computes, and step i's result travels back (own stream)
+    while step i+1 computes.  Two device buffer sets, reused under events."""
+
+    def __init__(self, torch, compute_stream, host_in, dev_in_sets, host_out, dev_out_sets):
+        self.torch, self.cs = torch, compute_stream
+        self.h2d, self.d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        self.host_in, self.dev_in = host_in, dev_in_sets
+        self.host_out, self.dev_out = host_out, dev_out_sets
+        E = torch.cuda.Event
+        self.in_ready, self.in_free = [E(), E()], [E(), E()]
+        self.out_ready, self.out_free = [E(), E()], [E(), E()]
+        self.i = 0
+
+    def start(self):  # copies issued from now on begin after everything already on the compute stream
+        self.h2d.wait_stream(self.cs)
+        self.d2h.wait_stream(self.cs)
+
+    def step(self, compute):
+        t, b = self.torch, self.i & 1
+        self.h2d.wait_event(self.in_free[b])  # step i-2 no longer reads this input set
+        with t.cuda.stream(self.h2d):
+            for d, h in zip(self.dev_in[b], self.host_in):
+                d.copy_(h, non_blocking=True)
+        self.in_ready[b].record(self.h2d)
+        self.cs.wait_event(self.in_ready[b])
+        self.cs.wait_event(self.out_free[b])  # step i-2's result has been read back
+        compute(self.dev_in[b], self.dev_out[b])
+        self.in_free[b].record(self.cs)
+        self.out_ready[b].record(self.cs)
+        self.d2h.wait_event(self.out_ready[b])
+        with t.cuda.stream(self.d2h):
+            for h, d in zip(self.host_out, self.dev_out[b]):
+                h.copy_(d, non_blocking=True)
+        self.out_free[b].record(self.d2h)
+        self.i += 1
+
+    def finish(self):  # the compute stream waits for the last copies
+        self.cs.wait_stream(self.h2d)
+        self.cs.wait_stream(self.d2h)
+
+
 def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.25):
     """(pass-1 launches, scan launches) of the library's piecewise prefill schedule for one sequence
     of seq_chunks chunks: scan pieces of max(min_piece, ceil(n / max_pieces)) chunks, pass 1 a lead
@@ -294,32 +338,36 @@ def bench_prefill(cx: Ctx, args):
     achieved_gbs = bytes_per_launch / (ms_local * 1e-3) / 1e9
     achieved_tf = flops_per_launch / (ms_local * 1e-3) / 1e12
 
-    # end to end through the same C-ABI call: pinned host inputs in, o and S_final out, every step
+    # end to end through the same C-ABI call: pinned host inputs in, o and S_final out, every step;
+    # the copies of neighbouring steps overlap this step's compute (CopyOverlap)
     names = ("q", "k", "v", "log_alpha", "beta", "cu_seqlens")
-    host = {n: getattr(p, n).cpu().pin_memory() for n in names}
-    dev_in = {n: torch.empty_like(getattr(p, n)) for n in names}
+    host_in = [getattr(p, n).cpu().pin_memory() for n in names]
+    dev_in = [[torch.empty_like(getattr(p, n)) for n in names] for _ in range(2)]
     o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     sf_host = torch.empty(sf.shape, dtype=sf.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    dev_out = [[torch.empty_like(o), torch.empty_like(sf)] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = o_host.numel() * o_host.element_size() + sf_host.numel() * sf_host.element_size()
+    pipe = CopyOverlap(torch, cx.stream, host_in, dev_in, [o_host, sf_host], dev_out)
 
-    def e2e_step():
-        for n, t in host.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        kda.kda_prefill(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["log_alpha"], dev_in["beta"],
-                        dev_in["cu_seqlens"], None, o=o, S_final=sf, workspace=work, stream=cx.stream)
-        o_host.copy_(o, non_blocking=True)
-        sf_host.copy_(sf, non_blocking=True)
+    def e2e_compute(x, y):
+        kda.kda_prefill(x[0], x[1], x[2], x[3], x[4], x[5], None, o=y[0], S_final=y[1], workspace=work,
+                        stream=cx.stream)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    pipe.start()
+    for _ in range(max(3, args.warmup)):
+        pipe.step(e2e_compute)
+    pipe.finish()
     cx.barrier()
     ev0.record(cx.stream)
+    pipe.start()
     for _ in range(args.steps):
-        e2e_step()
+        pipe.step(e2e_compute)
+    pipe.finish()
     ev1.record(cx.stream)
     cx.barrier()
     e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    del dev_in, dev_out
 
     # the same call with the fused prologue / epilogue, and with a state snapshot every 1024 tokens
     g = torch.Generator(device=cx.dev).manual_seed(7 + cx.rank)
@@ -378,7 +426,9 @@ def bench_prefill(cx: Ctx, args):
                    "frac": round(achieved_tf / pk["bf16"], 4), "flops_per_launch": flops_per_launch,
                    "peak_source": pk["src"] + " bf16 burst"},
         "e2e": {"value": round(tokens_per_step / (e2e_ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "overlap": "H2D of step i+1 and D2H of step i-1 run beside step i (two buffer sets, "
+                           "copy streams ordered by events)"},
         "clocks": clk.summary(),
     }
 
@@ -470,27 +520,31 @@ def bench_decode(cx: Ctx, args):
              "state_gbs": round(cx.ws * n_units * 2 * STATE_BYTES / (f_ms * 1e-3) / 1e9, 1)}
     del gate
 
-    # end to end: each step's inputs H2D from pinned memory and its o D2H; the states stay in HBM
+    # end to end: each step's inputs H2D from pinned memory and its o D2H; the states stay in HBM;
+    # the copies of neighbouring steps overlap this step's compute (CopyOverlap)
     names = ("q", "k", "v", "log_alpha", "beta")
     hq = [getattr(d, n)[0].cpu().pin_memory() for n in names]
-    dq = [getattr(d, n)[0].clone() for n in names]
+    dq = [[getattr(d, n)[0].clone() for n in names] for _ in range(2)]
     oh = torch.empty(od[0].shape, dtype=od.dtype).pin_memory()
+    dout = [[torch.empty_like(od[0])] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in hq)
     d2h = oh.numel() * oh.element_size()
+    pipe = CopyOverlap(torch, cx.stream, hq, dq, [oh], dout)
 
-    def e2e_step():
-        for a_, b_ in zip(dq, hq):
-            a_.copy_(b_, non_blocking=True)
-        kda.kda_decode_step(dq[0], dq[1], dq[2], dq[3], dq[4], d.S, None, o=od[0], stream=cx.stream)
-        oh.copy_(od[0], non_blocking=True)
+    def e2e_compute(x, y):
+        kda.kda_decode_step(x[0], x[1], x[2], x[3], x[4], d.S, None, o=y[0], stream=cx.stream)
 
+    pipe.start()
     for _ in range(3):
-        e2e_step()
+        pipe.step(e2e_compute)
+    pipe.finish()
     cx.barrier()
     n_e2e = 100
     ev0.record(cx.stream)
+    pipe.start()
     for _ in range(n_e2e):
-        e2e_step()
+        pipe.step(e2e_compute)
+    pipe.finish()
     ev1.record(cx.stream)
     cx.barrier()
     e2e_ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / n_e2e)
@@ -507,7 +561,9 @@ def bench_decode(cx: Ctx, args):
                      "bytes_per_launch": n_units * DECODE_BYTES_PER_UNIT},
         "e2e": {"value": round(cx.ws * n_units * 2 * STATE_BYTES / (e2e_ms * 1e-3) / 1e9, 1),
                 "unit": "state GB/s", "us_per_step": round(e2e_ms * 1e3, 2),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "H2D of step i+1 and D2H of step i-1 run beside step i (two buffer sets, "
+                           "copy streams ordered by events); the state updates stay in order"},
         "clocks": clk.summary(),
         "multi_token": multi,
         "fused_prologue_epilogue": fused,
