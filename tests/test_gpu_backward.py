@@ -116,3 +116,19 @@ def test_backward_8k_sampled_heads():
     got = _gpu(p, dO, dSf)
     heads = [0, 31]
     _compare(got, _oracle(p, dO, dSf, heads), heads)
+
+
+def test_backward_degenerate_gates():
+    """Tokens with beta = 0 (no write: du still drives dbeta) and log_alpha = 0 (no decay)."""
+    p = synth.prefill_inputs([200, 90], H=2, s0_std=0.02, seed=51)
+    p.beta[::7] = 0.0
+    p.log_alpha[::5] = 0.0
+    dO, dSf = _cotangents(p, 52)
+    _compare(_gpu(p, dO, dSf), _oracle(p, dO, dSf))
+
+
+def test_backward_strong_decay():
+    """log_alpha ~ U[-1, 0]: per-chunk gate spans up to e^{32} around the reference row."""
+    p = synth.prefill_inputs([256, 77], H=2, lo=-1.0, s0_std=0.02, seed=53)
+    dO, dSf = _cotangents(p, 54)
+    _compare(_gpu(p, dO, dSf), _oracle(p, dO, dSf))

@@ -114,6 +114,36 @@ def test_decode_multi_equals_single_steps(dtype):
         assert torch.equal(steps[:, t], S_ref[idx])
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_multi_many_units_equals_single_steps(dtype):
+    """More (sequence, head) units than two per SM: each CTA walks several units with the next one's
+    state and inputs prefetched; results stay bitwise equal to single steps, including a bad slot
+    (flagged and skipped by both paths) and the per-token state output."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, T = 4, 4
+    N = (2 * sms) // H + 37  # > 2 * SM count units, not a multiple of the grid
+    d = synth.decode_inputs(N, H, T, dtype=dtype, seed=73, device="cuda", num_slots=N + 5, permute_slots=True)
+    idx = d.state_indices.clone()
+    idx[N // 3] = N + 5  # out of range
+    st_s = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S_single = d.S.clone()
+    o_single = torch.stack([kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], S_single, idx,
+                                                device_status=st_s) for t in range(T)], dim=1)
+    tm = lambda x: x.transpose(0, 1).contiguous()
+    st_m = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S_multi = d.S.clone()
+    o_multi, steps = kda.kda_decode_multi(tm(d.q), tm(d.k), tm(d.v), tm(d.log_alpha), tm(d.beta), S_multi, idx,
+                                          device_status=st_m, return_steps=True)
+    torch.cuda.synchronize()
+    assert int(st_m.item()) == kda.KDA_DEV_BAD_SLOT and int(st_s.item()) == kda.KDA_DEV_BAD_SLOT
+    ok = torch.ones(N, dtype=torch.bool, device="cuda")
+    ok[N // 3] = False
+    assert torch.equal(o_multi[ok], o_single[ok])
+    assert torch.equal(S_multi, S_single)
+    good = idx[ok].long()
+    assert torch.equal(steps[ok][:, -1], S_multi[good])
+
+
 def test_decode_multi_oracle_and_slots():
     N, H, T = 6, 4, 4
     d = synth.decode_inputs(N, H, T, seed=72, device="cuda", num_slots=10, permute_slots=True)

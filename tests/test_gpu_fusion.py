@@ -170,6 +170,38 @@ def test_decode_fused_steps(dtype, flags):
     assert int(status.item()) == 0
 
 
+def test_decode_multi_fused_many_units():
+    """The fused multi-token path with more units than two per SM (prefetched units, T = 3)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, T = 2, 3
+    N = sms + 17
+    d = synth.decode_inputs(N, H, T, seed=631, device="cuda", num_slots=N + 2, permute_slots=True)
+    g = torch.Generator(device="cuda").manual_seed(632)
+    scale = lambda x: (x.float() * (0.3 + 2.7 * torch.rand(x.shape[:-1] + (1,), generator=g, device="cuda"))).to(
+        torch.bfloat16)
+    q, k = scale(d.q), scale(d.k)
+    beta = torch.randn(d.beta.shape, generator=g, device="cuda")
+    gate = torch.randn(d.q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    tm = lambda x: x.transpose(0, 1).contiguous()
+    S_ref = host(d.S).astype(np.float64)
+    idx = d.state_indices.cpu().numpy()
+    o_ref = []
+    for t in range(T):
+        qq, kk = oracle.l2_normalize(host(q[t]), L2_EPS), oracle.l2_normalize(host(k[t]), L2_EPS)
+        ot = oracle.kda_decode_step(qq, kk, host(d.v[t]), host(d.log_alpha[t]), oracle.sigmoid(host(beta[t])), S_ref,
+                                    idx)
+        o_ref.append(oracle.rmsnorm_gate(ot, host(gate[t]), np.ones(128), RMS_EPS))
+    o_ref = np.stack(o_ref, axis=1)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS, out_gate=tm(gate), rms_eps=RMS_EPS)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = kda.kda_decode_multi_ex(tm(q), tm(k), tm(d.v), tm(d.log_alpha), tm(beta), d.S, d.state_indices, fusion=fz,
+                                device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert rell2(host(o), o_ref) < TOL
+    assert rell2(host(d.S), S_ref) < 1e-4
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_decode_multi_fused(dtype):
     N, H, T = 5, 3, 11  # two token batches in the kernel (8 + 3)
