@@ -634,7 +634,6 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
     a.rec = reinterpret_cast<float*>(ws + fwd.copies);  // the forward's copies and images are dead now
     a.xbuf = reinterpret_cast<float*>(ws + lay.xbuf);
     a.u_scratch = grad_q;
-    a.device_status = device_status;
     a.num_seqs = num_seqs;
     a.H = H;
     return kda::launch_backward(a, qkv_dtype == KDA_DTYPE_F32, lay.entries, stream) == cudaSuccess ? KDA_OK

@@ -747,287 +747,6 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
     }
 }
 
-// ================================================================ key (tcgen05) ==
-// The key kernel on the 5th-generation tensor cores: tf32 operands (fp32 data, the MMA reads
-// its tf32 part) in 128-byte-swizzled K-major shared tiles, fp32 accumulators in TMEM.  Every
-// product is taken with the 128 key channels i as the M dimension (the transposed form of
-// dq, dk), so each is one M = 128 tcgen05.mma chain and the epilogue reads one key channel per
-// TMEM lane: for a token t the 32 lanes of a warp hold 32 consecutive channels, so the stores
-// of dq, dk and dlog_alpha are coalesced and the reverse cumulative sum runs down a thread.
-//   batch 1:  D_P = [dO; U] [U; dv]^T                (dO U^T and U dv^T, 128 x 128)
-//             aq_s = S dO^T, akb_s = S dv^T, aka_s = X U^T      (128 x 64 each)
-//   batch 2:  aq_i = Kb^T P0^T, aka_i = Qh^T P0 + Kh^T P1, akb_i = Kb^T P1^T
-// with P0 = lower (dO U^T), P1 = strict upper (U dY^T), dY = -dv, and the row scalings
-// e^{gm} (S) and e^{gC - gm} (X) applied in the epilogue.
-__device__ __forceinline__ float rnd(float x) { return __uint_as_float(to_tf32(x)); }
-// 16-byte cp.async to any shared address; valid = false zero-fills the destination
-__device__ __forceinline__ void cp16z(void* dst, const float* src, bool valid) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-__device__ __forceinline__ void tc_mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// byte offset of fp32 element (row, k) in a K-major 128B-swizzled tile of `rows` rows
-// (32-element K blocks, `rows` x 128 bytes each)
-__device__ __forceinline__ uint32_t sw32(int row, int k, int rows) {
-    return static_cast<uint32_t>((k >> 5) * rows * 128 + row * 128 + (((((k & 31) >> 2) ^ row) & 7) << 4) +
-                                 ((k & 3) << 2));
-}
-// D (+)= A B^T over K (multiple of 8): A = rows a_row0 .. of a tile of a_rows rows, B likewise
-__device__ __forceinline__ void tc_gemm(uint32_t d, uint32_t a, int a_rows, int a_row0, uint32_t b, int b_rows,
-                                        int b_row0, int K, uint32_t idesc, bool acc) {
-    for (int ks = 0; ks < K / 8; ++ks) {
-        const int blk = ks >> 2, w = ks & 3;
-        const uint64_t ad = sdesc_sw128(a + blk * a_rows * 128 + a_row0 * 128 + w * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(b + blk * b_rows * 128 + b_row0 * 128 + w * 32, 16, 1024);
-        tc_mma_tf32(d, ad, bd, idesc, (acc || ks > 0) ? 1u : 0u);
-    }
-}
-
-struct KeyTcL {
-    static constexpr uint32_t TA = 0;                  // [dO; U; dv]: 192 rows, K = 128  (96 KB)
-    static constexpr uint32_t TS0 = 192 * 512;         // start state, 128 rows, K = 128 (64 KB)
-    static constexpr uint32_t TS1 = TS0 + 65536;       // adjoint after the chunk        (64 KB)
-    static constexpr uint32_t END = TS1 + 65536;
-    // after batch 1
-    static constexpr uint32_t KBT = 0, QHT = 32768, KHT = 65536;  // [128 rows i][K = 64 tokens] each
-    static constexpr uint32_t P0 = TS0, P0T = TS0 + 16384, P1 = TS0 + 32768, P1T = TS0 + 49152;  // [64][K = 64]
-    static constexpr uint32_t CARRY = TS0;             // after batch 2: [128] fp32
-    static constexpr uint32_t ALLOC = END + 1024;
-};
-static_assert(KeyTcL::ALLOC + 1600 <= 232448, "key kernel shared memory");
-
-template <typename IoT>
-__global__ void __launch_bounds__(BT, 1) kda_bwd_key_tc_kernel(const BackwardArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using L = KeyTcL;
-    __shared__ float bnd[D], gmid[D], gtot[D];  // boundary term; g at rows 31 and 63
-    __shared__ uint64_t bar[2];
-    __shared__ uint32_t tslot;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
-    ChunkPos p;
-    if (!chunk_pos(a, gc, p)) return;
-    const IoT* q = static_cast<const IoT*>(a.q);
-    const IoT* k = static_cast<const IoT*>(a.k);
-    const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
-    const float* S = chunk_start_state(a, p, gc, h);
-    const uint32_t base = smem_u32(sm);
-
-    if (warp == 0) tmem_alloc(&tslot, 512);
-    if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        fence_mbar_init();
-    }
-    // batch-1 operands: U, dv, S, X by cp.async into the swizzled tiles (rows >= L zero), dO converted
-#pragma unroll 4
-    for (int it = 0; it < C * 32 / BT; ++it) {  // 64 rows x 32 chunks of 16 bytes
-        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
-        const int rr = r < p.L ? r : p.L - 1;
-        const size_t g = (static_cast<size_t>(p.t0 + rr) * H + h) * D + c4;
-        cp16z(sm + L::TA + sw32(64 + r, c4, 192), a.u_scratch + g, r < p.L);
-        cp16z(sm + L::TA + sw32(128 + r, c4, 192), a.dv + g, r < p.L);
-    }
-#pragma unroll 4
-    for (int it = 0; it < D * 32 / BT; ++it) {  // 128 rows x 32 chunks
-        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
-        if (S) cp16z(sm + L::TS0 + sw32(r, c4, 128), S + r * D + c4, true);
-        cp16z(sm + L::TS1 + sw32(r, c4, 128), X + r * D + c4, true);
-    }
-    cp_commit();
-    {
-        const IoT* dO = static_cast<const IoT*>(a.dO);
-#pragma unroll
-        for (int it = 0; it < C * 32 / BT; ++it) {
-            const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < p.L) v = ld4(dO + (static_cast<size_t>(p.t0 + r) * H + h) * D + c4);
-            *reinterpret_cast<float4*>(sm + L::TA + sw32(r, c4, 192)) = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
-        }
-    }
-    // cumulative log-decay in registers: thread (i = tid & 127, half = tid >> 7) owns tokens
-    // 32 half .. 32 half + 31 of channel i (the epilogue's mapping); the first half's total and
-    // g at row 31 go through shared memory
-    const int gi = tid & 127, ghalf = tid >> 7;
-    float gv[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int t = 32 * ghalf + j;
-        gv[j] = t < p.L ? a.log_alpha[(static_cast<size_t>(p.t0 + t) * H + h) * D + gi] : 0.f;
-    }
-#pragma unroll
-    for (int j = 1; j < 32; ++j) gv[j] += gv[j - 1];
-    if (ghalf == 0) gmid[gi] = gv[31];
-    {   // boundary term of the last row: rowsum(S_next * X), S_next = the snapshot after this chunk
-        const float* Sn = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D;
-        const int i = tid >> 1, j0 = (tid & 1) * 64;
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 sv = *reinterpret_cast<const float4*>(Sn + i * D + j0 + j);
-            const float4 xv = *reinterpret_cast<const float4*>(X + i * D + j0 + j);
-            s = fmaf(sv.x, xv.x, fmaf(sv.y, xv.y, fmaf(sv.z, xv.z, fmaf(sv.w, xv.w, s))));
-        }
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        if ((tid & 1) == 0) bnd[i] = s;
-    }
-    cp_wait<0>();
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tslot;
-    if (tid == 0) {
-        tc_gemm(tmem, base + L::TA, 192, 0, base + L::TA, 192, 64, D, idesc_tf32(128, 128), false);
-        if (S) {
-            tc_gemm(tmem + 128, base + L::TS0, 128, 0, base + L::TA, 192, 0, D, idesc_tf32(128, 64), false);
-            tc_gemm(tmem + 192, base + L::TS0, 128, 0, base + L::TA, 192, 128, D, idesc_tf32(128, 64), false);
-        }
-        tc_gemm(tmem + 256, base + L::TS1, 128, 0, base + L::TA, 192, 64, D, idesc_tf32(128, 64), false);
-        mma_commit(&bar[0]);
-    }
-    bool ok = mbar_wait(&bar[0], 0, pf::kWaitLimit);
-    tc_fence_after();
-    if (ok) {  // P0 = lower (dO U^T), P1 = strict upper (U dY^T) = -(U dv^T); each also stored transposed
-        const int q4 = warp & 3, half = warp >> 2, row = 32 * q4 + lane;
-        float v[32];
-        if (q4 < 2) {
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * half, v);
-            tmem_ld_wait();
-            const int t = row;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int s = 32 * half + j;
-                const float x = s <= t ? rnd(v[j]) : 0.f;
-                *reinterpret_cast<float*>(sm + L::P0 + sw32(t, s, 64)) = x;
-                *reinterpret_cast<float*>(sm + L::P0T + sw32(s, t, 64)) = x;
-            }
-        } else {
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + 32 * half, v);
-            tmem_ld_wait();
-            const int s = row - 64;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = 32 * half + j;
-                const float x = r > s ? rnd(-v[j]) : 0.f;
-                *reinterpret_cast<float*>(sm + L::P1 + sw32(s, r, 64)) = x;
-                *reinterpret_cast<float*>(sm + L::P1T + sw32(r, s, 64)) = x;
-            }
-        }
-    }
-    __syncthreads();  // batch-1 operand tiles are read no more; gmid is written
-    if (ghalf == 1) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) gv[j] += gmid[gi];
-        gtot[gi] = gv[31];
-    }
-    {   // transposed gated operands: rows i, K = tokens (all of the thread's q, k loads in flight together)
-        const int i = gi, t0 = 32 * ghalf;
-        const float gmi = gmid[i];
-        float kv[32], qv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int t = t0 + j;
-            const size_t o = (static_cast<size_t>(p.t0 + (t < p.L ? t : 0)) * H + h) * D + i;
-            kv[j] = t < p.L ? ld1(k + o) : 0.f;
-            qv[j] = t < p.L ? ld1(q + o) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int t = t0 + j;
-            const float x = gv[j] - gmi;
-            const float ep = expf(x), en = expf(-x);
-            *reinterpret_cast<float*>(sm + L::KBT + sw32(i, t, 128)) = rnd(kv[j] * en);
-            *reinterpret_cast<float*>(sm + L::QHT + sw32(i, t, 128)) = rnd(qv[j] * ep);
-            *reinterpret_cast<float*>(sm + L::KHT + sw32(i, t, 128)) = rnd(kv[j] * ep);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0 && ok) {
-        tc_gemm(tmem + 320, base + L::KBT, 128, 0, base + L::P0, 64, 0, C, idesc_tf32(128, 64), false);
-        tc_gemm(tmem + 384, base + L::QHT, 128, 0, base + L::P0T, 64, 0, C, idesc_tf32(128, 64), false);
-        tc_gemm(tmem + 384, base + L::KHT, 128, 0, base + L::P1, 64, 0, C, idesc_tf32(128, 64), true);
-        tc_gemm(tmem + 448, base + L::KBT, 128, 0, base + L::P1T, 64, 0, C, idesc_tf32(128, 64), false);
-        mma_commit(&bar[1]);
-    }
-    if (ok) ok = mbar_wait(&bar[1], 0, pf::kWaitLimit);
-    tc_fence_after();
-    if (!ok && tid == 0 && a.device_status) atomicOr(a.device_status, KDA_DEV_TIMEOUT);
-    float* carry = reinterpret_cast<float*>(sm + L::CARRY);
-    const int q4 = warp & 3, half = warp >> 2, i = 32 * q4 + lane;
-    float dgv[32];
-    if (ok) {
-        const float gmi = gmid[i], em = expf(gmi), ec = expf(gtot[i] - gmi), bi = bnd[i];
-        const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-#pragma unroll
-        for (int c16 = 0; c16 < 2; ++c16) {
-            const uint32_t col = 32 * half + 16 * c16;
-            float qs[16], qi[16], bs[16], bi2[16], as[16], ai[16];
-            if (S) {
-                tmem_ld16(lb + 128 + col, qs);
-                tmem_ld16(lb + 192 + col, bs);
-            }
-            tmem_ld16(lb + 256 + col, as);
-            tmem_ld16(lb + 320 + col, qi);
-            tmem_ld16(lb + 384 + col, ai);
-            tmem_ld16(lb + 448 + col, bi2);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int t = col + j;
-                const float x = gv[16 * c16 + j] - gmi;
-                const float eq = expf(x), eb = expf(-x);
-                const float aq = S ? fmaf(em, qs[j], qi[j]) : qi[j];
-                const float akb = S ? fmaf(-em, bs[j], bi2[j]) : bi2[j];
-                const float aka = fmaf(ec, as[j], ai[j]);
-                const float dq = eq * aq, dka = eb * aka, dkb = eq * akb;
-                float dg = 0.f;
-                if (t < p.L) {
-                    const size_t o = (static_cast<size_t>(p.t0 + t) * H + h) * D + i;
-                    dg = ld1(q + o) * dq + ld1(k + o) * (dkb - dka);
-                    if (t == p.L - 1) dg += bi;
-                    a.dq[o] = dq;
-                    a.dk[o] = dka + dkb;
-                }
-                dgv[16 * c16 + j] = dg;
-            }
-        }
-        if (half == 1) {
-            float tot = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) tot += dgv[j];
-            carry[i] = tot;
-        }
-    }
-    __syncthreads();
-    if (ok) {  // dlog_alpha = reverse cumulative sum of dg down the thread's 32 tokens (+ the later half)
-        float s = half == 0 ? carry[i] : 0.f;
-#pragma unroll
-        for (int j = 31; j >= 0; --j) {
-            const int t = 32 * half + j;
-            s += dgv[j];
-            if (t < p.L) a.dla[(static_cast<size_t>(p.t0 + t) * H + h) * D + i] = s;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
-}
-
 // Snapshot entries for every chunk end of every sequence: entry chunk_off[n] + c - 1 is the state
 // after chunk c - 1 of sequence n (c = 1 .. nch_n; the last is the final state).  Entries past the
 // batch's chunk count are sentinels (sequence N) that no scan CTA takes.
@@ -1073,7 +792,7 @@ cudaError_t launch_all(const BackwardArgs& a, int64_t chunk_slots, cudaStream_t 
         return err;
     if ((err = launch_smem(kda_bwd_value_kernel<IoT>, per_chunk, ValueL::FLOATS * 4, a, stream)) != cudaSuccess)
         return err;
-    return launch_smem(kda_bwd_key_tc_kernel<IoT>, per_chunk, KeyTcL::ALLOC, a, stream);
+    return launch_smem(kda_bwd_key_kernel<IoT>, per_chunk, KeyL::FLOATS * 4, a, stream);
 }
 
 }  // namespace

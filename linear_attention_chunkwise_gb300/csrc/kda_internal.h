@@ -121,7 +121,6 @@ struct BackwardArgs {
     float* rec = nullptr;        // per-(chunk, head) records of the prep kernel (backward_record_bytes each)
     float* xbuf = nullptr;       // adjoint of the state after every chunk, indexed like ckpt
     float* u_scratch = nullptr;  // [T, H, 128] rows u_t between the value and key kernels (may be dq)
-    int32_t* device_status = nullptr;
     int32_t num_seqs = 0;
     int32_t H = 0;
 };
