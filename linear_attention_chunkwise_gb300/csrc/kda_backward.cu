@@ -77,8 +77,6 @@ __device__ __forceinline__ float ld1<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-__device__ __forceinline__ float comp(const float4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
-
 // ---- products on shared tiles ---------------------------------------------------------------
 // Tensor-core products of fp32 shared tiles: operands rounded to tf32 (cvt.rna), fp32 accumulate,
 // mma.sync m16n8k8.  One warp owns 16 output rows from r0 and NT 8-column tiles from c0; its
