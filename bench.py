@@ -570,6 +570,44 @@ def bench_decode(cx: Ctx, args):
     }
 
 
+def bench_prefill_fused(cx: Ctx, args):
+    """The 8k prefill through kda_prefill_ex with every fusion: q/k L2 norm, sigmoid beta and the
+    output RMSNorm x gate (2-CTA cluster scan).  Device-resident inputs, CUDA events."""
+    torch = cx.torch
+    import linear_attention_chunkwise_gb300 as kda
+    from linear_attention_chunkwise_gb300 import synth
+
+    c = synth.CONFIGS[PREFILL_CFG]
+    p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
+                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+    T = p.total_tokens
+    g = torch.Generator(device=cx.dev).manual_seed(7 + cx.rank)
+    gate = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, out_gate=gate,
+                    rms_weight=torch.ones(D, dtype=torch.float32, device=cx.dev))
+    o = torch.empty_like(p.q)
+    sf = torch.empty((1, H, D, D), dtype=torch.float32, device=cx.dev)
+    work = torch.empty(kda.kda_prefill_workspace_bytes(torch.bfloat16, 1, T, H), dtype=torch.uint8, device=cx.dev)
+
+    def call():
+        kda.kda_prefill_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, None, fusion=fz, o=o, S_final=sf,
+                           workspace=work, stream=cx.stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    cx.barrier()
+    ev0, ev1 = cx.events()
+    ev0.record(cx.stream)
+    for _ in range(args.steps):
+        call()
+    ev1.record(cx.stream)
+    cx.barrier()
+    ms = cx.max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    return {"workload": "KDA chunkwise prefill B=1 H=32 T=8192 through kda_prefill_ex with L2-normalised q/k, "
+                        "sigmoid beta and RMSNorm x output gate fused",
+            "value": round(T * cx.ws / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "us_per_call": round(ms * 1e3, 1)}
+
+
 def bench_backward(cx: Ctx, args):
     """Prefill backward on the 8k workload (grad_o ~ N(0,1) bf16, grad_S_final ~ N(0, 0.01)): one call
     reruns the chunkwise forward with a snapshot per chunk and walks every head back."""
@@ -640,6 +678,7 @@ def run_ours(args):
     pf = bench_prefill(cx, args) if args.only in ("all", "prefill") else None
     dc = bench_decode(cx, args) if args.only in ("all", "decode") else None
     bw = bench_backward(cx, args) if args.only in ("all", "backward") else None
+    pfz = bench_prefill_fused(cx, args) if args.only == "prefill_fused" else None
     out = {"metric": METRIC}
     if pf is not None:
         out.update({
@@ -660,6 +699,8 @@ def run_ours(args):
         out["decode"] = dc
     if bw is not None:
         out["backward"] = bw
+    if pfz is not None:
+        out["prefill_fused"] = pfz
     if cx.rank == 0 and not args.no_cpu_baseline and pf is not None:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if cx.rank == 0:
@@ -758,7 +799,7 @@ def main(argv=None):
     ap.add_argument("--decode-reps", type=int, default=5, help="replays of the 100-step decode graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "prefill_fused"], default="all",
                     help="profiling aid: run only one workload (the JSON line then lacks the other)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
