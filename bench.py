@@ -32,8 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-PREFILL_CFG = 1
-DECODE_CFG = 3
+PREFILL_WORKLOAD = "prefill_8k"
+DECODE_WORKLOAD = "decode_256x32"
 H, D = 32, 128
 # algorithmic bytes / flops per token-head (q, k, v bf16 + log_alpha fp32 + beta fp32 + o bf16)
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2          # 1540
@@ -307,9 +307,9 @@ def bench_prefill(cx: Ctx, args):
     import linear_attention_chunkwise_gb300 as kda
     from linear_attention_chunkwise_gb300 import synth
 
-    c = synth.CONFIGS[PREFILL_CFG]
+    c = synth.WORKLOADS[PREFILL_WORKLOAD]
     p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
-                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+                             synth.workload_seed(PREFILL_WORKLOAD) + 1000 * cx.rank, cx.dev)
     T = p.total_tokens
     o = torch.empty_like(p.q)
     sf = torch.empty((1, H, D, D), dtype=torch.float32, device=cx.dev)
@@ -439,9 +439,9 @@ def bench_decode(cx: Ctx, args):
     import linear_attention_chunkwise_gb300 as kda
     from linear_attention_chunkwise_gb300 import synth
 
-    dc = synth.CONFIGS[DECODE_CFG]
+    dc = synth.WORKLOADS[DECODE_WORKLOAD]
     d = synth.decode_inputs(dc["N"], dc["H"], dc["steps"], D, dc["dtype"], dc["lo"], dc["s_std"],
-                            synth.config_seed(DECODE_CFG) + 1000 * cx.rank, cx.dev)
+                            synth.workload_seed(DECODE_WORKLOAD) + 1000 * cx.rank, cx.dev)
     n_units = dc["N"] * dc["H"]
     steps = dc["steps"]
     od = torch.empty((steps, dc["N"], dc["H"], D), dtype=torch.bfloat16, device=cx.dev)
@@ -472,7 +472,7 @@ def bench_decode(cx: Ctx, args):
     # multi-token step (speculative verify): T_MULTI tokens per sequence in one launch
     T_MULTI = 4
     dm = synth.decode_inputs(dc["N"], dc["H"], T_MULTI, D, dc["dtype"], dc["lo"], dc["s_std"],
-                             synth.config_seed(DECODE_CFG) + 5000 + 1000 * cx.rank, cx.dev)
+                             synth.workload_seed(DECODE_WORKLOAD) + 5000 + 1000 * cx.rank, cx.dev)
     tm = lambda x: x.transpose(0, 1).contiguous()
     mq, mk, mv, mla, mb = tm(dm.q), tm(dm.k), tm(dm.v), tm(dm.log_alpha), tm(dm.beta)
     mo = torch.empty_like(mq)
@@ -577,9 +577,9 @@ def bench_prefill_fused(cx: Ctx, args):
     import linear_attention_chunkwise_gb300 as kda
     from linear_attention_chunkwise_gb300 import synth
 
-    c = synth.CONFIGS[PREFILL_CFG]
+    c = synth.WORKLOADS[PREFILL_WORKLOAD]
     p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
-                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+                             synth.workload_seed(PREFILL_WORKLOAD) + 1000 * cx.rank, cx.dev)
     T = p.total_tokens
     g = torch.Generator(device=cx.dev).manual_seed(7 + cx.rank)
     gate = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
@@ -615,9 +615,9 @@ def bench_backward(cx: Ctx, args):
     import linear_attention_chunkwise_gb300 as kda
     from linear_attention_chunkwise_gb300 import synth
 
-    c = synth.CONFIGS[PREFILL_CFG]
+    c = synth.WORKLOADS[PREFILL_WORKLOAD]
     p = synth.prefill_inputs(c["lengths"], c["H"], D, c["dtype"], c["lo"], c["s0_std"],
-                             synth.config_seed(PREFILL_CFG) + 1000 * cx.rank, cx.dev)
+                             synth.workload_seed(PREFILL_WORKLOAD) + 1000 * cx.rank, cx.dev)
     T = p.total_tokens
     g = torch.Generator(device=cx.dev).manual_seed(11 + cx.rank)
     dO = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
@@ -715,7 +715,7 @@ def run_ours(args):
 def _oracle_inputs(tokens: int, seed: int):
     """The 8k prefill workload's inputs (or its first `tokens` tokens), generated on the CPU."""
     from linear_attention_chunkwise_gb300 import synth
-    c = synth.CONFIGS[PREFILL_CFG]
+    c = synth.WORKLOADS[PREFILL_WORKLOAD]
     pi = synth.prefill_inputs([tokens], c["H"], D, c["dtype"], c["lo"], None, seed, "cpu")
     f = lambda t: t.float().numpy()
     return f(pi.q), f(pi.k), f(pi.v), f(pi.log_alpha), f(pi.beta), [0, tokens]
@@ -746,7 +746,7 @@ def _time_oracle_runs(target_seconds: float, max_steps: int | None = None):
 
 def synth_tokens() -> int:
     from linear_attention_chunkwise_gb300 import synth
-    return int(synth.CONFIGS[PREFILL_CFG]["lengths"][0])
+    return int(synth.WORKLOADS[PREFILL_WORKLOAD]["lengths"][0])
 
 
 def cpu_baseline(target_seconds: float):

@@ -32,16 +32,16 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.l
 
 // Device must be sm_103 (the kernels are built for sm_103a only).
 kda_status check_device() {
-    static int verdict[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+    static int support[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev >= 0 && dev < kMaxDevices && verdict[dev] != 0) return verdict[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED;
+    if (dev >= 0 && dev < kMaxDevices && support[dev] != 0) return support[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return KDA_ERR_CUDA;
     const bool ok = (major == 10 && minor == 3);
-    if (dev >= 0 && dev < kMaxDevices) verdict[dev] = ok ? 1 : 2;
+    if (dev >= 0 && dev < kMaxDevices) support[dev] = ok ? 1 : 2;
     return ok ? KDA_OK : KDA_ERR_UNSUPPORTED;
 }
 

@@ -24,25 +24,25 @@ import torch
 
 SLAB_TOKENS = 65536
 
-# The five workloads: tiny fp32 prefill, 8k prefill, packed varlen prefill with
-# start states, 256 x 32-head decode, and the 1M-token prefill.
-CONFIGS = {
-    0: dict(kind="prefill", name="tiny prefill B=1 H=2 T=256 d=128 fp32", lengths=[256], H=2,
-            dtype=torch.float32, lo=-0.2, s0_std=None),
-    1: dict(kind="prefill", name="prefill B=1 H=32 T=8192 d=128 bf16", lengths=[8192], H=32,
-            dtype=torch.bfloat16, lo=-0.2, s0_std=None),
-    2: dict(kind="prefill", name="varlen prefill N=16 len~U[1024,65536] H=32 d=128 bf16, S0~N(0,0.02)",
-            lengths=None, num_seqs=16, len_lo=1024, len_hi=65536, H=32, dtype=torch.bfloat16,
-            lo=-0.2, s0_std=0.02),
-    3: dict(kind="decode", name="decode N=256 H=32 d=128 bf16, 100 steps, S~N(0,0.02)", N=256, H=32,
-            steps=100, dtype=torch.bfloat16, lo=-0.2, s_std=0.02),
-    4: dict(kind="prefill", name="long prefill B=1 H=32 T=1048576 d=128 bf16", lengths=[1048576], H=32,
-            dtype=torch.bfloat16, lo=-0.05, s0_std=None),
+# The five workloads, by name: tiny fp32 prefill, 8k prefill, packed varlen
+# prefill with start states, 256 x 32-head decode, and the 1M-token prefill.
+WORKLOADS = {
+    "tiny_prefill": dict(kind="prefill", name="tiny prefill B=1 H=2 T=256 d=128 fp32", seed=20260, lengths=[256],
+                         H=2, dtype=torch.float32, lo=-0.2, s0_std=None),
+    "prefill_8k": dict(kind="prefill", name="prefill B=1 H=32 T=8192 d=128 bf16", seed=20261, lengths=[8192], H=32,
+                       dtype=torch.bfloat16, lo=-0.2, s0_std=None),
+    "varlen_prefill": dict(kind="prefill", name="varlen prefill N=16 len~U[1024,65536] H=32 d=128 bf16, S0~N(0,0.02)",
+                           seed=20262, lengths=None, num_seqs=16, len_lo=1024, len_hi=65536, H=32,
+                           dtype=torch.bfloat16, lo=-0.2, s0_std=0.02),
+    "decode_256x32": dict(kind="decode", name="decode N=256 H=32 d=128 bf16, 100 steps, S~N(0,0.02)", seed=20263,
+                          N=256, H=32, steps=100, dtype=torch.bfloat16, lo=-0.2, s_std=0.02),
+    "long_prefill_1m": dict(kind="prefill", name="long prefill B=1 H=32 T=1048576 d=128 bf16", seed=20264,
+                            lengths=[1048576], H=32, dtype=torch.bfloat16, lo=-0.05, s0_std=None),
 }
 
 
-def config_seed(idx: int) -> int:
-    return 20260 + int(idx)
+def workload_seed(name: str) -> int:
+    return int(WORKLOADS[name]["seed"])
 
 
 def varlen_lengths(num_seqs: int, lo: int, hi: int, seed: int) -> list[int]:
@@ -52,11 +52,11 @@ def varlen_lengths(num_seqs: int, lo: int, hi: int, seed: int) -> list[int]:
     return [int(x) for x in torch.randint(lo, hi + 1, (num_seqs,), generator=g)]
 
 
-def config_lengths(idx: int) -> list[int]:
-    c = CONFIGS[idx]
+def workload_lengths(name: str) -> list[int]:
+    c = WORKLOADS[name]
     if c.get("lengths") is not None:
         return list(c["lengths"])
-    return varlen_lengths(c["num_seqs"], c["len_lo"], c["len_hi"], config_seed(idx) + 7)
+    return varlen_lengths(c["num_seqs"], c["len_lo"], c["len_hi"], workload_seed(name) + 7)
 
 
 @dataclass
@@ -165,10 +165,10 @@ def decode_inputs(N: int, H: int, steps: int, d: int = 128, dtype=torch.bfloat16
     return DecodeInputs(q, k, v, beta, log_alpha, S, idx)
 
 
-def config_inputs(idx: int, device="cuda"):
-    c = CONFIGS[idx]
+def workload_inputs(name: str, device="cuda"):
+    c = WORKLOADS[name]
     if c["kind"] == "prefill":
-        return prefill_inputs(config_lengths(idx), c["H"], 128, c["dtype"], c["lo"], c["s0_std"],
-                              config_seed(idx), device)
+        return prefill_inputs(workload_lengths(name), c["H"], 128, c["dtype"], c["lo"], c["s0_std"],
+                              workload_seed(name), device)
     return decode_inputs(c["N"], c["H"], c["steps"], 128, c["dtype"], c["lo"], c["s_std"],
-                         config_seed(idx), device)
+                         workload_seed(name), device)

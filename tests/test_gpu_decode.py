@@ -59,8 +59,8 @@ def test_decode_bad_slot_is_reported_and_skipped():
 def test_decode_config3_graph_sampled():
     """256 sequences x 32 heads, 100 steps captured in one CUDA graph (the bench's launch
     configuration); o of every step and the final state checked on sampled (seq, head) units."""
-    c = synth.CONFIGS[3]
-    d = synth.config_inputs(3, device="cuda")
+    c = synth.WORKLOADS["decode_256x32"]
+    d = synth.workload_inputs("decode_256x32", device="cuda")
     N, H, steps = c["N"], c["H"], c["steps"]
     g = torch.Generator().manual_seed(99)
     units = [(int(n), int(h)) for n, h in zip(torch.randint(0, N, (48,), generator=g),

@@ -110,7 +110,7 @@ def test_prefill_fused_long_sequence_pieces():
 
 
 def test_prefill_fused_8k_workload():
-    p = synth.config_inputs(1, device="cuda")
+    p = synth.workload_inputs("prefill_8k", device="cuda")
     g = torch.Generator(device="cuda").manual_seed(624)
     T, H, _ = p.q.shape
     p.q = (p.q.float() * 1.7).to(p.q.dtype)

@@ -140,7 +140,7 @@ def test_prefill_bad_cu_seqlens_reported(path):
 
 
 def test_prefill_config0_tiny_fp32():
-    p = synth.config_inputs(0, device="cuda")
+    p = synth.workload_inputs("tiny_prefill", device="cuda")
     o, sf, st = run_gpu(p)
     assert st == 0 and o.dtype == torch.float32
     check_against_oracle(p, o, sf)
@@ -148,7 +148,7 @@ def test_prefill_config0_tiny_fp32():
 
 @pytest.mark.parametrize("path", PATHS)
 def test_prefill_config1_all_heads(path):
-    p = synth.config_inputs(1, device="cuda")
+    p = synth.workload_inputs("prefill_8k", device="cuda")
     o, sf, st = run_gpu(p, path=path)
     assert st == 0
     errs = check_against_oracle(p, o, sf)
@@ -156,7 +156,7 @@ def test_prefill_config1_all_heads(path):
 
 
 def test_prefill_config2_varlen_sampled_heads():
-    p = synth.config_inputs(2, device="cuda")
+    p = synth.workload_inputs("varlen_prefill", device="cuda")
     o, sf, st = run_gpu(p)
     assert st == 0
     N, H = len(p.lengths), p.q.shape[1]
@@ -167,7 +167,7 @@ def test_prefill_config2_varlen_sampled_heads():
 
 @pytest.mark.slow
 def test_prefill_config4_long_two_heads():
-    p = synth.config_inputs(4, device="cuda")
+    p = synth.workload_inputs("long_prefill_1m", device="cuda")
     o, sf, st = run_gpu(p)
     assert st == 0
     g = torch.Generator().manual_seed(4)

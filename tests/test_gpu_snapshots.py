@@ -90,7 +90,7 @@ def test_snapshots_across_pieces_of_a_long_sequence():
 def test_snapshots_on_the_8k_workload():
     # full-size 8k prefill (B=1, H=32, T=8192) with a state every 1024 tokens, in the
     # launch configuration the bench times; the oracle checks two sampled heads
-    p = synth.config_inputs(1, device="cuda")
+    p = synth.workload_inputs("prefill_8k", device="cuda")
     entries = [(0, 1024 * i) for i in range(1, 9)]
     o, sf, ss, st = _run(p, entries)
     assert st == 0
