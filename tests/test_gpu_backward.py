@@ -132,3 +132,26 @@ def test_backward_strong_decay():
     p = synth.prefill_inputs([256, 77], H=2, lo=-1.0, s0_std=0.02, seed=53)
     dO, dSf = _cotangents(p, 54)
     _compare(_gpu(p, dO, dSf), _oracle(p, dO, dSf))
+
+
+def test_backward_in_cuda_graph():
+    """The whole backward call (its chunkwise forward included) captures into a CUDA graph and
+    replays bit for bit like the eager call."""
+    p = synth.prefill_inputs([700, 130], H=2, s0_std=0.02, seed=55)
+    dO, dSf = _cotangents(p, 56)
+    ref = _gpu(p, dO, dSf)
+    T, H, _ = p.q.shape
+    ws = torch.empty(kda.kda_prefill_backward_workspace_bytes(p.q.dtype, 2, T, H), dtype=torch.uint8, device="cuda")
+    grads = tuple(torch.empty_like(x) for x in ref)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        kda.kda_prefill_backward(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, dSf, grads=grads,
+                                 workspace=ws, stream=s)
+    for x in grads:
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(grads, ref):
+        assert torch.equal(x, y)
