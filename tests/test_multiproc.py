@@ -52,3 +52,21 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(bench.argparse.Namespace(steps=1, warmup=0, cpu_seconds=1.0))
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line(monkeypatch, capsys):
+    """Rank 0 prints one JSON line with the contract's keys, the oracle as the reference."""
+    import json
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(bench.argparse.Namespace(steps=1, warmup=0, cpu_seconds=0.5))
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
