@@ -178,3 +178,31 @@ def rmsnorm_gate(o, g, w=None, eps: float = 0.0) -> np.ndarray:
     if w is not None:
         y = y * np.asarray(w, dtype=np.float64)
     return y * np.asarray(g, dtype=np.float64)
+
+
+def kda_prefill_backward_fused(q, k, v, log_alpha, beta, cu_seqlens, S0, dO, dS_final=None, l2norm_qk=True,
+                               beta_sigmoid=True, l2_eps: float = 0.0, nthreads: int = 0, lib=None):
+    """Gradient of the prefill with its fused prologue: q and k L2-normalised and beta = sigmoid(logits)
+    before the recurrence ("kimi delta attn from first principles" (aryagxr), "KDA Architecture" and
+    "KDA has three gates").  The recurrence's gradient is kda_prefill_backward at the normalised
+    inputs; the two elementwise maps are then differentiated in fp64:
+      x_hat = x / n, n = sqrt(sum_c x_c^2 + eps):  dx = (dx_hat - x_hat <x_hat, dx_hat>) / n
+      beta = sigmoid(b):                           db = dbeta * beta * (1 - beta)
+    Returns (dq, dk, dv, dlog_alpha, dbeta_logits_or_dbeta, dS0) in float64.
+    """
+    q64 = np.asarray(q, dtype=np.float64)
+    k64 = np.asarray(k, dtype=np.float64)
+    b64 = np.asarray(beta, dtype=np.float64)
+    qh = l2_normalize(q64, l2_eps) if l2norm_qk else q64
+    kh = l2_normalize(k64, l2_eps) if l2norm_qk else k64
+    bh = sigmoid(b64) if beta_sigmoid else b64
+    dq, dk, dv, dla, db, ds0 = kda_prefill_backward(qh, kh, v, log_alpha, bh, cu_seqlens, S0, dO, dS_final,
+                                                    nthreads=nthreads, lib=lib)
+    if l2norm_qk:
+        nq = np.sqrt(np.sum(q64 * q64, axis=-1, keepdims=True) + l2_eps)
+        nk = np.sqrt(np.sum(k64 * k64, axis=-1, keepdims=True) + l2_eps)
+        dq = (dq - qh * np.sum(qh * dq, axis=-1, keepdims=True)) / nq
+        dk = (dk - kh * np.sum(kh * dk, axis=-1, keepdims=True)) / nk
+    if beta_sigmoid:
+        db = db * bh * (1.0 - bh)
+    return dq, dk, dv, dla, db, ds0

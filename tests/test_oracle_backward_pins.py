@@ -65,3 +65,41 @@ def test_backward_without_final_gradient_and_empty_sequence():
             h = 2.0 ** -12
             fd = (4 * _fd(x, cu, dO, zero, name, idx, h / 2) - _fd(x, cu, dO, zero, name, idx, h)) / 3
             assert abs(grad[idx] - fd) <= 1e-7 * (1 + abs(fd)), (name, idx)
+
+
+def test_fused_prologue_backward_matches_finite_differences():
+    """kda_prefill_backward_fused (L2 norm of q, k and sigmoid beta before the recurrence) against
+    central differences of the fused forward evaluated in fp64 (the chunkwise CPU model, exact to
+    1e-12 against the oracle loop, so no fp32 rounding enters the differences)."""
+    from tests.chunk_model import chunk_prefill
+    rng = np.random.default_rng(11)
+    lengths = (3, 2)
+    H, dk, dv, T = 2, 3, 2, 5
+    x = dict(q=rng.standard_normal((T, H, dk)) * 1.7, k=rng.standard_normal((T, H, dk)) * 0.8,
+             v=rng.standard_normal((T, H, dv)), log_alpha=-0.4 * rng.random((T, H, dk)),
+             beta=rng.standard_normal((T, H)) * 1.5, S0=0.5 * rng.standard_normal((len(lengths), H, dk, dv)))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    dO = rng.standard_normal((T, H, dv))
+    dSf = rng.standard_normal((len(lengths), H, dk, dv))
+    eps = 1e-3
+
+    def loss(y):
+        o, sf = chunk_prefill(oracle.l2_normalize(y["q"], eps), oracle.l2_normalize(y["k"], eps), y["v"],
+                              y["log_alpha"], oracle.sigmoid(y["beta"]), cu, y["S0"], chunk=4)
+        return float(np.sum(o * dO) + np.sum(sf * dSf))
+
+    def fd(name, idx, h):
+        xp = {a: b.copy() for a, b in x.items()}
+        xm = {a: b.copy() for a, b in x.items()}
+        xp[name][idx] += h
+        xm[name][idx] -= h
+        return (loss(xp) - loss(xm)) / (2 * h)
+
+    g = oracle.kda_prefill_backward_fused(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], cu, x["S0"], dO, dSf,
+                                          l2_eps=eps)
+    for name, grad in zip(("q", "k", "v", "log_alpha", "beta", "S0"), g):
+        for idx in np.ndindex(*x[name].shape):
+            h = 2.0 ** -14
+            ref = (4 * fd(name, idx, h / 2) - fd(name, idx, h)) / 3
+            # the oracle's C routine takes its (normalised) inputs in float32: ~1e-7 relative
+            assert abs(grad[idx] - ref) <= 2e-6 * (1 + abs(ref)), (name, idx, grad[idx], ref)
