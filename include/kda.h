@@ -269,6 +269,35 @@ KDA_API kda_status kda_prefill_backward(const void *q, const void *k, const void
                                         kda_stream_t stream);
 
 /*
+ * kda_prefill_backward_ex -- kda_prefill_backward through the fused prologue
+ * of kda_prefill_ex: q, k are the raw projections (L2-normalised per (token,
+ * head) with KDA_FUSE_L2NORM_QK, "KDA Architecture") and beta the logits
+ * (KDA_FUSE_BETA_SIGMOID, "KDA has three gates").  grad_q, grad_k, grad_beta
+ * are then the gradients with respect to those raw inputs:
+ *     dx = (dx_hat - x_hat <x_hat, dx_hat>) / sqrt(|x|^2 + l2_eps),
+ *     db = dbeta_hat sigma(b) (1 - sigma(b)),
+ * the exact chain rule through the prologue, taken in fp32.  The call
+ * writes the normalised q, k (in qkv_dtype) and sigmoid beta into the
+ * workspace, runs the plain backward on them, and applies the chain rule in
+ * place.  KDA_FUSE_OUT_GATE returns KDA_ERR_UNSUPPORTED (the output gate's
+ * backward is not built); fusion NULL or flags 0 is kda_prefill_backward.
+ *
+ * Workspace: >= kda_prefill_backward_ex_workspace_bytes(...) (the plain
+ * figure plus (2 x 128 x sizeof(qkv_dtype) + 12) bytes per (token, head)).
+ * Other arguments, errors and overlap rules as kda_prefill_backward.
+ */
+KDA_API size_t kda_prefill_backward_ex_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
+                                                       int64_t total_tokens, int32_t H, int32_t dk, int32_t dv);
+KDA_API kda_status kda_prefill_backward_ex(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                           const float *log_alpha, const float *beta, const float *S0,
+                                           const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                           int32_t H, int32_t dk, int32_t dv, const void *grad_o,
+                                           const float *grad_S_final, float *grad_q, float *grad_k,
+                                           float *grad_v, float *grad_log_alpha, float *grad_beta,
+                                           float *grad_S0, const kda_fusion *fusion, void *workspace,
+                                           size_t workspace_bytes, int32_t *device_status, kda_stream_t stream);
+
+/*
  * kda_decode_step -- one fused recurrent step for N sequences
  * ("Understanding Kimi Delta Attention" (pyshine), section "The Chunkwise
  * DPLR Algorithm": the step-by-step "fused recurrent mode" for decode).

@@ -1,9 +1,10 @@
 """GB300-native Kimi Delta Attention: chunkwise prefill and fused decode (libkda).
 
 Python names mirror the C ABI in include/kda.h:
-  kda_prefill, kda_prefill_snapshots, kda_prefill_ex, kda_prefill_backward,
+  kda_prefill, kda_prefill_snapshots, kda_prefill_ex, kda_prefill_backward, kda_prefill_backward_ex,
   kda_decode_step, kda_decode_step_ex, kda_decode_multi, kda_decode_multi_ex,
-  kda_prefill_workspace_bytes, kda_prefill_backward_workspace_bytes, kda_status_string.
+  kda_prefill_workspace_bytes, kda_prefill_backward_workspace_bytes,
+  kda_prefill_backward_ex_workspace_bytes, kda_status_string.
 The library must be built first (``__graft_entry__.build()`` or
 ``python -m linear_attention_chunkwise_gb300._build``); there is no fallback.
 """
@@ -31,6 +32,8 @@ from ._binding import (  # noqa: F401
     kda_decode_step_ex,
     kda_prefill,
     kda_prefill_backward,
+    kda_prefill_backward_ex,
+    kda_prefill_backward_ex_workspace_bytes,
     kda_prefill_backward_workspace_bytes,
     kda_prefill_ex,
     kda_prefill_min_workspace_bytes,

@@ -61,7 +61,8 @@ class Fusion:
 EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_bytes",
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
                     "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex",
-                    "kda_decode_multi_ex", "kda_prefill_backward_workspace_bytes", "kda_prefill_backward")
+                    "kda_decode_multi_ex", "kda_prefill_backward_workspace_bytes", "kda_prefill_backward",
+                    "kda_prefill_backward_ex_workspace_bytes", "kda_prefill_backward_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -115,6 +116,11 @@ def load_library(path: str | None = None):
         lib.kda_prefill_backward.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
                                              P, P, P, P, P, P, P, sz, P, P]
         lib.kda_prefill_backward.restype = ctypes.c_int
+        lib.kda_prefill_backward_ex_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
+        lib.kda_prefill_backward_ex_workspace_bytes.restype = sz
+        lib.kda_prefill_backward_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
+                                                P, P, P, P, P, P, FP, P, sz, P, P]
+        lib.kda_prefill_backward_ex.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_multi.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P, P, P]
@@ -277,6 +283,13 @@ def kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens:
                                                                    int(dk), int(dv)))
 
 
+def kda_prefill_backward_ex_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: int, dk: int = 128,
+                                            dv: int = 128) -> int:
+    code = qkv_dtype if isinstance(qkv_dtype, int) else _dtype_code(qkv_dtype)
+    return int(load_library().kda_prefill_backward_ex_workspace_bytes(code, int(num_seqs), int(total_tokens),
+                                                                      int(H), int(dk), int(dv)))
+
+
 def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, grad_S_final=None, *,
                          need_grad_S0=True, grads=None, workspace=None, device_status=None, stream=None):
     """Gradient of kda_prefill for L = <o, grad_o> + <S_final, grad_S_final> (see include/kda.h).
@@ -285,6 +298,24 @@ def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, 
     Returns (grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0), all fp32; grad_S0 is None
     when need_grad_S0 is False.  `grads` may pass those six output tensors in.
     """
+    return _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0, grad_S_final, need_grad_S0, grads,
+                     workspace, device_status, stream, None)
+
+
+def kda_prefill_backward_ex(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, grad_S_final=None, *,
+                            fusion=None, need_grad_S0=True, grads=None, workspace=None, device_status=None,
+                            stream=None):
+    """kda_prefill_backward through the fused prologue of `fusion` (a Fusion: l2norm_qk, beta_sigmoid).
+
+    q, k are the raw projections and beta the logits, as kda_prefill_ex takes them; grad_q, grad_k,
+    grad_beta are with respect to those.  An output gate raises KdaError (KDA_ERR_UNSUPPORTED).
+    """
+    return _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0, grad_S_final, need_grad_S0, grads,
+                     workspace, device_status, stream, fusion)
+
+
+def _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0, grad_S_final, need_grad_S0, grads, workspace,
+              device_status, stream, fusion):
     lib = load_library()
     dev = q.device
     _check(q, "q", device=dev)
@@ -310,18 +341,26 @@ def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, 
         raise ValueError("grads must hold six tensors (the last may be None)")
     for t, n in zip(grads, ("grad_q", "grad_k", "grad_v", "grad_log_alpha", "grad_beta", "grad_S0")):
         _check(t, n, torch.float32, dev)
-    need = int(lib.kda_prefill_backward_workspace_bytes(code, N, T, H, dk, dv))
+    fused = fusion is not None
+    query = lib.kda_prefill_backward_ex_workspace_bytes if fused else lib.kda_prefill_backward_workspace_bytes
+    need = int(query(code, N, T, H, dk, dv))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", torch.uint8, dev)
     _check(device_status, "device_status", torch.int32, dev)
     gq, gk, gv, gla, gb, gs0 = grads
-    st = lib.kda_prefill_backward(_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                                  _ptr(cu_seqlens), N, T, H, dk, dv, _ptr(grad_o), _ptr(grad_S_final), _ptr(gq),
-                                  _ptr(gk), _ptr(gv), _ptr(gla), _ptr(gb), _ptr(gs0), _ptr(workspace),
-                                  workspace.numel(), _ptr(device_status), _stream_handle(stream))
+    args = [_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens), N, T, H, dk,
+            dv, _ptr(grad_o), _ptr(grad_S_final), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gla), _ptr(gb), _ptr(gs0)]
+    tail = [_ptr(workspace), workspace.numel(), _ptr(device_status), _stream_handle(stream)]
+    if fused:
+        name = "kda_prefill_backward_ex"
+        fz = _check_fusion(fusion, q, T)
+        st = lib.kda_prefill_backward_ex(*args, ctypes.byref(fz), *tail)
+    else:
+        name = "kda_prefill_backward"
+        st = lib.kda_prefill_backward(*args, *tail)
     if st != KDA_OK:
-        raise KdaError("kda_prefill_backward", st, kda_status_string(st))
+        raise KdaError(name, st, kda_status_string(st))
     return gq, gk, gv, gla, gb, gs0
 
 

@@ -515,6 +515,22 @@ BwdLayout bwd_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
     return b;
 }
 
+// After the plain backward's workspace: the fused prologue's normalised q, k (input dtype), sigmoid beta
+// and the inverse norms of q and k, per (token, head).
+struct BwdPrologueLayout {
+    size_t qh = 0, kh = 0, bh = 0, inv = 0, total = 0;
+};
+BwdPrologueLayout bwd_prologue_layout(kda_dtype t, int64_t T, int32_t H, size_t plain_total) {
+    BwdPrologueLayout p;
+    const size_t rows = static_cast<size_t>(T) * H;
+    p.qh = round_up(plain_total, kAlign);
+    p.kh = p.qh + round_up(rows * kHeadDim * esize_of(t), kAlign);
+    p.bh = p.kh + round_up(rows * kHeadDim * esize_of(t), kAlign);
+    p.inv = p.bh + round_up(rows * 4, kAlign);
+    p.total = p.inv + round_up(rows * 8, kAlign);
+    return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -526,19 +542,32 @@ size_t kda_prefill_backward_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seq
     return bwd_layout(qkv_dtype, num_seqs, total_tokens, H).total;
 }
 
-kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
-                                const float* log_alpha, const float* beta, const float* S0,
-                                const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
-                                int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
-                                float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
-                                float* grad_beta, float* grad_S0, void* workspace, size_t workspace_bytes,
-                                int32_t* device_status, kda_stream_t stream_) {
+size_t kda_prefill_backward_ex_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens,
+                                               int32_t H, int32_t dk, int32_t dv) {
+    const size_t plain = kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
+    return plain == 0 ? 0 : bwd_prologue_layout(qkv_dtype, total_tokens, H, plain).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The backward of kda_prefill, optionally through the fused prologue `pre` (flags 0 = plain inputs).
+kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                         const float* log_alpha, const float* beta, const float* S0,
+                         const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                         int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
+                         float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
+                         float* grad_beta, float* grad_S0, void* workspace, size_t workspace_bytes,
+                         int32_t* device_status, kda_stream_t stream_, uint32_t pre_flags, float l2_eps) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
-    const size_t need = kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
-    if (need == 0 || !sizes_ok(num_seqs, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
+    const size_t plain_need = kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
+    if (plain_need == 0 || !sizes_ok(num_seqs, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
+    const BwdPrologueLayout pl = bwd_prologue_layout(qkv_dtype, total_tokens, H, plain_need);
+    const size_t need = pre_flags ? pl.total : plain_need;
     if (!cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
     const bool have_tokens = total_tokens > 0;
     if (have_tokens && (!q || !k || !v || !log_alpha || !beta || !grad_o || !grad_q || !grad_k || !grad_v ||
@@ -588,6 +617,20 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
     const kda_status dev = check_device();
     if (dev != KDA_OK) return dev;
 
+    // 0. fused prologue: normalised q, k and sigmoid beta into the workspace's tail
+    const int64_t rows = total_tokens * H;
+    uint8_t* const wsb = static_cast<uint8_t*>(workspace);
+    const bool f32_io = qkv_dtype == KDA_DTYPE_F32;
+    const bool norm = (pre_flags & KDA_FUSE_L2NORM_QK) != 0, sig = (pre_flags & KDA_FUSE_BETA_SIGMOID) != 0;
+    const void* const qc = norm ? static_cast<const void*>(wsb + pl.qh) : q;
+    const void* const kc = norm ? static_cast<const void*>(wsb + pl.kh) : k;
+    const float* const bc = sig ? reinterpret_cast<const float*>(wsb + pl.bh) : beta;
+    float* const inv = reinterpret_cast<float*>(wsb + pl.inv);
+    if (pre_flags && kda::launch_bwd_prologue(f32_io, q, k, beta, wsb + pl.qh, wsb + pl.kh,
+                                              reinterpret_cast<float*>(wsb + pl.bh), inv, rows, pre_flags, l2_eps,
+                                              stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+
     // 1. chunk table (validates cu_seqlens into device_status) and a snapshot entry at every chunk end
     const WsLayout fwd = split_layout(qkv_dtype, num_seqs, total_tokens, H);
     const BwdLayout lay = bwd_layout(qkv_dtype, num_seqs, total_tokens, H);
@@ -607,17 +650,17 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
     snap.pos = snap_pos;
     snap.count = static_cast<int32_t>(lay.entries);
     snap.S = ckpt;
-    const kda_status fs = prefill_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens,
+    const kda_status fs = prefill_impl(qc, kc, v, qkv_dtype, log_alpha, bc, S0, cu_seqlens, num_seqs, total_tokens,
                                        H, dk, dv, ws + lay.o, nullptr, snap, nullptr, workspace, fwd.total, nullptr,
                                        stream_);
     if (fs != KDA_OK) return fs;
     // 3. prep, scan of the adjoint over chunks, value and key kernels
     kda::BackwardArgs a;
-    a.q = q;
-    a.k = k;
+    a.q = qc;
+    a.k = kc;
     a.v = v;
     a.log_alpha = log_alpha;
-    a.beta = beta;
+    a.beta = bc;
     a.S0 = S0;
     a.cu_seqlens = cu_seqlens;
     a.order = reinterpret_cast<const int32_t*>(ws);  // the prefill's schedule
@@ -636,8 +679,43 @@ kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda
     a.u_scratch = grad_q;
     a.num_seqs = num_seqs;
     a.H = H;
-    return kda::launch_backward(a, qkv_dtype == KDA_DTYPE_F32, lay.entries, stream) == cudaSuccess ? KDA_OK
-                                                                                                  : KDA_ERR_CUDA;
+    if (kda::launch_backward(a, f32_io, lay.entries, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    // 4. chain rule through the prologue, in place on grad_q, grad_k, grad_beta
+    if (pre_flags && kda::launch_bwd_epilogue(f32_io, q, k, reinterpret_cast<const float*>(wsb + pl.bh), inv,
+                                              grad_q, grad_k, grad_beta, rows, pre_flags, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_backward(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                const float* log_alpha, const float* beta, const float* S0,
+                                const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
+                                float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
+                                float* grad_beta, float* grad_S0, void* workspace, size_t workspace_bytes,
+                                int32_t* device_status, kda_stream_t stream) {
+    return backward_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
+                         grad_o, grad_S_final, grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0, workspace,
+                         workspace_bytes, device_status, stream, 0u, 0.f);
+}
+
+kda_status kda_prefill_backward_ex(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                   const float* log_alpha, const float* beta, const float* S0,
+                                   const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                   int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
+                                   float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
+                                   float* grad_beta, float* grad_S0, const kda_fusion* fusion, void* workspace,
+                                   size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
+    kda::DecodeFusion fz;
+    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
+    if (fz.flags & KDA_FUSE_OUT_GATE) return KDA_ERR_UNSUPPORTED;
+    return backward_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
+                         grad_o, grad_S_final, grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0, workspace,
+                         workspace_bytes, device_status, stream, fz.flags, fz.l2_eps);
 }
 
 }  // extern "C"

@@ -71,6 +71,18 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 template <typename T>
+__device__ __forceinline__ void st4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void st4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&a);
+    w.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = w;
+}
+template <typename T>
 __device__ __forceinline__ float ld1(const T* p);
 template <>
 __device__ __forceinline__ float ld1<float>(const float* p) { return *p; }
@@ -745,6 +757,69 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
     }
 }
 
+// ============================================================ fused prologue ==
+// kda_prefill_backward_ex: the prologue of "kimi delta attn from first principles" (aryagxr),
+// "KDA Architecture" (q, k L2-normalised) and "KDA has three gates" (beta = sigmoid of its
+// projection) is applied to copies before the backward, and differentiated after it:
+//   x_hat = x s, s = 1 / sqrt(sum_c x_c^2 + eps):  dx = s (dx_hat - x_hat <x_hat, dx_hat>)
+//   beta = sigmoid(b):                             db = dbeta beta (1 - beta)
+// One warp per (token, head) row; x_hat is recomputed in fp32 from the original x.
+template <typename IoT>
+__global__ void kda_bwd_prologue_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k,
+                                        const float* __restrict__ beta, IoT* __restrict__ qh, IoT* __restrict__ kh,
+                                        float* __restrict__ bh, float* __restrict__ inv, int64_t rows, uint32_t flags,
+                                        float eps) {
+    const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    if (flags & KDA_FUSE_L2NORM_QK) {
+        const size_t o = static_cast<size_t>(row) * D + 4 * lane;
+        const float4 qv = ld4(q + o), kv = ld4(k + o);
+        float aq = qv.x * qv.x + qv.y * qv.y + qv.z * qv.z + qv.w * qv.w;
+        float ak = kv.x * kv.x + kv.y * kv.y + kv.z * kv.z + kv.w * kv.w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            aq += __shfl_xor_sync(0xffffffffu, aq, off);
+            ak += __shfl_xor_sync(0xffffffffu, ak, off);
+        }
+        const float sq = 1.f / sqrtf(aq + eps), sk = 1.f / sqrtf(ak + eps);
+        st4(qh + o, make_float4(qv.x * sq, qv.y * sq, qv.z * sq, qv.w * sq));
+        st4(kh + o, make_float4(kv.x * sk, kv.y * sk, kv.z * sk, kv.w * sk));
+        if (lane == 0) *reinterpret_cast<float2*>(inv + 2 * row) = make_float2(sq, sk);
+    }
+    if ((flags & KDA_FUSE_BETA_SIGMOID) && lane == 0) bh[row] = 1.f / (1.f + expf(-beta[row]));
+}
+
+template <typename IoT>
+__global__ void kda_bwd_epilogue_kernel(const IoT* __restrict__ q, const IoT* __restrict__ k,
+                                        const float* __restrict__ bh, const float* __restrict__ inv,
+                                        float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dbeta,
+                                        int64_t rows, uint32_t flags) {
+    const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    if (flags & KDA_FUSE_L2NORM_QK) {
+        const size_t o = static_cast<size_t>(row) * D + 4 * lane;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const float s = inv[2 * row + w];
+            const float4 x = ld4((w == 0 ? q : k) + o);
+            float* g = (w == 0 ? dq : dk) + o;
+            const float4 d = *reinterpret_cast<const float4*>(g);
+            const float4 xh = make_float4(x.x * s, x.y * s, x.z * s, x.w * s);
+            float dot = xh.x * d.x + xh.y * d.y + xh.z * d.z + xh.w * d.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            *reinterpret_cast<float4*>(g) = make_float4(s * (d.x - xh.x * dot), s * (d.y - xh.y * dot),
+                                                        s * (d.z - xh.z * dot), s * (d.w - xh.w * dot));
+        }
+    }
+    if ((flags & KDA_FUSE_BETA_SIGMOID) && lane == 0) {
+        const float b = bh[row];
+        dbeta[row] *= b * (1.f - b);
+    }
+}
+
 // Snapshot entries for every chunk end of every sequence: entry chunk_off[n] + c - 1 is the state
 // after chunk c - 1 of sequence n (c = 1 .. nch_n; the last is the final state).  Entries past the
 // batch's chunk count are sentinels (sequence N) that no scan CTA takes.
@@ -802,6 +877,37 @@ cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_
     const int threads = 128, blocks = (N + 1 + threads - 1) / threads;
     kda_ckpt_entries_kernel<<<blocks, threads, 0, stream>>>(cu_seqlens, chunk_off, N, max_entries, snap_seq,
                                                             snap_pos);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prologue(bool f32_io, const void* q, const void* k, const float* beta, void* qh, void* kh,
+                                float* bh, float* inv, int64_t rows, uint32_t flags, float eps, cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (f32_io)
+        kda_bwd_prologue_kernel<float><<<blocks, 256, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), beta, static_cast<float*>(qh),
+            static_cast<float*>(kh), bh, inv, rows, flags, eps);
+    else
+        kda_bwd_prologue_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), beta,
+            static_cast<__nv_bfloat16*>(qh), static_cast<__nv_bfloat16*>(kh), bh, inv, rows, flags, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_epilogue(bool f32_io, const void* q, const void* k, const float* bh, const float* inv,
+                                float* dq, float* dk, float* dbeta, int64_t rows, uint32_t flags,
+                                cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    if (f32_io)
+        kda_bwd_epilogue_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(q),
+                                                                   static_cast<const float*>(k), bh, inv, dq, dk,
+                                                                   dbeta, rows, flags);
+    else
+        kda_bwd_epilogue_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), bh, inv, dq, dk, dbeta,
+            rows, flags);
     return cudaGetLastError();
 }
 

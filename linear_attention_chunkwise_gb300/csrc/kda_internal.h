@@ -128,6 +128,13 @@ size_t backward_record_bytes();
 // Snapshot entries at every chunk end (and sentinels up to max_entries) from the chunk table.
 cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_off, int32_t N, int32_t max_entries,
                                 int32_t* snap_seq, int32_t* snap_pos, cudaStream_t stream);
+// Fused prologue of the backward (q, k L2 norms, sigmoid beta into copies; inv = 1/norm of q and k
+// per (token, head)) and the chain rule through it afterwards, in place on dq, dk, dbeta.
+cudaError_t launch_bwd_prologue(bool f32_io, const void* q, const void* k, const float* beta, void* qh, void* kh,
+                                float* bh, float* inv, int64_t rows, uint32_t flags, float eps, cudaStream_t stream);
+cudaError_t launch_bwd_epilogue(bool f32_io, const void* q, const void* k, const float* bh, const float* inv,
+                                float* dq, float* dk, float* dbeta, int64_t rows, uint32_t flags,
+                                cudaStream_t stream);
 // prep, scan, value and key kernels; chunk_slots bounds the batch's chunk count.
 cudaError_t launch_backward(const BackwardArgs& a, bool f32_io, int64_t chunk_slots, cudaStream_t stream);
 

@@ -284,3 +284,62 @@ TOK = 128 * 2 * 128
 ])
 def test_backward_rejects_bad_arguments(lib, over, expect):
     assert _backward(lib, **over) == expect
+
+
+def test_backward_ex_workspace_bytes(lib):
+    # the plain backward's workspace, then normalised q and k (input dtype), sigmoid beta (fp32) and the
+    # two inverse norms (fp32) per (token, head), each region 256-byte aligned
+    up = lambda x: -(-x // 256) * 256
+    for dt, es in ((kda.KDA_DTYPE_BF16, 2), (kda.KDA_DTYPE_F32, 4)):
+        for T, H, N in ((128, 2, 1), (1000, 32, 16), (0, 4, 3)):
+            plain = kda.kda_prefill_backward_workspace_bytes(dt, N, T, H)
+            want = plain + 2 * up(T * H * 128 * es) + up(T * H * 4) + up(T * H * 8)
+            assert kda.kda_prefill_backward_ex_workspace_bytes(dt, N, T, H) == want
+    assert kda.kda_prefill_backward_ex_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
+    assert kda.kda_prefill_backward_ex_workspace_bytes(kda.KDA_DTYPE_BF16, 1, 10, 2, 128, 64) == 0
+
+
+def _backward_ex(lib, fz, **over):
+    T, H, N = 128, 2, 1
+    tok = T * H * 128
+    need = kda.kda_prefill_backward_ex_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H)
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, dO=BASE + 12 * tok, dSf=None,
+             gq=BASE + 20 * tok, gk=BASE + 24 * tok, gv=BASE + 28 * tok, gla=BASE + 32 * tok, gb=BASE + 36 * tok,
+             gs0=BASE + 40 * tok, ws=BASE + 64 * tok, wsb=need, status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill_backward_ex(P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]),
+                                       P(a["S0"]), P(a["cu"]), a["N"], a["T"], a["H"], a["dk"], a["dv"],
+                                       P(a["dO"]), P(a["dSf"]), P(a["gq"]), P(a["gk"]), P(a["gv"]), P(a["gla"]),
+                                       P(a["gb"]), P(a["gs0"]), None if fz is None else ctypes.byref(fz),
+                                       P(a["ws"]), a["wsb"], P(a["status"]), None)
+
+
+PLAIN_BWD_WS = 128 * 2 * 128 * 64  # offset of the workspace in the fake layout above
+
+
+@pytest.mark.parametrize("fz,over,expect", [
+    (dict(flags=0x8), {}, kda.KDA_ERR_INVALID_ARG),                                    # unknown flag
+    (dict(flags=kda.KDA_FUSE_L2NORM_QK, l2_eps=-1.0), {}, kda.KDA_ERR_INVALID_ARG),     # negative eps
+    (dict(flags=kda.KDA_FUSE_OUT_GATE), {}, kda.KDA_ERR_INVALID_ARG),                   # gate missing
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GATE), {}, kda.KDA_ERR_UNSUPPORTED),           # gate's backward not built
+    (dict(flags=kda.KDA_FUSE_L2NORM_QK | kda.KDA_FUSE_BETA_SIGMOID), dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(flags=kda.KDA_FUSE_BETA_SIGMOID), dict(gq=BASE + 2 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),  # = k
+])
+def test_backward_ex_rejects_bad_arguments(lib, fz, over, expect):
+    assert _backward_ex(lib, _fusion(**fz), **over) == expect
+
+
+def test_backward_ex_workspace_covers_the_prologue_copies(lib):
+    """The plain figure is too small once a prologue flag is set, and the copies' tail is checked for overlap."""
+    N, T, H = 1, 128, 2
+    plain = kda.kda_prefill_backward_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H)
+    fz = _fusion(flags=kda.KDA_FUSE_L2NORM_QK)
+    assert _backward_ex(lib, fz, wsb=plain) == kda.KDA_ERR_WORKSPACE
+    in_tail = BASE + PLAIN_BWD_WS + plain  # grad_S0 on the normalised-q copy
+    assert _backward_ex(lib, fz, gs0=in_tail) == kda.KDA_ERR_INVALID_ARG
+    # without prologue flags the tail is not the call's: the same grad_S0 passes every argument check
+    # and the call stops only at the device check (no GPU here)
+    for none in (None, _fusion(flags=0)):
+        assert _backward_ex(lib, none, gs0=in_tail, wsb=plain) == kda.KDA_ERR_CUDA

@@ -155,3 +155,74 @@ def test_backward_in_cuda_graph():
     torch.cuda.synchronize()
     for x, y in zip(grads, ref):
         assert torch.equal(x, y)
+
+
+# ------------------------------------------------------------- fused prologue --
+L2_EPS = 1e-6
+
+
+def _raw(lengths, H, dtype, seed):
+    """Inputs as kda_prefill_ex takes them raw: q, k rows scaled by U[0.3, 3], beta as N(0, 1.5^2) logits."""
+    p = synth.prefill_inputs(lengths, H=H, dtype=dtype, s0_std=0.02, seed=seed)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed + 7)
+    T = p.q.shape[0]
+    p.q = (p.q.float() * (0.3 + 2.7 * torch.rand((T, H, 1), generator=g, device="cuda"))).to(dtype)
+    p.k = (p.k.float() * (0.3 + 2.7 * torch.rand((T, H, 1), generator=g, device="cuda"))).to(dtype)
+    p.beta = torch.randn((T, H), generator=g, device="cuda") * 1.5
+    return p
+
+
+def _fused_oracle(p, dO, dSf, l2norm_qk, beta_sigmoid):
+    return oracle.kda_prefill_backward_fused(host(p.q), host(p.k), host(p.v), host(p.log_alpha), host(p.beta),
+                                             p.cu_seqlens.cpu().numpy(), host(p.S0), host(dO),
+                                             None if dSf is None else host(dSf), l2norm_qk=l2norm_qk,
+                                             beta_sigmoid=beta_sigmoid, l2_eps=L2_EPS)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_backward_fused_prologue_matches_oracle(dtype):
+    p = _raw([300, 0, 64, 1, 129, 200], H=2, dtype=dtype, seed=61)
+    dO, dSf = _cotangents(p, 62)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS)
+    got = kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, dSf, fusion=fz,
+                                      device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _compare(got, _fused_oracle(p, dO, dSf, True, True))
+
+
+@pytest.mark.parametrize("l2norm_qk,beta_sigmoid", [(True, False), (False, True)])
+def test_backward_fused_prologue_single_flags(l2norm_qk, beta_sigmoid):
+    p = _raw([190, 70], H=3, dtype=torch.bfloat16, seed=63)
+    if not l2norm_qk:  # the plain recurrence wants unit-norm q, k
+        p.q = torch.nn.functional.normalize(p.q.float(), dim=-1).to(p.q.dtype)
+        p.k = torch.nn.functional.normalize(p.k.float(), dim=-1).to(p.k.dtype)
+    if not beta_sigmoid:
+        p.beta = torch.sigmoid(p.beta)
+    dO, dSf = _cotangents(p, 64)
+    fz = kda.Fusion(l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid, l2_eps=L2_EPS)
+    got = kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, dSf, fusion=fz)
+    torch.cuda.synchronize()
+    _compare(got, _fused_oracle(p, dO, dSf, l2norm_qk, beta_sigmoid))
+
+
+def test_backward_ex_without_flags_is_the_plain_backward():
+    p = synth.prefill_inputs([100, 250], H=2, s0_std=0.02, seed=65)
+    dO, dSf = _cotangents(p, 66)
+    a = _gpu(p, dO, dSf)
+    b = kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, dSf,
+                                    fusion=kda.Fusion())
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_ex_rejects_the_output_gate():
+    p = _raw([64], H=1, dtype=torch.bfloat16, seed=67)
+    dO, _ = _cotangents(p, 68, with_final=False)
+    fz = kda.Fusion(l2norm_qk=True, out_gate=torch.ones_like(p.q))
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, fusion=fz)
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
