@@ -366,6 +366,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     if (kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     kda::PrefillArgs a;
+    a.log_alpha = log_alpha;
     a.beta = beta;
     a.S0 = S0;
     a.cu_seqlens = cu_seqlens;
@@ -402,7 +403,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
             cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
             ps = piece_streams();
         if (!ps)
-            return kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_la, og ? &tm_g : nullptr, a,
+            return kda::launch_prefill_split(tm_q, tm_k, tm_v, og ? &tm_g : nullptr, a,
                                              max_chunks(num_seqs, total_tokens), out_f32,
                                              stream) == cudaSuccess
                        ? KDA_OK
@@ -432,7 +433,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
                 a.piece_begin = static_cast<int32_t>(prepared);
                 a.piece_len = static_cast<int32_t>(prep_end - prepared);
                 ok = ok &&
-                     kda::launch_chunk_prep(tm_q, tm_k, tm_la, a, static_cast<int64_t>(num_seqs) * a.piece_len,
+                     kda::launch_chunk_prep(tm_q, tm_k, a, static_cast<int64_t>(num_seqs) * a.piece_len,
                                             stream) == cudaSuccess &&
                      cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
                      cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess;

@@ -32,6 +32,7 @@ cudaError_t launch_decode_multi(bool f32_io, const void* q, const void* k, const
 
 // ---- prefill ----
 struct PrefillArgs {
+    const float* log_alpha;  // two-pass path's pass 1 reads it directly (the single pass by TMA)
     const float* beta;
     const float* S0;
     const int32_t* cu_seqlens;
@@ -86,13 +87,12 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
                                int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
                                int32_t num_snaps, cudaStream_t stream);
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap& tm_la, const CUtensorMap* tm_g, const PrefillArgs& a,
+                                 const CUtensorMap* tm_g, const PrefillArgs& a,
                                  int64_t max_chunks, bool out_f32, cudaStream_t stream);
 // The two passes separately, for the piecewise schedule.  Pass 1's grid is
 // `units` x H CTAs: units = chunk slots of the whole batch (piece_len = 0) or
 // num_seqs x piece_len (piece mode).  Pass 2 has num_seqs x H x 2 CTAs.
-cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_la,
-                              const PrefillArgs& a, int64_t units, cudaStream_t stream);
+cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units, cudaStream_t stream);
 // tm_g: TMA map of the output gate (required with KDA_FUSE_OUT_GATE, else unused / NULL).
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
                               cudaStream_t stream);

@@ -245,8 +245,9 @@ __global__ void __launch_bounds__(NT, 1)
             if (tid == 0) fl_la = fl_qk = false;
             wait_bar(BAR_LA);
             wait_bar(BAR_QK);
-            gate_chunk(reinterpret_cast<const float*>(sm + L::LA), opa, opkb, Lc, red, beta_s, beta_next, egm,
-                       egc + b * 128, egcm + b * 128, tid);
+            float g0[16], g1[16];
+            gate_load(reinterpret_cast<const float*>(sm + L::LA), D, Lc, tid, g0, g1);
+            gate_chunk(g0, g1, opa, opkb, Lc, red, beta_s, beta_next, egm, egc + b * 128, egcm + b * 128, tid);
             if (tid == 0 && c + 1 < nch) {  // log_alpha staging consumed: fetch the next chunk's
                 issue_la(c + 1);
                 fl_la = true;
@@ -342,8 +343,8 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_before();
             __syncthreads();
             // ---- T = (I + N)^-1;  Tb = T Diag(beta) -> rows 0..63 of OP_A3 ----
-            lower_inverse(Nf, Tf, Xs, tid);
-            store_tb(sm + L::OP_A3, Tf, beta_s, tid);
+            lower_inverse(rows64(Nf), rows64(Tf), Xs, tid);
+            store_tb(sm + L::OP_A3, rows64(Tf), beta_s, tid);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();

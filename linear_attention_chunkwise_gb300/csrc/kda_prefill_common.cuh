@@ -49,6 +49,22 @@ __device__ __forceinline__ float4& m4(float* M, int r, int c4) {
 __device__ __forceinline__ float& m1(float* M, int r, int c) {
     return M[r * 64 + ((((c >> 2) ^ r) & 15) << 2) + (c & 3)];
 }
+// The same [64][64] scratch with rows 0..31 at `lo` and rows 32..63 at `hi` (two separate 8 KB
+// regions, e.g. the halves of a tile that has already been stored).
+struct Rows64 {
+    float* lo;
+    float* hi;
+};
+__device__ __forceinline__ Rows64 rows64(float* M) { return Rows64{M, M + 32 * 64}; }
+__device__ __forceinline__ float* row_of(const Rows64& M, int r) {
+    return (r < 32 ? M.lo : M.hi) + (r & 31) * 64;
+}
+__device__ __forceinline__ float4& m4(const Rows64& M, int r, int c4) {
+    return *reinterpret_cast<float4*>(row_of(M, r) + (((c4 ^ r) & 15) << 2));
+}
+__device__ __forceinline__ float& m1(const Rows64& M, int r, int c) {
+    return row_of(M, r)[((((c >> 2) ^ r) & 15) << 2) + (c & 3)];
+}
 
 __device__ __forceinline__ uint4 pack8(const float* v) {
     uint4 pk;
@@ -75,28 +91,39 @@ __device__ __forceinline__ float4 fma4(float s, const float4& a, const float4& a
     return make_float4(fmaf(s, a.x, acc.x), fmaf(s, a.y, acc.y), fmaf(s, a.z, acc.z), fmaf(s, a.w, acc.w));
 }
 
+// log_alpha of the rows this thread handles in the gate phase (rows 16 (tid / 64) .. +15, channels
+// 2 (tid % 64), +1; zero past row Lc), from shared or global memory with `stride` floats per row.
+__device__ __forceinline__ void gate_load(const float* la, int stride, int Lc, int tid, float (&g0)[16],
+                                          float (&g1)[16]) {
+    const int cp = tid & 63, rq = tid >> 6;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * rq + i;
+        float2 l2 = make_float2(0.f, 0.f);
+        if (r < Lc) l2 = *reinterpret_cast<const float2*>(la + static_cast<size_t>(r) * stride + 2 * cp);
+        g0[i] = l2.x;
+        g1[i] = l2.y;
+    }
+}
+
 // Gate phase of one chunk (all NT threads; one __syncthreads inside).
-//   la_s : [64][128] f32 log_alpha of the chunk (plain rows)
+//   g0/g1: this thread's log_alpha values from gate_load (overwritten)
 //   opa  : operand tile [2 blk][128 rows][128 B]; rows 0..63 hold k and rows
 //          64..127 hold q on entry (128B-swizzled bf16), Kh and Qh on exit
 //   opkb : [2 blk][64 rows][128 B], receives Kb
 //   Lc   : valid rows of the chunk; red: f32 [4][128] scratch
 //   beta_s[64] receives beta (masked) from beta_cur of threads 0..63
 //   egm/egc/egcm[128] receive exp(gm), exp(gC), exp(gC - gm) per channel
-__device__ __forceinline__ void gate_chunk(const float* la_s, uint8_t* opa, uint8_t* opkb, int Lc, float* red,
-                                           float* beta_s, float beta_cur, float* egm, float* egc, float* egcm,
-                                           int tid, const float* inv_norm = nullptr) {
+__device__ __forceinline__ void gate_chunk(float (&g0)[16], float (&g1)[16], uint8_t* opa, uint8_t* opkb, int Lc,
+                                           float* red, float* beta_s, float beta_cur, float* egm, float* egc,
+                                           float* egcm, int tid, const float* inv_norm = nullptr) {
     const int cp = tid & 63;  // channel pair (2cp, 2cp+1)
     const int rq = tid >> 6;  // rows 16rq .. 16rq+15
-    float g0[16], g1[16];
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const int r = 16 * rq + i;
-        float2 l2 = make_float2(0.f, 0.f);
-        if (r < Lc) l2 = *reinterpret_cast<const float2*>(la_s + r * D + 2 * cp);
-        acc0 += l2.x;
-        acc1 += l2.y;
+        acc0 += g0[i];
+        acc1 += g1[i];
         g0[i] = acc0;
         g1[i] = acc1;
     }
@@ -182,7 +209,7 @@ __device__ __forceinline__ void store_m_row(uint8_t* tile, int row, int rr, int 
 }
 
 // Tb = T Diag(beta) (lower incl. diagonal) -> bf16 rows 0..63 of a swizzled tile.
-__device__ __forceinline__ void store_tb(uint8_t* tile, float* Tf, const float* beta_s, int tid) {
+__device__ __forceinline__ void store_tb(uint8_t* tile, const Rows64& Tf, const float* beta_s, int tid) {
     const int r = tid >> 2, c0 = 16 * (tid & 3);
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -204,7 +231,7 @@ __device__ __forceinline__ void store_tb(uint8_t* tile, float* Tf, const float* 
 // T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
 // diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
 // for block distance d = R - I = 1, 2, 3.  All NT threads; ends synchronised.
-__device__ __forceinline__ void lower_inverse(float* Nf, float* Tf, float* Xs, int tid) {
+__device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
         const int B = warp, j = lane;

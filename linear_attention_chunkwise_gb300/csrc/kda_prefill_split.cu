@@ -175,28 +175,35 @@ __global__ void __launch_bounds__(1024) kda_chunk_table_kernel(const int32_t* __
 }
 
 // =========================================================== pass 1 ======
+// Three CTAs per SM (the kernel is latency-bound: its throughput grows with
+// the CTAs resident).  To fit, log_alpha goes straight from global memory to
+// registers, and the parts of the image that are final after the gate phase
+// (Qh, Kb, the exp vectors) are stored right away, so that their shared
+// memory holds the inverse's fp32 scratch: N in the Kb tile, T in the two Qh
+// halves, the partial sums and the block products in the Tb rows.
 struct PrepSmem {
     static constexpr uint32_t OP_A = 0;          // [2 blk][128 rows][128 B]: [k;q] -> [Kh;Qh] -> [-W;Qh]
-    static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb
+    static constexpr uint32_t T_LO = OP_A + 8192;           // f32 rows 0..31 of T (blk 0's Qh rows)
+    static constexpr uint32_t T_HI = OP_A + 16384 + 8192;   // f32 rows 32..63 of T (blk 1's Qh rows)
+    static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb, then f32 [64][64] N
     static constexpr uint32_t OP_A3 = 49152;     // [Tb (64 rows) | M (64 rows)] x 128 B
-    static constexpr uint32_t LA = 65536;        // [64][128] f32 log_alpha; then the inverse scratch
-    static constexpr uint32_t INV_N = LA;        // f32 [64][64]
-    static constexpr uint32_t INV_T = LA + 16384;
-    static constexpr uint32_t XS = LA + 32768;   // f32 [3][16][16]
-    static constexpr uint32_t BETA = XS + 3072;  // f32 [64]
-    static constexpr uint32_t RED = BETA + 256;  // f32 [4][128]
-    static constexpr uint32_t EV = RED + 2048;   // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
-    static constexpr uint32_t INV = EV + 1536;   // f32 [128]: 1/|row| of k (0..63) and q (64..127)
-    static constexpr uint32_t BARS = INV + 512;  // 3 x u64
-    static constexpr uint32_t TMEM_SLOT = BARS + 24;
+    static constexpr uint32_t XS = OP_A3;        // f32 [3][16][16] block products (Tb rows, before Tb)
+    static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [4][128] gate partial sums (Tb rows, gate phase)
+    static constexpr uint32_t EV = 65536;        // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
+    static constexpr uint32_t BETA = EV + 1536;  // f32 [64]
+    static constexpr uint32_t INV = BETA + 256;  // f32 [128]: 1/|row| of k (0..63) and q (64..127)
+    static constexpr uint32_t BARS = INV + 512;  // 2 x u64: q/k loaded, mma
+    static constexpr uint32_t TMEM_SLOT = BARS + 16;
     static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
-static_assert(2 * (PrepSmem::ALLOC + 1024) <= 233472, "two prep CTAs must fit on one SM");
+static_assert(PrepSmem::XS + 3072 <= PrepSmem::RED && PrepSmem::RED + 2048 <= PrepSmem::OP_A3 + 8192,
+              "scratch inside the Tb rows");
+static_assert(3 * (PrepSmem::ALLOC + 1024) <= 233472, "three prep CTAs must fit on one SM");
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(NT, 3)
     kda_chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_la, const PrefillArgs p) {
+                          const PrefillArgs p) {
     using L = PrepSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -227,25 +234,26 @@ __global__ void __launch_bounds__(NT, 2)
     const int64_t t0 = static_cast<int64_t>(p.cu_seqlens[seq]) + static_cast<int64_t>(j - co[seq]) * C;
     const int64_t rem = p.cu_seqlens[seq + 1] - t0;
     const int Lc = static_cast<int>(rem < C ? rem : C);
+    uint8_t* const blob = p.blobs + (static_cast<size_t>(j) * H + h) * kPrefillBlobBytes;
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);  // 0: log_alpha, 1: q/k, 2: mma
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);  // 0: q/k, 1: mma
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
     float* ev = reinterpret_cast<float*>(sm + L::EV);
     float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bars[0], C * D * 4);
-        tma_load_3d(sm + L::LA, &tm_la, &bars[0], 0, h, static_cast<int32_t>(t0));
-        mbar_arrive_expect_tx(&bars[1], 4 * 8192);
+        mbar_arrive_expect_tx(&bars[0], 4 * 8192);
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
-            tma_load_3d(sm + L::OP_A + kh * 16384, &tm_k, &bars[1], 64 * kh, h, static_cast<int32_t>(t0));
-            tma_load_3d(sm + L::OP_A + kh * 16384 + 8192, &tm_q, &bars[1], 64 * kh, h, static_cast<int32_t>(t0));
+            tma_load_3d(sm + L::OP_A + kh * 16384, &tm_k, &bars[0], 64 * kh, h, static_cast<int32_t>(t0));
+            tma_load_3d(sm + L::OP_A + kh * 16384 + 8192, &tm_q, &bars[0], 64 * kh, h, static_cast<int32_t>(t0));
         }
     }
+    // log_alpha rows of this thread, in flight while q and k land
+    float g0[16], g1[16];
+    gate_load(p.log_alpha + (t0 * H + h) * D, H * D, Lc, tid, g0, g1);
     float beta_cur = (tid < Lc) ? p.beta[(t0 + tid) * H + h] : 0.f;
     if ((p.fuse_flags & KDA_FUSE_BETA_SIGMOID) && tid < Lc) beta_cur = 1.f / (1.f + expf(-beta_cur));
     if (warp == 0) {
@@ -258,37 +266,46 @@ __global__ void __launch_bounds__(NT, 2)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tq = tmem + tmem_lane(qw);
     bool ok = mbar_wait(&bars[0], 0, kWaitLimit);
-    ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
 
     float* inv = nullptr;
     if (p.fuse_flags & KDA_FUSE_L2NORM_QK) {  // read by gate_chunk after its internal barrier
         inv = reinterpret_cast<float*>(sm + L::INV);
         row_inv_norms(sm + L::OP_A, p.l2_eps, inv, tid);
     }
-    gate_chunk(reinterpret_cast<const float*>(sm + L::LA), sm + L::OP_A, sm + L::OP_KB, Lc,
-               reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev, ev + 128, ev + 256, tid, inv);
+    gate_chunk(g0, g1, sm + L::OP_A, sm + L::OP_KB, Lc, reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur,
+               ev, ev + 128, ev + 256, tid, inv);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     const uint32_t a_base = smem_u32(sm + L::OP_A), kb_base = smem_u32(sm + L::OP_KB);
     const uint32_t a3_base = smem_u32(sm + L::OP_A3);
-    if (tid == 0) {  // D = [Kh; Qh] Kb^T  (128 x 64)
+    if (tid == 0) {
         tc_fence_after();
+        // D = [Kh; Qh] Kb^T  (128 x 64)
         constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
             mma_bf16(tmem, sdesc_sw128(a_base + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
                      sdesc_sw128(kb_base + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), id, s > 0);
-        mma_commit(&bars[2]);
+        mma_commit(&bars[1]);
+        // the parts of the image that are final now: Qh (rows 64..127 of both blocks), Kb, exp vectors
+        bulk_s2g(blob + kBlobA + 8192, sm + L::OP_A + 8192, 8192);
+        bulk_s2g(blob + kBlobA + 16384 + 8192, sm + L::OP_A + 16384 + 8192, 8192);
+        bulk_s2g(blob + kBlobKb, sm + L::OP_KB, 16384);
+        bulk_s2g(blob + kBlobEv, sm + L::EV, 1536);
+        bulk_commit();
     }
-    ok = mbar_wait(&bars[2], 0, kWaitLimit) && ok;
+    ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
     tc_fence_after();
-    float* Nf = reinterpret_cast<float*>(sm + L::INV_N);
-    float* Tf = reinterpret_cast<float*>(sm + L::INV_T);
+    float* Nf = reinterpret_cast<float*>(sm + L::OP_KB);
+    const Rows64 Tf{reinterpret_cast<float*>(sm + L::T_LO), reinterpret_cast<float*>(sm + L::T_HI)};
     {
         float a[32];
         tmem_ld32(tq + 32 * hw, a);
         tmem_ld_wait();
+        if (tid == 0) bulk_wait_read();  // Qh and Kb have been read: their space becomes scratch
+        tc_fence_before();
+        __syncthreads();
         if (qw < 2) {
             const int r = 32 * qw + lane;
             store_n_row(Nf, r, hw, beta_s[r], a);
@@ -297,9 +314,8 @@ __global__ void __launch_bounds__(NT, 2)
             store_m_row(sm + L::OP_A3, 64 + rr, rr, hw, a);
         }
     }
-    tc_fence_before();
     __syncthreads();
-    lower_inverse(Nf, Tf, reinterpret_cast<float*>(sm + L::XS), tid);
+    lower_inverse(rows64(Nf), Tf, reinterpret_cast<float*>(sm + L::XS), tid);
     store_tb(sm + L::OP_A3, Tf, beta_s, tid);
     fence_async_smem();
     tc_fence_before();
@@ -311,9 +327,9 @@ __global__ void __launch_bounds__(NT, 2)
         for (int s = 0; s < 4; ++s)
             mma_bf16(tmem, sdesc_sw128(a3_base + s * 32, 16, 1024), sdesc_sw128(a_base + s * 2048, 16384, 1024), id,
                      s > 0);
-        mma_commit(&bars[2]);
+        mma_commit(&bars[1]);
     }
-    ok = mbar_wait(&bars[2], 1, kWaitLimit) && ok;
+    ok = mbar_wait(&bars[1], 1, kWaitLimit) && ok;
     tc_fence_after();
     if (qw < 2) {  // -W -> rows 0..63 of OP_A
         const int r = 32 * qw + lane;
@@ -334,11 +350,9 @@ __global__ void __launch_bounds__(NT, 2)
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        uint8_t* blob = p.blobs + (static_cast<size_t>(j) * H + h) * kPrefillBlobBytes;
-        bulk_s2g(blob + kBlobA, sm + L::OP_A, 32768);
-        bulk_s2g(blob + kBlobKb, sm + L::OP_KB, 16384);
+        bulk_s2g(blob + kBlobA, sm + L::OP_A, 8192);                   // -W, block 0
+        bulk_s2g(blob + kBlobA + 16384, sm + L::OP_A + 16384, 8192);   // -W, block 1
         bulk_s2g(blob + kBlobTb, sm + L::OP_A3, 16384);  // Tb and M, adjacent in both layouts
-        bulk_s2g(blob + kBlobEv, sm + L::EV, 1536);
         bulk_commit();
         bulk_wait_read();  // shared memory may go once the copies have read it
     }
@@ -732,15 +746,21 @@ __global__ void __launch_bounds__(NTS, 1)
     if (OG) cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
 }
 
+// Sets one function attribute on first use per device.
 template <typename K>
-cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
+cudaError_t set_attr_once(K kernel, cudaFuncAttribute attr, int value, int* configured) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    err = cudaFuncSetAttribute(kernel, attr, value);
     if (err == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
     return err;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
+    return set_attr_once(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes), configured);
 }
 
 }  // namespace
@@ -753,23 +773,27 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_la,
-                              const PrefillArgs& a, int64_t units, cudaStream_t stream) {
+cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units,
+                              cudaStream_t stream) {
     static int cfg_prep[64];
     cudaError_t err = set_smem(kda_chunk_prep_kernel, PrepSmem::ALLOC, cfg_prep);
     if (err != cudaSuccess) return err;
+    static int carveout_prep[64];  // all of the unified L1 as shared memory: three CTAs per SM
+    err = set_attr_once(kda_chunk_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                        cudaSharedmemCarveoutMaxShared, carveout_prep);
+    if (err != cudaSuccess) return err;
     const long long prep_ctas = static_cast<long long>(units) * a.H;
     if (prep_ctas > 0) {
-        kda_chunk_prep_kernel<<<static_cast<unsigned>(prep_ctas), NT, PrepSmem::ALLOC, stream>>>(tm_q, tm_k, tm_la, a);
+        kda_chunk_prep_kernel<<<static_cast<unsigned>(prep_ctas), NT, PrepSmem::ALLOC, stream>>>(tm_q, tm_k, a);
         err = cudaGetLastError();
     }
     return err;
 }
 
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap& tm_la, const CUtensorMap* tm_g, const PrefillArgs& a,
+                                 const CUtensorMap* tm_g, const PrefillArgs& a,
                                  int64_t max_chunks, bool out_f32, cudaStream_t stream) {
-    const cudaError_t err = launch_chunk_prep(tm_q, tm_k, tm_la, a, max_chunks, stream);
+    const cudaError_t err = launch_chunk_prep(tm_q, tm_k, a, max_chunks, stream);
     if (err != cudaSuccess) return err;
     return launch_chunk_scan(tm_v, tm_g, a, out_f32, stream);
 }
