@@ -71,7 +71,7 @@ int sm_count() {
 // first copies), which bounds the piece count.
 constexpr int64_t kScanPieceChunks = 48;  // smallest scan piece (chunks per sequence); each piece costs a few us
 constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
-constexpr double kPrepLag = 0.25;          // lead of pass 1, as a fraction of the chunks scanned after piece 0
+constexpr double kPrepLag = 0.1;           // lead of pass 1, as a fraction of the chunks scanned after piece 0
 
 struct PieceStreams {
     std::mutex mu;  // one call at a time enqueues record/wait pairs on these

@@ -98,20 +98,6 @@ __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) { re
 //   BK: B(k, n) = B[k * ldb + n]     BN: B(k, n) = B[n * ldb + k]
 enum { AR = 0, AC = 1, BK = 0, BN = 1 };
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 template <int NT, int AM, int BM>
 __device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int lda, const float* B, int ldb, int K,
                                       int r0, int c0, int lane) {

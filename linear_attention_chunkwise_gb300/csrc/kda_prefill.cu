@@ -63,7 +63,7 @@ struct Smem {
     static constexpr uint32_t INV_T = OP_SM + 16384;      // f32 [64][64]
     static constexpr uint32_t OP_U = OP_SM + 32768;       // [2 blk][64 rows][128 B]: U
     static constexpr uint32_t SMALL = OP_U + 16384;
-    static constexpr uint32_t XS = SMALL;                 // f32 [3][16][16] inverse scratch
+    static constexpr uint32_t XS = SMALL;                 // f32 [6][16][8] inverse scratch
     static constexpr uint32_t BETA = XS + 3 * 256 * 4;    // f32 [64]
     static constexpr uint32_t RED = BETA + 64 * 4;        // f32 [4][128] cumsum partials
     static constexpr uint32_t EGM = RED + 4 * 128 * 4;    // f32 [128] exp(gm)
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_before();
             __syncthreads();
             // ---- T = (I + N)^-1;  Tb = T Diag(beta) -> rows 0..63 of OP_A3 ----
-            lower_inverse(rows64(Nf), rows64(Tf), Xs, tid);
+            lower_inverse_tc(rows64(Nf), rows64(Tf), Xs, tid);
             store_tb(sm + L::OP_A3, rows64(Tf), beta_s, tid);
             fence_async_smem();
             tc_fence_before();

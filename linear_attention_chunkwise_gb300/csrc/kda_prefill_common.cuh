@@ -231,7 +231,9 @@ __device__ __forceinline__ void store_tb(uint8_t* tile, const Rows64& Tf, const 
 // T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
 // diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
 // for block distance d = R - I = 1, 2, 3.  All NT threads; ends synchronised.
-__device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
+// Diagonal 16 x 16 blocks of T = (I + N)^-1 by forward substitution (warps 0..3, one column per
+// lane of the first half-warp).  No barrier inside.
+__device__ __forceinline__ void lower_inverse_diag(const Rows64& Nf, const Rows64& Tf, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
         const int B = warp, j = lane;
@@ -259,6 +261,13 @@ __device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf
 #pragma unroll
         for (int r = 0; r < 16; ++r) m1(Tf, 16 * B + r, 16 * B + j) = t[r];
     }
+}
+
+// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
+// diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
+// for block distance d = R - I = 1, 2, 3, in fp32.  All NT threads; ends synchronised.
+__device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
+    lower_inverse_diag(Nf, Tf, tid);
     __syncthreads();
     const int I = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
 #pragma unroll 1
@@ -294,6 +303,57 @@ __device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf
             }
             m4(Tf, 16 * R + r, 4 * I + cq) = make_float4(-(acc0.x + acc1.x), -(acc0.y + acc1.y),
                                                          -(acc0.z + acc1.z), -(acc0.w + acc1.w));
+        }
+        __syncthreads();
+    }
+}
+
+// The same inverse with the off-diagonal block products on the tensor cores: per level d,
+//   X = sum_{J=I}^{R-1} N_RJ T_JI,  T_RI = -T_RR X   (R = I + d)
+// as tf32 mma.sync products with fp32 accumulation, one warp per 16 x 8 column tile of T_RI (2 (4 - d)
+// warps), X staged through the warp's own 16 x 8 slot of Xs (f32 [6][16][8]).  Three block
+// barriers instead of six, and a fraction of the instructions of the CUDA-core products; the
+// operands are rounded to tf32 (2^-11), below the bf16 rounding Tb takes afterwards.  Needs NT >= 192
+// threads; ends synchronised.
+__device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
+    lower_inverse_diag(Nf, Tf, tid);
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    float* xs = Xs + warp * 128;  // [16][8]
+#pragma unroll 1
+    for (int d = 1; d <= 3; ++d) {
+        if (warp < 2 * (4 - d)) {
+            const int I = warp >> 1, R = I + d, n0 = 16 * I + 8 * (warp & 1);
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int J = I; J < R; ++J) {
+#pragma unroll
+                for (int kk = 0; kk < 16; kk += 8) {
+                    const int k0 = 16 * J + kk;
+                    const uint32_t a[4] = {to_tf32(m1(Nf, 16 * R + g, k0 + t)), to_tf32(m1(Nf, 16 * R + g + 8, k0 + t)),
+                                           to_tf32(m1(Nf, 16 * R + g, k0 + t + 4)),
+                                           to_tf32(m1(Nf, 16 * R + g + 8, k0 + t + 4))};
+                    mma_tf32(x, a, to_tf32(m1(Tf, k0 + t, n0 + g)), to_tf32(m1(Tf, k0 + t + 4, n0 + g)));
+                }
+            }
+            xs[g * 8 + 2 * t] = x[0];
+            xs[g * 8 + 2 * t + 1] = x[1];
+            xs[(g + 8) * 8 + 2 * t] = x[2];
+            xs[(g + 8) * 8 + 2 * t + 1] = x[3];
+            __syncwarp();
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 16; kk += 8) {
+                const int k0 = 16 * R + kk;
+                const uint32_t a[4] = {to_tf32(m1(Tf, 16 * R + g, k0 + t)), to_tf32(m1(Tf, 16 * R + g + 8, k0 + t)),
+                                       to_tf32(m1(Tf, 16 * R + g, k0 + t + 4)),
+                                       to_tf32(m1(Tf, 16 * R + g + 8, k0 + t + 4))};
+                mma_tf32(y, a, to_tf32(xs[(kk + t) * 8 + g]), to_tf32(xs[(kk + t + 4) * 8 + g]));
+            }
+            // columns n0 + 2t, +1 share one swizzled float4 group: one 8-byte store per row
+            *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g, n0 + 2 * t)) = make_float2(-y[0], -y[1]);
+            *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g + 8, n0 + 2 * t)) = make_float2(-y[2], -y[3]);
         }
         __syncthreads();
     }

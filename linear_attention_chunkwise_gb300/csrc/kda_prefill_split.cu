@@ -187,7 +187,7 @@ struct PrepSmem {
     static constexpr uint32_t T_HI = OP_A + 16384 + 8192;   // f32 rows 32..63 of T (blk 1's Qh rows)
     static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb, then f32 [64][64] N
     static constexpr uint32_t OP_A3 = 49152;     // [Tb (64 rows) | M (64 rows)] x 128 B
-    static constexpr uint32_t XS = OP_A3;        // f32 [3][16][16] block products (Tb rows, before Tb)
+    static constexpr uint32_t XS = OP_A3;        // f32 [6][16][8] block products (Tb rows, before Tb)
     static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [4][128] gate partial sums (Tb rows, gate phase)
     static constexpr uint32_t EV = 65536;        // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
     static constexpr uint32_t BETA = EV + 1536;  // f32 [64]
@@ -260,12 +260,15 @@ __global__ void __launch_bounds__(NT, 3)
         tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
     }
+    // Only thread 0 waits on each mbarrier; the others sleep in the block barrier that follows
+    // (a spinning wait would take issue slots from the other CTAs on the SM).
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait(&bars[0], 0, kWaitLimit);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tq = tmem + tmem_lane(qw);
-    bool ok = mbar_wait(&bars[0], 0, kWaitLimit);
 
     float* inv = nullptr;
     if (p.fuse_flags & KDA_FUSE_L2NORM_QK) {  // read by gate_chunk after its internal barrier
@@ -295,7 +298,11 @@ __global__ void __launch_bounds__(NT, 3)
         bulk_s2g(blob + kBlobEv, sm + L::EV, 1536);
         bulk_commit();
     }
-    ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
+    if (tid == 0) {
+        ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
+        bulk_wait_read();  // Qh and Kb have been read: their space becomes scratch
+    }
+    __syncthreads();
     tc_fence_after();
     float* Nf = reinterpret_cast<float*>(sm + L::OP_KB);
     const Rows64 Tf{reinterpret_cast<float*>(sm + L::T_LO), reinterpret_cast<float*>(sm + L::T_HI)};
@@ -303,9 +310,6 @@ __global__ void __launch_bounds__(NT, 3)
         float a[32];
         tmem_ld32(tq + 32 * hw, a);
         tmem_ld_wait();
-        if (tid == 0) bulk_wait_read();  // Qh and Kb have been read: their space becomes scratch
-        tc_fence_before();
-        __syncthreads();
         if (qw < 2) {
             const int r = 32 * qw + lane;
             store_n_row(Nf, r, hw, beta_s[r], a);
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(NT, 3)
         }
     }
     __syncthreads();
-    lower_inverse(rows64(Nf), Tf, reinterpret_cast<float*>(sm + L::XS), tid);
+    lower_inverse_tc(rows64(Nf), Tf, reinterpret_cast<float*>(sm + L::XS), tid);
     store_tb(sm + L::OP_A3, Tf, beta_s, tid);
     fence_async_smem();
     tc_fence_before();
@@ -329,7 +333,8 @@ __global__ void __launch_bounds__(NT, 3)
                      s > 0);
         mma_commit(&bars[1]);
     }
-    ok = mbar_wait(&bars[1], 1, kWaitLimit) && ok;
+    if (tid == 0) ok = mbar_wait(&bars[1], 1, kWaitLimit) && ok;
+    __syncthreads();
     tc_fence_after();
     if (qw < 2) {  // -W -> rows 0..63 of OP_A
         const int r = 32 * qw + lane;

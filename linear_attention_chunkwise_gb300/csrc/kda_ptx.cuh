@@ -189,4 +189,22 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     return __bfloat1622float2(h);
 }
 
+// ------------------------------------------------------- warp-level tf32 ----
+// fp32 -> tf32 with round-to-nearest (ties away), as the tf32 mma operands.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// d += a b for one 16 x 8 tile (m16n8k8, tf32 operands, fp32 accumulate).  With g = lane / 4 and
+// t = lane % 4: a = A(g, t), A(g + 8, t), A(g, t + 4), A(g + 8, t + 4); b0 = B(t, g), b1 = B(t + 4, g);
+// d = D(g, 2t), D(g, 2t + 1), D(g + 8, 2t), D(g + 8, 2t + 1).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 }  // namespace kda
