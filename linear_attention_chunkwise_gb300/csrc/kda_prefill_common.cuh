@@ -168,6 +168,86 @@ __device__ __forceinline__ void gate_chunk(float (&g0)[16], float (&g1)[16], uin
     }
 }
 
+// The gate phase with 4 channels x 8 rows per thread: thread tid handles channels 4 (tid % 32) .. +3
+// of rows 8 (tid / 32) .. +7, so a warp covers one 8-row group across all 128 channels (whole
+// 512-byte rows of log_alpha per load, conflict-free 8-byte tile accesses, and a quarter of the
+// address arithmetic per channel of gate_chunk).  Same results as gate_chunk.
+__device__ __forceinline__ void gate_load4(const float* la, int stride, int Lc, int tid, float4 (&g)[8]) {
+    const int c4 = tid & 31, rg = tid >> 5;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
+        g[i] = r < Lc ? *reinterpret_cast<const float4*>(la + static_cast<size_t>(r) * stride + 4 * c4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+__device__ __forceinline__ float4 add4(const float4& a, const float4& b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
+    return make_uint2(pack_bf16(a, b), pack_bf16(c, d));
+}
+
+//   g    : this thread's log_alpha rows from gate_load4 (overwritten)
+//   opa, opkb, Lc, beta_s, beta_cur, egm/egc/egcm, inv_norm: as gate_chunk; red: f32 [8][128] scratch
+__device__ __forceinline__ void gate_chunk4(float4 (&g)[8], uint8_t* opa, uint8_t* opkb, int Lc, float* red,
+                                            float* beta_s, float beta_cur, float* egm, float* egc, float* egcm,
+                                            int tid, const float* inv_norm = nullptr) {
+    const int c4 = tid & 31, rg = tid >> 5;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        acc = add4(acc, g[i]);
+        g[i] = acc;
+    }
+    reinterpret_cast<float4*>(red + rg * D)[c4] = acc;
+    if (tid < C) beta_s[tid] = (tid < Lc) ? beta_cur : 0.f;
+    __syncthreads();
+    float4 off = make_float4(0.f, 0.f, 0.f, 0.f), gm = off, gc = off;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 pq = reinterpret_cast<const float4*>(red + q * D)[c4];
+        if (q < rg) off = add4(off, pq);
+        if (q < 4) gm = add4(gm, pq);  // g at row 31, the last row of group 3
+        gc = add4(gc, pq);
+    }
+    if (rg == 0) {
+        *reinterpret_cast<float4*>(egm + 4 * c4) = make_float4(expf(gm.x), expf(gm.y), expf(gm.z), expf(gm.w));
+        *reinterpret_cast<float4*>(egc + 4 * c4) = make_float4(expf(gc.x), expf(gc.y), expf(gc.z), expf(gc.w));
+        *reinterpret_cast<float4*>(egcm + 4 * c4) =
+            make_float4(expf(gc.x - gm.x), expf(gc.y - gm.y), expf(gc.z - gm.z), expf(gc.w - gm.w));
+    }
+    const float4 cc = make_float4((off.x - gm.x) * kLog2e, (off.y - gm.y) * kLog2e, (off.z - gm.z) * kLog2e,
+                                  (off.w - gm.w) * kLog2e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
+        const float x0 = fmaf(g[i].x, kLog2e, cc.x), x1 = fmaf(g[i].y, kLog2e, cc.y);
+        const float x2 = fmaf(g[i].z, kLog2e, cc.z), x3 = fmaf(g[i].w, kLog2e, cc.w);
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1), e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+        const float f0 = ex2_approx(-x0), f1 = ex2_approx(-x1), f2 = ex2_approx(-x2), f3 = ex2_approx(-x3);
+        const uint32_t koff = sw128_off(r, 4 * c4, 16384);
+        const uint32_t qoff = sw128_off(64 + r, 4 * c4, 16384);
+        float2 k01 = make_float2(0.f, 0.f), k23 = k01, q01 = k01, q23 = k01;
+        if (r < Lc) {
+            const uint2 kw = *reinterpret_cast<const uint2*>(opa + koff);
+            const uint2 qw = *reinterpret_cast<const uint2*>(opa + qoff);
+            k01 = unpack_bf16(kw.x); k23 = unpack_bf16(kw.y);
+            q01 = unpack_bf16(qw.x); q23 = unpack_bf16(qw.y);
+            if (inv_norm) {  // fused L2 normalisation of k and q rows
+                const float ik = inv_norm[r], iq = inv_norm[64 + r];
+                k01.x *= ik; k01.y *= ik; k23.x *= ik; k23.y *= ik;
+                q01.x *= iq; q01.y *= iq; q23.x *= iq; q23.y *= iq;
+            }
+        }
+        *reinterpret_cast<uint2*>(opa + koff) = pack4(k01.x * e0, k01.y * e1, k23.x * e2, k23.y * e3);
+        *reinterpret_cast<uint2*>(opa + qoff) = pack4(q01.x * e0, q01.y * e1, q23.x * e2, q23.y * e3);
+        *reinterpret_cast<uint2*>(opkb + sw128_off(r, 4 * c4, 8192)) =
+            pack4(k01.x * f0, k01.y * f1, k23.x * f2, k23.y * f3);
+    }
+}
+
 // 1 / sqrt(|x|^2 + eps) of the 128 rows of an operand tile [2 blk][128 rows][128 B]
 // (rows 0..63 k, 64..127 q) into inv[128]; all NT threads, no barrier inside.
 __device__ __forceinline__ void row_inv_norms(const uint8_t* opa, float eps, float* inv, int tid) {

@@ -188,7 +188,7 @@ struct PrepSmem {
     static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb, then f32 [64][64] N
     static constexpr uint32_t OP_A3 = 49152;     // [Tb (64 rows) | M (64 rows)] x 128 B
     static constexpr uint32_t XS = OP_A3;        // f32 [6][16][8] block products (Tb rows, before Tb)
-    static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [4][128] gate partial sums (Tb rows, gate phase)
+    static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [8][128] gate partial sums (Tb rows, gate phase)
     static constexpr uint32_t EV = 65536;        // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
     static constexpr uint32_t BETA = EV + 1536;  // f32 [64]
     static constexpr uint32_t INV = BETA + 256;  // f32 [128]: 1/|row| of k (0..63) and q (64..127)
@@ -197,7 +197,7 @@ struct PrepSmem {
     static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
-static_assert(PrepSmem::XS + 3072 <= PrepSmem::RED && PrepSmem::RED + 2048 <= PrepSmem::OP_A3 + 8192,
+static_assert(PrepSmem::XS + 3072 <= PrepSmem::RED && PrepSmem::RED + 4096 <= PrepSmem::OP_A3 + 8192,
               "scratch inside the Tb rows");
 static_assert(3 * (PrepSmem::ALLOC + 1024) <= 233472, "three prep CTAs must fit on one SM");
 
@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(NT, 3)
         }
     }
     // log_alpha rows of this thread, in flight while q and k land
-    float g0[16], g1[16];
-    gate_load(p.log_alpha + (t0 * H + h) * D, H * D, Lc, tid, g0, g1);
+    float4 g[8];
+    gate_load4(p.log_alpha + (t0 * H + h) * D, H * D, Lc, tid, g);
     float beta_cur = (tid < Lc) ? p.beta[(t0 + tid) * H + h] : 0.f;
     if ((p.fuse_flags & KDA_FUSE_BETA_SIGMOID) && tid < Lc) beta_cur = 1.f / (1.f + expf(-beta_cur));
     if (warp == 0) {
@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(NT, 3)
         inv = reinterpret_cast<float*>(sm + L::INV);
         row_inv_norms(sm + L::OP_A, p.l2_eps, inv, tid);
     }
-    gate_chunk(g0, g1, sm + L::OP_A, sm + L::OP_KB, Lc, reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur,
-               ev, ev + 128, ev + 256, tid, inv);
+    gate_chunk4(g, sm + L::OP_A, sm + L::OP_KB, Lc, reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev,
+                ev + 128, ev + 256, tid, inv);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
