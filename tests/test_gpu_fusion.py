@@ -231,3 +231,32 @@ def test_decode_multi_fused(dtype):
     assert int(status.item()) == 0
     assert rell2(host(o), o_ref) < TOL
     assert rell2(host(d.S), S_ref) < 1e-4
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_multi_fused_prologue_only(dtype):
+    """Prologue fusions without the output gate, with the per-step states."""
+    N, H, T = 6, 3, 10  # two token batches in the kernel (8 + 2)
+    d = synth.decode_inputs(N, H, T, dtype=dtype, seed=630, device="cuda", num_slots=9, permute_slots=True)
+    g = torch.Generator(device="cuda").manual_seed(631)
+    scale = lambda x: (x.float() * (0.3 + 2.7 * torch.rand(x.shape[:-1] + (1,), generator=g, device="cuda"))).to(dtype)
+    q, k = scale(d.q), scale(d.k)
+    beta = torch.randn(d.beta.shape, generator=g, device="cuda")
+    tm = lambda x: x.transpose(0, 1).contiguous()  # [T, N, ...] -> [N, T, ...]
+    S_ref = host(d.S).astype(np.float64)
+    idx = d.state_indices.cpu().numpy()
+    o_ref = []
+    for t in range(T):
+        qq, kk = oracle.l2_normalize(host(q[t]), L2_EPS), oracle.l2_normalize(host(k[t]), L2_EPS)
+        o_ref.append(oracle.kda_decode_step(qq, kk, host(d.v[t]), host(d.log_alpha[t]),
+                                            oracle.sigmoid(host(beta[t])), S_ref, idx))
+    o_ref = np.stack(o_ref, axis=1)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS)
+    S_steps = torch.empty((N, T, H, 128, 128), dtype=torch.float32, device="cuda")
+    o, steps = kda.kda_decode_multi_ex(tm(q), tm(k), tm(d.v), tm(d.log_alpha), tm(beta), d.S, d.state_indices,
+                                       fusion=fz, S_steps=S_steps, return_steps=True)
+    torch.cuda.synchronize()
+    assert rell2(host(o), o_ref) < TOL
+    assert rell2(host(d.S), S_ref) < 1e-4
+    # the last step's state is the state written back
+    assert torch.equal(steps[:, T - 1], d.S[d.state_indices.long()])
