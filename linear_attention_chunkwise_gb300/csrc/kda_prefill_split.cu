@@ -397,6 +397,52 @@ static_assert(ScanSmem::ALLOC_OG <= 232448, "scan shared memory (output gate) ov
 static_assert(ScanSmem::ALLOC <= 232448, "scan shared memory over the per-CTA limit");
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 
+// Store a warp's 32 x PC block of the state (lane = block row, PC consecutive columns) to global
+// memory, `dst` = the block's first row, rows D floats apart.  The block is transposed through the
+// warp's own 32 x PC floats of shared memory (16-byte chunks xor-swizzled by the row), so each store
+// instruction writes whole PC * 4-byte row segments of 32 / (PC / 4) rows instead of 16 bytes in each
+// of 32 rows.
+template <int PC>
+__device__ __forceinline__ void store_state_rows(float* dst, const float (&S)[PC], float* stage, int lane) {
+    constexpr int CH = PC / 4;    // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;  // rows per store instruction
+#pragma unroll
+    for (int j = 0; j < CH; ++j)
+        *reinterpret_cast<float4*>(stage + lane * PC + 4 * (j ^ (lane & (CH - 1)))) =
+            make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+    __syncwarp();
+    const int rr = lane / CH, j = lane % CH;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int r = i * RPI + rr;
+        *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * D + 4 * j) =
+            *reinterpret_cast<const float4*>(stage + r * PC + 4 * (j ^ (r & (CH - 1))));
+    }
+    __syncwarp();
+}
+
+// The reverse of store_state_rows: whole row segments from global memory, transposed through the
+// warp's shared memory into lane = block row, PC consecutive columns.
+template <int PC>
+__device__ __forceinline__ void load_state_rows(const float* src, float (&S)[PC], float* stage, int lane) {
+    constexpr int CH = PC / 4;
+    constexpr int RPI = 32 / CH;
+    const int rr = lane / CH, j = lane % CH;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int r = i * RPI + rr;
+        *reinterpret_cast<float4*>(stage + r * PC + 4 * (j ^ (r & (CH - 1)))) =
+            *reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D + 4 * j);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int jj = 0; jj < CH; ++jj) {
+        const float4 t = *reinterpret_cast<const float4*>(stage + lane * PC + 4 * (jj ^ (lane & (CH - 1))));
+        S[4 * jj] = t.x; S[4 * jj + 1] = t.y; S[4 * jj + 2] = t.z; S[4 * jj + 3] = t.w;
+    }
+    __syncwarp();
+}
+
 // OG (fused output gate): the two dv slices of a (sequence, head) run as one
 // 2-CTA cluster and swap per-row sums of o^2 through distributed shared
 // memory, so each writes y = o / sqrt(mean o^2 + eps) * weight * gate.
@@ -463,12 +509,9 @@ __global__ void __launch_bounds__(NTS, 1)
     const int rho = 32 * qw + lane;
     float S[PC];
     const size_t srow = ((static_cast<size_t>(seq) * H + h) * D + rho) * D + j0 + PC * cq;
-    if (S_in) {
-#pragma unroll
-        for (int j = 0; j < PC; j += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(S_in + srow + j);
-            S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
-        }
+    if (S_in) {  // staged in operand set 0, which the first copies fill only after the block barrier below
+        load_state_rows<PC>(S_in + ((static_cast<size_t>(seq) * H + h) * D + 32 * qw) * D + j0 + PC * cq, S,
+                            reinterpret_cast<float*>(sm) + warp * 32 * PC, lane);
     } else {
 #pragma unroll
         for (int j = 0; j < PC; ++j) S[j] = 0.f;
@@ -683,12 +726,10 @@ __global__ void __launch_bounds__(NTS, 1)
         {  // state snapshots at the end of this chunk (positions are sequence-relative)
             const int64_t done = min(static_cast<int64_t>(cb + c + 1) * C, seq_len);
             while (next_snap <= done) {
-                if (next_snap == done) {
-                    float* dst = p.S_snap + ((static_cast<size_t>(si) * H + h) * D + rho) * D + j0 + PC * cq;
-#pragma unroll
-                    for (int j = 0; j < PC; j += 4)
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-                }
+                if (next_snap == done)  // staged in this chunk's operand set: its MMAs have completed
+                    store_state_rows<PC>(
+                        p.S_snap + ((static_cast<size_t>(si) * H + h) * D + 32 * qw) * D + j0 + PC * cq, S,
+                        reinterpret_cast<float*>(set) + warp * 32 * PC, lane);
                 ++si;
                 next_snap = si < se ? p.snap_pos[si] : INT_MAX;
             }
@@ -740,11 +781,9 @@ __global__ void __launch_bounds__(NTS, 1)
         mma_commit(&bars[4]);
         (void)mbar_wait(&bars[4], 0, kWaitLimit);
     }
-    if (p.S_final && ok) {
-#pragma unroll
-        for (int j = 0; j < PC; j += 4)
-            *reinterpret_cast<float4*>(p.S_final + srow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
+    if (p.S_final && ok)  // staged in operand set 0: every copy into it has been consumed
+        store_state_rows<PC>(p.S_final + ((static_cast<size_t>(seq) * H + h) * D + 32 * qw) * D + j0 + PC * cq, S,
+                             reinterpret_cast<float*>(sm) + warp * 32 * PC, lane);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
