@@ -434,10 +434,14 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
             for (int e = 0; e < 4; ++e) {
                 const int r = frow(16 * warp, lane, e), col = fcol(0, lane, j, e);
                 XS[r * LDS + col] = X[j][e];
-                xo[r * D + c0 + col] = X[j][e];
             }
         cp_wait<1>();  // this chunk's stage has landed
         __syncthreads();
+        // the adjoint of this chunk's end state, as whole 128-byte row segments of the slice
+        for (int e = tid; e < D * (NCS / 4); e += BT) {
+            const int r = e / (NCS / 4), c4 = 4 * (e % (NCS / 4));
+            *reinterpret_cast<float4*>(xo + r * D + c0 + c4) = *reinterpret_cast<const float4*>(XS + r * LDS + c4);
+        }
         {   // dY = dY0 - Wbc X  (64 x 32: warp rows 16 (warp & 3), columns 16 (warp >> 2))
             const int r0 = 16 * (warp & 3), cc = 16 * (warp >> 2);
             float acc[2][4];
@@ -448,12 +452,16 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = frow(r0, lane, e), col = fcol(cc, lane, j, e);
-                    const float dy = st[L::Y0 + r * LDS + col] - acc[j][e];
-                    DY[r * LDS + col] = dy;
-                    if (r < Lr) a.dv[(static_cast<size_t>(t0 + r) * H + h) * D + c0 + col] = -dy;
+                    DY[r * LDS + col] = st[L::Y0 + r * LDS + col] - acc[j][e];
                 }
         }
         __syncthreads();
+        for (int e = tid; e < Lr * (NCS / 4); e += BT) {  // dv = -dY, whole row segments of the slice
+            const int r = e / (NCS / 4), c4 = 4 * (e % (NCS / 4));
+            const float4 dy = *reinterpret_cast<const float4*>(DY + r * LDS + c4);
+            *reinterpret_cast<float4*>(a.dv + (static_cast<size_t>(t0 + r) * H + h) * D + c0 + c4) =
+                make_float4(-dy.x, -dy.y, -dy.z, -dy.w);
+        }
         {   // X <- Diag(e^{gC}) X + P + Khm^T dY
             float acc[4][4];
             zero(acc);
