@@ -88,6 +88,15 @@ template <>
 __device__ __forceinline__ float ld1<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+// two adjacent elements (p even-aligned)
+template <typename T>
+__device__ __forceinline__ float2 ld2(const T* p);
+template <>
+__device__ __forceinline__ float2 ld2<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
+template <>
+__device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
 
 // ---- products on shared tiles ---------------------------------------------------------------
 // Tensor-core products of fp32 shared tiles: operands rounded to tf32 (cvt.rna), fp32 accumulate,
@@ -578,10 +587,11 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_kernel(const BackwardArgs
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
             const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-            T3[r * LDW + i] = acc[j][e];
-            if (r < p.L) a.u_scratch[(static_cast<size_t>(p.t0 + r) * H + h) * D + i] = acc[j][e];
+            const float2 u = make_float2(acc[j][e], acc[j][e + 1]);
+            *reinterpret_cast<float2*>(T3 + r * LDW + i) = u;
+            if (r < p.L) *reinterpret_cast<float2*>(a.u_scratch + (static_cast<size_t>(p.t0 + r) * H + h) * D + i) = u;
         }
     __syncthreads();
     zero(acc);
@@ -726,20 +736,31 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
             const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-            const float gx = T3[r * LDW + i] - T3[(C / 2 - 1) * LDW + i];
-            const float eq = expf(gx), eb = expf(-gx);
-            const float dq = eq * aq[j][e], dka = eb * aka[j][e], dkb = eq * akb[j][e];
-            float dg = 0.f;
+            float dq[2], dk[2], dg[2] = {0.f, 0.f}, dd[2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float gx = T3[r * LDW + i + x] - T3[(C / 2 - 1) * LDW + i + x];
+                const float eq = expf(gx), eb = expf(-gx);
+                const float dka = eb * aka[j][e + x], dkb = eq * akb[j][e + x];
+                dq[x] = eq * aq[j][e + x];
+                dk[x] = dka + dkb;
+                dd[x] = dkb - dka;
+            }
             if (r < p.L) {
                 const size_t o = (static_cast<size_t>(p.t0 + r) * H + h) * D + i;
-                dg = ld1(q + o) * dq + ld1(k + o) * (dkb - dka);
-                if (r == p.L - 1) dg += bnd[i];
-                a.dq[o] = dq;
-                a.dk[o] = dka + dkb;
+                const float2 qv = ld2(q + o), kv = ld2(k + o);
+                dg[0] = qv.x * dq[0] + kv.x * dd[0];
+                dg[1] = qv.y * dq[1] + kv.y * dd[1];
+                if (r == p.L - 1) {
+                    dg[0] += bnd[i];
+                    dg[1] += bnd[i + 1];
+                }
+                *reinterpret_cast<float2*>(a.dq + o) = make_float2(dq[0], dq[1]);
+                *reinterpret_cast<float2*>(a.dk + o) = make_float2(dk[0], dk[1]);
             }
-            T0[r * LDW + i] = dg;
+            *reinterpret_cast<float2*>(T0 + r * LDW + i) = make_float2(dg[0], dg[1]);
         }
     __syncthreads();
     if (tid < D) {  // dlog_alpha = reverse cumulative sum of dg
