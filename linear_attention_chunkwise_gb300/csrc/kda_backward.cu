@@ -325,9 +325,10 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
                 const int i = 64 * half + frow(r0, lane, e), col = fcol(c128, lane, j, e);
-                rec[kRecP + i * D + col] = egm[i] * acc[j][e];
+                *reinterpret_cast<float2*>(rec + kRecP + i * D + col) =
+                    make_float2(egm[i] * acc[j][e], egm[i] * acc[j][e + 1]);
             }
     }
     __syncthreads();
@@ -349,10 +350,11 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 4; e += 2) {
                 const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-                rec[kRecWbc + r * D + i] = acc[j][e] * egcm[i];
-                QH[r * LDW + i] = md[j][e];
+                *reinterpret_cast<float2*>(rec + kRecWbc + r * D + i) =
+                    make_float2(acc[j][e] * egcm[i], acc[j][e + 1] * egcm[i + 1]);
+                *reinterpret_cast<float2*>(QH + r * LDW + i) = make_float2(md[j][e], md[j][e + 1]);
             }
     }
     __syncthreads();
@@ -363,8 +365,9 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                rec[kRecDY0 + frow(r0, lane, e) * D + fcol(c128, lane, j, e)] = -acc[j][e];
+            for (int e = 0; e < 4; e += 2)
+                *reinterpret_cast<float2*>(rec + kRecDY0 + frow(r0, lane, e) * D + fcol(c128, lane, j, e)) =
+                    make_float2(-acc[j][e], -acc[j][e + 1]);
     }
 }
 
