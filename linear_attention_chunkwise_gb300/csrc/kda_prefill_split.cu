@@ -394,6 +394,10 @@ struct ScanSmem {
     static constexpr uint32_t ALLOC_OG = WRMS + 256 + 1024;
 };
 static_assert(ScanSmem::ALLOC_OG <= 232448, "scan shared memory (output gate) over the per-CTA limit");
+// per-warp staging inside a consumed operand set: the state slice (128 rows x 64 fp32 over all warps)
+// fits the [-W; Qh] tile, the output rows (64 rows x 64 columns, at most fp32) the Kb tile
+static_assert(128 * 64 * 4 <= ScanSmem::S_KB - ScanSmem::S_A, "state stage over the [-W; Qh] tile");
+static_assert(64 * 64 * 4 <= ScanSmem::S_A3 - ScanSmem::S_KB, "output stage over the Kb tile");
 static_assert(ScanSmem::ALLOC <= 232448, "scan shared memory over the per-CTA limit");
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 
@@ -439,6 +443,42 @@ __device__ __forceinline__ void load_state_rows(const float* src, float (&S)[PC]
     for (int jj = 0; jj < CH; ++jj) {
         const float4 t = *reinterpret_cast<const float4*>(stage + lane * PC + 4 * (jj ^ (lane & (CH - 1))));
         S[4 * jj] = t.x; S[4 * jj + 1] = t.y; S[4 * jj + 2] = t.z; S[4 * jj + 3] = t.w;
+    }
+    __syncwarp();
+}
+
+// Store a warp's 32 output rows (lane = row, PC consecutive columns as fp32) to `dst` (row 0, rows
+// `row_stride` elements apart; only rows < nrows), converted to OutT, as whole row segments: the
+// packed rows are transposed through the warp's PC * sizeof(OutT) * 32 bytes of shared memory
+// (16-byte chunks xor-swizzled so both passes are conflict-free).
+template <typename OutT, int PC>
+__device__ __forceinline__ void store_out_rows(OutT* dst, int64_t row_stride, int nrows, const float (&a)[PC],
+                                               uint8_t* stage, int lane) {
+    constexpr int RB = PC * static_cast<int>(sizeof(OutT));  // bytes per row
+    constexpr int CH = RB / 16;                               // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;                              // rows per store instruction
+    constexpr int SH = RB >= 128 ? 0 : (RB == 64 ? 1 : 2);    // rows sharing one 128-byte bank line
+    static_assert(CH >= 2 && CH <= 8, "row segment of 32 to 128 bytes");
+    const int key = (lane >> SH) & (CH - 1);
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch) {
+        uint4 pk;
+        if constexpr (sizeof(OutT) == 2) {
+            pk = pack8(a + 8 * ch);
+        } else {
+            pk = make_uint4(__float_as_uint(a[4 * ch]), __float_as_uint(a[4 * ch + 1]), __float_as_uint(a[4 * ch + 2]),
+                            __float_as_uint(a[4 * ch + 3]));
+        }
+        *reinterpret_cast<uint4*>(stage + lane * RB + 16 * (ch ^ key)) = pk;
+    }
+    __syncwarp();
+    const int rr = lane / CH, j = lane % CH;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int r = i * RPI + rr;
+        if (r < nrows)
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(dst + r * row_stride) + 16 * j) =
+                *reinterpret_cast<const uint4*>(stage + r * RB + 16 * (j ^ ((r >> SH) & (CH - 1))));
     }
     __syncwarp();
 }
@@ -759,12 +799,14 @@ __global__ void __launch_bounds__(NTS, 1)
                 float a[PC];
                 tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
                 tmem_ld_wait();
-                if (rr < Lc) {
-                    OutT* dst =
-                        static_cast<OutT*>(p.o) + ((t0 + rr) * H + h) * static_cast<int64_t>(D) + j0 + PC * cq;
-#pragma unroll
-                    for (int ch = 0; ch < PC / 8; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
-                }
+                // staged in this chunk's Kb tile (its MMAs have completed; every load of the set
+                // rewrites it), beside the [-W; Qh] tile the state snapshot may use -- never in the
+                // zero rows of [Tb | 0 | M], which are written once
+                const int row0 = 32 * (qw - 2);
+                store_out_rows<OutT, PC>(
+                    static_cast<OutT*>(p.o) + ((t0 + row0) * H + h) * static_cast<int64_t>(D) + j0 + PC * cq,
+                    static_cast<int64_t>(H) * D, Lc - row0, a, set + L::S_KB + ((qw - 2) + 2 * cq) * (32 * PC * 4),
+                    lane);
             }
         }
         tc_fence_before();
