@@ -384,7 +384,8 @@ struct ScanSmem {
     static constexpr uint32_t ABORT = TMEM_SLOT + 4;
     static constexpr uint32_t OSQ = ABORT + 4;       // f32 [2][64]: sum of o^2 per O row, per column half
     static constexpr uint32_t RX = OSQ + 512;        // f32 [2][64]: the peer CTA's row sums, by chunk parity
-    static constexpr uint32_t TOTAL = RX + 512;
+    static constexpr uint32_t EVBAR = RX + 512;      // 2 x u64: a set's exp vectors landed (by chunk parity)
+    static constexpr uint32_t TOTAL = EVBAR + 16;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
     // fused output gate only: the gate tiles of two chunks (TMA, 128B-swizzled rows of 128 B:
     // one 64-column box for bf16, two 32-column boxes for fp32) and their barriers
@@ -566,6 +567,7 @@ __global__ void __launch_bounds__(NTS, 1)
     }
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
+    uint64_t* evbar = reinterpret_cast<uint64_t*>(sm + L::EVBAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
     volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
     uint64_t* rxbar = reinterpret_cast<uint64_t*>(sm + L::RXBAR);
@@ -573,6 +575,8 @@ __global__ void __launch_bounds__(NTS, 1)
     if (tid == 0) {
         *abort_s = 0;
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&evbar[0], 1);
+        mbar_init(&evbar[1], 1);
         if (OG) {
             mbar_init(&rxbar[0], 1);  // this CTA's arrive.expect_tx + the peer's 64 async stores
             mbar_init(&rxbar[1], 1);
@@ -610,19 +614,21 @@ __global__ void __launch_bounds__(NTS, 1)
         uint8_t* set = sm + (c & 1) * L::SET;
         uint64_t* bar = &bars[c & 1];
         const uint8_t* blob = p.blobs + (static_cast<size_t>(jb + c) * H + h) * kPrefillBlobBytes;
-        mbar_arrive_expect_tx(bar, kLoadBytes);
+        // the exp vectors first, on their own barrier: the state conversion needs only them
+        mbar_arrive_expect_tx(&evbar[c & 1], 1536);
+        bulk_g2s(set + L::S_EV, blob + kBlobEv, 1536, &evbar[c & 1]);
+        mbar_arrive_expect_tx(bar, kLoadBytes - 1536);
         bulk_g2s(set + L::S_A, blob + kBlobA, 32768, bar);
         bulk_g2s(set + L::S_KB, blob + kBlobKb, 16384, bar);
         bulk_g2s(set + L::S_A3, blob + kBlobTb, 8192, bar);
         bulk_g2s(set + L::S_A3 + 16384, blob + kBlobM, 8192, bar);
-        bulk_g2s(set + L::S_EV, blob + kBlobEv, 1536, bar);
         tma_load_3d(set + L::S_V, &tm_v, bar, j0, h, static_cast<int32_t>(t_begin + static_cast<int64_t>(c) * C));
     };
     if (tid == 0) {
         issue_loads(0);
         if (nch > 1) issue_loads(1);
     }
-    uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] in bit i
+    uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] (and evbar[i]) in bit i
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
         if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
         ph ^= 1u;
@@ -685,14 +691,19 @@ __global__ void __launch_bounds__(NTS, 1)
         const float* evs = reinterpret_cast<const float*>(set + L::S_EV);
         const int64_t t0 = t_begin + static_cast<int64_t>(c) * C;
         const int Lc = static_cast<int>(t_end - t0 < C ? t_end - t0 : C);
-        if (!mbar_wait(&bars[b], (ph_load >> b) & 1u, kWaitLimit)) *abort_s = 1;
+        // Every thread waits for the exp vectors only; the state conversion below overlaps the rest
+        // of the copies, which thread 0 waits for before the block barrier (all threads in the last,
+        // ragged chunk, whose v rows past the sequence end they clear).
+        const uint32_t par = (ph_load >> b) & 1u;
         ph_load ^= 1u << b;
         if (Lc < C) {  // rows of v past the sequence end -> 0
+            if (!mbar_wait(&bars[b], par, kWaitLimit)) *abort_s = 1;
             for (int e = tid; e < (C - Lc) * 8; e += NTS) {
                 const int r = Lc + (e >> 3);
                 *reinterpret_cast<uint4*>(set + L::S_V + sw128_chunk(r, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        if (!mbar_wait(&evbar[b], par, kWaitLimit)) *abort_s = 1;
         {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks PC*cq/8 ..)
             const float sc = evs[rho];
 #pragma unroll
@@ -704,6 +715,7 @@ __global__ void __launch_bounds__(NTS, 1)
             }
         }
         fence_async_smem();
+        if (Lc == C && tid == 0 && !mbar_wait(&bars[b], par, kWaitLimit)) *abort_s = 1;
         tc_fence_before();
         __syncthreads();
         if (*abort_s) break;  // a bounded wait expired: every thread sees it after the barrier
