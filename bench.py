@@ -650,6 +650,27 @@ def bench_backward(cx: Ctx, args):
     flops_per_call = 2 * BACKWARD_MACS_PER_CHUNK_HEAD * (-(-T // 64)) * H
     achieved_tf = flops_per_call / (ms_local * 1e-3) / 1e12
     pk = cx.peaks
+    del work
+
+    # the same call through the fused prologue (q, k L2-normalised and beta = sigmoid(logits) inside,
+    # the chain rule through both applied to the gradients): its two elementwise kernels on top
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=1e-6)
+    work = torch.empty(kda.kda_prefill_backward_ex_workspace_bytes(torch.bfloat16, 1, T, H), dtype=torch.uint8,
+                       device=cx.dev)
+
+    def call_fused():
+        kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, None, dSf, fusion=fz,
+                                    grads=grads, workspace=work, stream=cx.stream)
+
+    for _ in range(3):
+        call_fused()
+    ev0, ev1 = cx.events()
+    ev0.record(cx.stream)
+    for _ in range(n):
+        call_fused()
+    ev1.record(cx.stream)
+    cx.stream.synchronize()
+    ms_fused = ev0.elapsed_time(ev1) / n
     del work, grads
     return {
         "workload": "KDA prefill backward B=1 H=32 T=8192 d=128, bf16 q/k/v/grad_o, fp32 gates, S0=0, "
@@ -667,6 +688,8 @@ def bench_backward(cx: Ctx, args):
                    "flops_per_launch": flops_per_call, "dtype": "tf32 (fp32 operands rounded), fp32 accumulate",
                    "peak_source": pk["src"] + " bf16 burst x nominal tf32/bf16 ratio 1.1/2.25"},
         "gpu_launches_per_call": 10,
+        "fused_prologue": {"ms_per_call": round(ms_fused, 3), "gpu_launches_per_call": 12,
+                           "what": "kda_prefill_backward_ex, L2 norm of q, k and sigmoid beta fused"},
         "clocks": clk.summary(),
     }
 
