@@ -6,7 +6,7 @@
 // that the work that does NOT depend on the state runs fully in parallel:
 //
 //   pass 0  chunk table: chunk offsets of every sequence (from cu_seqlens).
-//   pass 1  chunk prep, one CTA per (chunk, head), two CTAs per SM: gates,
+//   pass 1  chunk prep, one CTA per (chunk, head), three CTAs per SM: gates,
 //           Kh/Qh/Kb, MMA [Kh;Qh] Kb^T, the triangular inverse, Tb, M and
 //           MMA W = Tb Kh.  It writes the scan's operands to the workspace as
 //           ready-to-copy images of the swizzled shared-memory tiles:
