@@ -67,8 +67,9 @@ def test_backward_without_final_gradient_and_empty_sequence():
             assert abs(grad[idx] - fd) <= 1e-7 * (1 + abs(fd)), (name, idx)
 
 
-def test_fused_prologue_backward_matches_finite_differences():
-    """kda_prefill_backward_fused (L2 norm of q, k and sigmoid beta before the recurrence) against
+@pytest.mark.parametrize("l2norm_qk,beta_sigmoid", [(True, True), (True, False), (False, True)])
+def test_fused_prologue_backward_matches_finite_differences(l2norm_qk, beta_sigmoid):
+    """kda_prefill_backward_fused (L2 norm of q, k and / or sigmoid beta before the recurrence) against
     central differences of the fused forward evaluated in fp64 (the chunkwise CPU model, exact to
     1e-12 against the oracle loop, so no fp32 rounding enters the differences)."""
     from tests.chunk_model import chunk_prefill
@@ -78,14 +79,19 @@ def test_fused_prologue_backward_matches_finite_differences():
     x = dict(q=rng.standard_normal((T, H, dk)) * 1.7, k=rng.standard_normal((T, H, dk)) * 0.8,
              v=rng.standard_normal((T, H, dv)), log_alpha=-0.4 * rng.random((T, H, dk)),
              beta=rng.standard_normal((T, H)) * 1.5, S0=0.5 * rng.standard_normal((len(lengths), H, dk, dv)))
+    if not beta_sigmoid:  # beta taken as given: keep it in (0, 1)
+        x["beta"] = oracle.sigmoid(x["beta"])
+    if not l2norm_qk:  # q, k taken as given: unit rows, as the plain recurrence wants
+        x["q"], x["k"] = oracle.l2_normalize(x["q"], 0.0), oracle.l2_normalize(x["k"], 0.0)
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     dO = rng.standard_normal((T, H, dv))
     dSf = rng.standard_normal((len(lengths), H, dk, dv))
     eps = 1e-3
+    nq = (lambda a: oracle.l2_normalize(a, eps)) if l2norm_qk else (lambda a: a)
+    sg = oracle.sigmoid if beta_sigmoid else (lambda a: a)
 
     def loss(y):
-        o, sf = chunk_prefill(oracle.l2_normalize(y["q"], eps), oracle.l2_normalize(y["k"], eps), y["v"],
-                              y["log_alpha"], oracle.sigmoid(y["beta"]), cu, y["S0"], chunk=4)
+        o, sf = chunk_prefill(nq(y["q"]), nq(y["k"]), y["v"], y["log_alpha"], sg(y["beta"]), cu, y["S0"], chunk=4)
         return float(np.sum(o * dO) + np.sum(sf * dSf))
 
     def fd(name, idx, h):
@@ -96,7 +102,7 @@ def test_fused_prologue_backward_matches_finite_differences():
         return (loss(xp) - loss(xm)) / (2 * h)
 
     g = oracle.kda_prefill_backward_fused(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], cu, x["S0"], dO, dSf,
-                                          l2_eps=eps)
+                                          l2norm_qk=l2norm_qk, beta_sigmoid=beta_sigmoid, l2_eps=eps)
     for name, grad in zip(("q", "k", "v", "log_alpha", "beta", "S0"), g):
         for idx in np.ndindex(*x[name].shape):
             h = 2.0 ** -14
