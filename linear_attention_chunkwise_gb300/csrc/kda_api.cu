@@ -45,6 +45,14 @@ kda_status check_device() {
     return ok ? KDA_OK : KDA_ERR_UNSUPPORTED;
 }
 
+}  // namespace
+
+namespace kda {
+kda_status device_check() { return check_device(); }
+}  // namespace kda
+
+namespace {
+
 int sm_count() {
     static int count[kMaxDevices];
     int dev = 0;

@@ -13,6 +13,10 @@ namespace kda {
 constexpr int kChunk = 64;   // chunk length of the prefill
 constexpr int kHeadDim = 128;  // dk = dv
 
+// KDA_OK when the current device is sm_103 (the only architecture the kernels are built for),
+// KDA_ERR_UNSUPPORTED for another one, KDA_ERR_CUDA when the runtime cannot say.
+kda_status device_check();
+
 // ---- decode ----
 struct DecodeFusion {  // KDA_FUSE_* bits and their parameters (see kda_fusion)
     uint32_t flags = 0;

@@ -53,6 +53,10 @@ extern "C" KDA_API kda_status kda_prefill_noalloc(const void* q, const void* k, 
                                                   float* S_final, int32_t* device_status, kda_stream_t stream) {
     if (qkv_dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;  // fp32 inputs need token-sized scratch
     if (num_seqs > KDA_NOALLOC_MAX_SEQS) return KDA_ERR_WORKSPACE;
+    // The same architecture check as kda_prefill, before the symbol lookup (which fails on a GPU
+    // the library has no code for), so both entry points give the same status there.
+    const kda_status dev = kda::device_check();
+    if (dev != KDA_OK) return dev;
     void* scratch = nullptr;
     const kda_status st = scratch_for_current_device(&scratch);
     if (st != KDA_OK) return st;

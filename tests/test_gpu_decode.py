@@ -56,35 +56,49 @@ def test_decode_bad_slot_is_reported_and_skipped():
     assert not torch.equal(d.S[0], S_before[0])
 
 
-def test_decode_config3_graph_sampled():
+def test_decode_config3_graph_all_units():
     """256 sequences x 32 heads, 100 steps captured in one CUDA graph (the bench's launch
-    configuration); o of every step and the final state checked on sampled (seq, head) units."""
+    configuration).  Every (sequence, head) unit is checked against the oracle, which runs the same
+    100 steps on the exact input bytes: o of every step and the state after step 100.  The bound is
+    applied to the whole tensors and to each unit on its own; the worst unit is printed."""
     c = synth.WORKLOADS["decode_256x32"]
     d = synth.workload_inputs("decode_256x32", device="cuda")
     N, H, steps = c["N"], c["H"], c["steps"]
-    g = torch.Generator().manual_seed(99)
-    units = [(int(n), int(h)) for n, h in zip(torch.randint(0, N, (48,), generator=g),
-                                              torch.randint(0, H, (48,), generator=g))]
-    units = sorted(set(units))
-    S0 = {u: host(d.S[u[0], u[1]]).astype(np.float64) for u in units}
+    S_ref = host(d.S).astype(np.float64)  # [N, H, 128, 128], updated in place by the oracle
     o_all = torch.empty((steps, N, H, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(graph, stream=stream):
         for t in range(steps):
-            kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], d.S, None, o=o_all[t])
+            kda.kda_decode_step(d.q[t], d.k[t], d.v[t], d.log_alpha[t], d.beta[t], d.S, None, o=o_all[t],
+                                device_status=status)
     graph.replay()
     torch.cuda.synchronize()
-    for (n, h) in units:
-        S = S0[(n, h)][None, None].copy()
-        o_ref = np.zeros((steps, 128))
-        for t in range(steps):
-            sl = lambda x: host(x[t, n:n + 1, h:h + 1])
-            o_ref[t] = oracle.kda_decode_step(sl(d.q), sl(d.k), sl(d.v), sl(d.log_alpha),
-                                              host(d.beta[t, n:n + 1, h:h + 1]), S)[0, 0]
-        assert rell2(host(o_all[:, n, h]), o_ref) < TOL
-        assert rell2(host(d.S[n, h]), S[0, 0]) < 1e-4
+    assert int(status.item()) == 0
+    err2 = np.zeros((N, H))  # per unit: squared error and squared reference norm of o over all steps
+    ref2 = np.zeros((N, H))
+    for t in range(steps):
+        o_ref = oracle.kda_decode_step(host(d.q[t]), host(d.k[t]), host(d.v[t]), host(d.log_alpha[t]),
+                                       host(d.beta[t]), S_ref)
+        diff = host(o_all[t]).astype(np.float64) - o_ref
+        err2 += np.sum(diff * diff, axis=-1)
+        ref2 += np.sum(o_ref * o_ref, axis=-1)
+    unit_o = np.sqrt(err2 / np.maximum(ref2, 1e-300))
+    S_gpu = host(d.S).astype(np.float64)
+    dS = S_gpu - S_ref
+    unit_s = np.sqrt(np.sum(dS * dS, axis=(2, 3)) / np.maximum(np.sum(S_ref * S_ref, axis=(2, 3)), 1e-300))
+    whole_o = float(np.sqrt(err2.sum() / ref2.sum()))
+    whole_s = rell2(S_gpu, S_ref)
+    wo = np.unravel_index(np.argmax(unit_o), unit_o.shape)
+    ws = np.unravel_index(np.argmax(unit_s), unit_s.shape)
+    print(f"decode 256x32x100: rel-L2 o {whole_o:.3e} (worst unit {tuple(int(x) for x in wo)}: "
+          f"{unit_o[wo]:.3e}), S after step 100 {whole_s:.3e} (worst unit {tuple(int(x) for x in ws)}: "
+          f"{unit_s[ws]:.3e})")
+    assert whole_o < TOL and float(unit_o.max()) < TOL
+    # the state path is fp32 end to end (bf16 only in the inputs): far inside the bf16 budget
+    assert whole_s < 1e-4 and float(unit_s.max()) < 1e-4
 
 
 # ------------------------------------------------------------ multi-token --

@@ -73,7 +73,7 @@ def test_snapshots_varlen_match_oracle_prefixes(dtype):
 
 
 def test_snapshots_across_pieces_of_a_long_sequence():
-    # one sequence, two heads: the scan runs piecewise (64 chunks per piece); entries sit on
+    # one sequence, two heads: the scan runs piecewise (48 chunks per piece); entries sit on
     # both sides of the piece boundary and at the ragged end
     L = 64 * 64 * 2 + 37
     p = synth.prefill_inputs([L], 2, s0_std=0.02, seed=612, device="cuda")
