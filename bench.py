@@ -570,6 +570,57 @@ def bench_decode(cx: Ctx, args):
     }
 
 
+def bench_prefill_workload(cx: Ctx, args, name: str, calls: int):
+    """One of the larger prefill workloads (the packed varlen batch with start states, or the 1M-token
+    sequence), device-resident, timed with CUDA events over `calls` calls after 2 warm-up calls."""
+    torch = cx.torch
+    import linear_attention_chunkwise_gb300 as kda
+    from linear_attention_chunkwise_gb300 import synth
+
+    c = synth.WORKLOADS[name]
+    p = synth.prefill_inputs(synth.workload_lengths(name), c["H"], D, c["dtype"], c["lo"], c["s0_std"],
+                             synth.workload_seed(name) + 1000 * cx.rank, cx.dev)
+    T, N = p.total_tokens, len(p.lengths)
+    o = torch.empty_like(p.q)
+    sf = torch.empty((N, H, D, D), dtype=torch.float32, device=cx.dev)
+    work = torch.empty(kda.kda_prefill_workspace_bytes(c["dtype"], N, T, H), dtype=torch.uint8, device=cx.dev)
+
+    def call():
+        kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, o=o, S_final=sf, workspace=work,
+                        stream=cx.stream)
+
+    for _ in range(2):
+        call()
+    cx.barrier()
+    ev0, ev1 = cx.events()
+    with ClockSampler(cx.dev) as clk:
+        ev0.record(cx.stream)
+        for _ in range(calls):
+            call()
+        ev1.record(cx.stream)
+        cx.barrier()
+    ms_local = ev0.elapsed_time(ev1) / calls
+    ms = cx.max_over_ranks(ms_local)
+    states = N * H * STATE_BYTES * (2 if p.S0 is not None else 1)  # S_final out (+ S0 in)
+    bytes_per_call = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + states
+    achieved = bytes_per_call / (ms_local * 1e-3) / 1e9
+    flops = T * H * PREFILL_FLOPS_PER_TOKEN_HEAD
+    pk = cx.peaks
+    del work, o, sf, p
+    torch.cuda.empty_cache()
+    return {
+        "workload": c["name"], "tokens": T, "sequences": N, "calls": calls,
+        "value": round(whole_job_mtok_s(T, cx.ws, ms), 3), "unit": "Mtok/s", "ms_per_call": round(ms, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4), "traffic": None,
+                     "kernel": "kda_prefill call (chunk table + chunk prep + scan kernels)",
+                     "peak_source": pk["src"] + " burst copy", "bytes_per_launch": bytes_per_call},
+        "tensor": {"achieved": round(flops / (ms_local * 1e-3) / 1e12, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                   "frac": round(flops / (ms_local * 1e-3) / 1e12 / pk["bf16"], 4)},
+        "clocks": clk.summary(),
+    }
+
+
 def bench_prefill_fused(cx: Ctx, args):
     """The 8k prefill through kda_prefill_ex with every fusion: q/k L2 norm, sigmoid beta and the
     output RMSNorm x gate (2-CTA cluster scan).  Device-resident inputs, CUDA events."""
@@ -702,6 +753,10 @@ def run_ours(args):
     dc = bench_decode(cx, args) if args.only in ("all", "decode") else None
     bw = bench_backward(cx, args) if args.only in ("all", "backward") else None
     pfz = bench_prefill_fused(cx, args) if args.only == "prefill_fused" else None
+    wl = {}
+    if args.only in ("all", "prefill", "prefill_large"):
+        wl["varlen_prefill"] = bench_prefill_workload(cx, args, "varlen_prefill", 5)
+        wl["long_prefill_1m"] = bench_prefill_workload(cx, args, "long_prefill_1m", 3)
     out = {"metric": METRIC}
     if pf is not None:
         out.update({
@@ -724,6 +779,8 @@ def run_ours(args):
         out["backward"] = bw
     if pfz is not None:
         out["prefill_fused"] = pfz
+    if wl:
+        out["prefill_workloads"] = wl
     if cx.rank == 0 and not args.no_cpu_baseline and pf is not None:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if cx.rank == 0:
@@ -822,7 +879,8 @@ def main(argv=None):
     ap.add_argument("--decode-reps", type=int, default=5, help="replays of the 100-step decode graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target wall time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "prefill_fused"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "prefill_fused", "prefill_large"],
+                    default="all",
                     help="profiling aid: run only one workload (the JSON line then lacks the other)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":

@@ -32,6 +32,7 @@ def test_our_arm_json_line(monkeypatch, capsys):
     monkeypatch.setattr(bench, "bench_prefill", _fake_prefill)
     monkeypatch.setattr(bench, "bench_decode", lambda cx, args: {"value": 1.0})
     monkeypatch.setattr(bench, "bench_backward", lambda cx, args: {"value": 1.0})
+    monkeypatch.setattr(bench, "bench_prefill_workload", lambda cx, args, name, calls: {"value": 1.0, "name": name})
     monkeypatch.setattr(bench, "cpu_baseline",
                         lambda s: {"value": 0.01, "unit": "Mtok/s", "cores": 16, "kind": "oracle", "sample": "x"})
     args = argparse.Namespace(steps=7, warmup=3, only="all", no_cpu_baseline=False, cpu_seconds=1.0)
@@ -52,3 +53,4 @@ def test_our_arm_json_line(monkeypatch, capsys):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["gpu_launches"] > 0
     assert "decode" in d and "backward" in d
+    assert set(d["prefill_workloads"]) == {"varlen_prefill", "long_prefill_1m"}
