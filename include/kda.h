@@ -27,10 +27,10 @@
  *     state_indices and device_status 4-byte aligned; the prefill workspace
  *     256-byte aligned.  The library allocates no device memory, never
  *     synchronises the host, and enqueues all work on `stream` (a
- *     cudaStream_t; NULL = the legacy default stream).  The two-pass prefill
- *     may also run part of its work on a library-owned stream per device
- *     (created on first use), ordered with `stream` by events: the call's
- *     work still completes before later work on `stream` starts.
+ *     cudaStream_t; NULL = the legacy default stream).  It owns no streams,
+ *     events or locks and keeps no state between calls except, per device,
+ *     the kernels' attribute settings, the entry points it looks up in the
+ *     driver, and (kda_prefill_noalloc only) its fixed scratch array.
  *   - Argument errors are returned synchronously before anything is
  *     enqueued.  Data-dependent errors found on the device are OR-ed into
  *     *device_status (if non-NULL) as KDA_DEV_* bits; the affected sequences

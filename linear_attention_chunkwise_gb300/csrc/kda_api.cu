@@ -64,64 +64,21 @@ int sm_count() {
     return count[dev];
 }
 
-// Piecewise schedule of the two-pass prefill.  When the scan has fewer CTAs
+// Piecewise schedule of the two-pass prefill.  When the scan has no more CTAs
 // than the GPU has SMs (few sequences), the scan runs in pieces of 48 or more
-// chunks per sequence (at most 32 pieces) and pass 1 runs ahead of it: a first
-// pass-1 launch prepares a lead of chunks on the whole GPU, and each later one
-// prepares its share while the previous scan piece runs on the SMs it leaves
-// idle (pass 2 then reads images written moments earlier, still in L2).  Pass 1
-// stays on the caller's stream; pass 2 runs on a library-owned high-priority
-// stream per device, ordered by events, and the caller's stream waits for the
-// last scan before the call returns.  A later pass-1 launch is held back (a
-// stream wait on a counter the scan CTAs bump as they start) until every CTA of
-// the running scan piece is resident, so prep CTAs cannot take the SMs the scan
-// needs.  Each piece boundary costs a few microseconds (launch, state carry,
-// first copies), which bounds the piece count.
+// chunks per sequence (at most 32 pieces) and pass 1 runs ahead of it, all on
+// the caller's stream: a first pass-1 launch prepares a lead of chunks on the
+// whole GPU; then each scan piece is followed by the next pass-1 share,
+// launched as a programmatic dependent of that piece, so that it starts once
+// every CTA of the piece is running and takes only the SMs the scan leaves
+// idle (pass 2 then reads images written moments earlier, still in L2).  Each
+// scan piece is an ordinary launch: it starts after everything before it on
+// the stream, the previous piece (whose S_final carries the state) and the
+// pass-1 shares included.  Each piece boundary costs a few microseconds
+// (launch, state carry, first copies), which bounds the piece count.
 constexpr int64_t kScanPieceChunks = 48;  // smallest scan piece (chunks per sequence); each piece costs a few us
 constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
 constexpr double kPrepLag = 0.1;           // lead of pass 1, as a fraction of the chunks scanned after piece 0
-
-struct PieceStreams {
-    std::mutex mu;  // one call at a time enqueues record/wait pairs on these
-    cudaStream_t scan = nullptr;
-    cudaEvent_t prep_done = nullptr, scan_done = nullptr;
-    bool failed = false;
-};
-PieceStreams* piece_streams() {
-    static PieceStreams res[kMaxDevices];
-    static std::mutex init_mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    PieceStreams& r = res[dev];
-    std::lock_guard<std::mutex> g(init_mu);
-    if (r.failed) return nullptr;
-    if (!r.scan) {
-        int least = 0, greatest = 0;
-        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&r.scan, cudaStreamNonBlocking, greatest) != cudaSuccess ||
-            cudaEventCreateWithFlags(&r.prep_done, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&r.scan_done, cudaEventDisableTiming) != cudaSuccess) {
-            r.failed = true;
-            return nullptr;
-        }
-    }
-    return &r;
-}
-
-// cuStreamWaitValue32 (driver entry point), or null when unavailable.
-PFN_cuStreamWaitValue32_v11070 wait_value_fn() {
-    static PFN_cuStreamWaitValue32_v11070 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 11070, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(p);
-    });
-    return fn;
-}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -167,7 +124,7 @@ int64_t max_chunks(int32_t N, int64_t T) { return (T + kda::kChunk - 1) / kda::k
 WsLayout split_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
     WsLayout w;
     w.table = round_up(static_cast<size_t>(N > 0 ? N : 1) * 4, kAlign);
-    w.copies = w.table + round_up(static_cast<size_t>(N + 3) * 4, kAlign);  // chunk table + start counter
+    w.copies = w.table + round_up(static_cast<size_t>(N + 2) * 4, kAlign);  // chunk table
     w.blobs = w.copies + copies_bytes(t, T, H);
     w.total = w.blobs + static_cast<size_t>(max_chunks(N, T)) * H * kda::kPrefillBlobBytes;
     return w;
@@ -406,55 +363,38 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const int64_t sq = std::max<int64_t>(kScanPieceChunks, (seq_chunks + kMaxScanPieces - 1) / kMaxScanPieces);
         const int64_t pieces = (seq_chunks + sq - 1) / sq;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        PieceStreams* ps = nullptr;
-        if (S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
-            cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
-            ps = piece_streams();
-        if (!ps)
+        const bool piecewise = S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
+                               cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
+        if (!piecewise)
             return kda::launch_prefill_split(tm_q, tm_k, tm_v, og ? &tm_g : nullptr, a,
                                              max_chunks(num_seqs, total_tokens), out_f32,
                                              stream) == cudaSuccess
                        ? KDA_OK
                        : KDA_ERR_CUDA;
-        // Scan piece j covers chunks [j sq, (j+1) sq).  Pass 1 runs ahead: its first piece prepares a
-        // lead of L0 chunks on the whole GPU, then its piece j (j >= 1) prepares the next share of the
-        // rest while scan piece j-1 runs; scan piece j starts once pass-1 pieces 0..j are done.
-        // L0 makes up for pass 1 being slower on the SMs the scan leaves than the scan is per chunk.
+        // Scan piece j covers chunks [j sq, (j+1) sq).  Pass 1's first launch prepares a lead of L0
+        // chunks; its launch j (j >= 1) prepares the next share of the rest beside scan piece j-1.  L0
+        // makes up for pass 1 being slower on the SMs the scan leaves than the scan is per chunk.
         const int64_t lead = std::min<int64_t>(
             seq_chunks, sq + static_cast<int64_t>(kPrepLag * static_cast<double>(sq * (pieces - 1)) + 0.999));
         const int64_t share = (seq_chunks - lead + pieces - 2) / (pieces - 1);
-        std::lock_guard<std::mutex> g(ps->mu);
-        auto wait_value = wait_value_fn();
-        uint32_t* started = reinterpret_cast<uint32_t*>(ws + two.table) + num_seqs + 2;
-        const uint32_t scan_ctas = static_cast<uint32_t>(num_seqs) * H * 2;
-        bool ok = !wait_value || cudaMemsetAsync(started, 0, 4, stream) == cudaSuccess;
-        a.started = wait_value ? started : nullptr;
-        int64_t prepared = 0;  // chunks [0, prepared) of every sequence have their images
+        bool ok = true;
+        int64_t prepared = 0;  // chunks [0, prepared) of every sequence have their images (or are queued)
         for (int64_t j = 0; j < pieces && ok; ++j) {
             const int64_t scan_end = std::min(seq_chunks, (j + 1) * sq);
             int64_t prep_end = j == 0 ? lead : std::min(seq_chunks, lead + j * share);
             prep_end = std::max(prep_end, scan_end);
             if (prep_end > prepared) {
-                if (j > 0 && wait_value)  // pass 1 starts once every CTA of scan piece j-1 is resident
-                    ok = wait_value(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(started),
-                                    static_cast<cuuint32_t>(j * scan_ctas), CU_STREAM_WAIT_VALUE_GEQ) == CUDA_SUCCESS;
                 a.piece_begin = static_cast<int32_t>(prepared);
                 a.piece_len = static_cast<int32_t>(prep_end - prepared);
-                ok = ok &&
-                     kda::launch_chunk_prep(tm_q, tm_k, a, static_cast<int64_t>(num_seqs) * a.piece_len,
-                                            stream) == cudaSuccess &&
-                     cudaEventRecord(ps->prep_done, stream) == cudaSuccess &&
-                     cudaStreamWaitEvent(ps->scan, ps->prep_done, 0) == cudaSuccess;
+                ok = kda::launch_chunk_prep(tm_q, tm_k, a, static_cast<int64_t>(num_seqs) * a.piece_len, stream,
+                                            j > 0) == cudaSuccess;
                 prepared = prep_end;
             }
             a.piece_begin = static_cast<int32_t>(j * sq);
             a.piece_len = static_cast<int32_t>(scan_end - j * sq);
-            ok = ok && kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, ps->scan) == cudaSuccess;
+            ok = ok && kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, stream) == cudaSuccess;
         }
-        // join even after a failed launch so later work on `stream` stays ordered
-        const bool joined = cudaEventRecord(ps->scan_done, ps->scan) == cudaSuccess &&
-                            cudaStreamWaitEvent(stream, ps->scan_done, 0) == cudaSuccess;
-        return ok && joined ? KDA_OK : KDA_ERR_CUDA;
+        return ok ? KDA_OK : KDA_ERR_CUDA;
     } else if (kda::launch_prefill_fused(tm_q, tm_k, tm_v, tm_la, a, out_f32, stream) != cudaSuccess) {
         return KDA_ERR_CUDA;
     }

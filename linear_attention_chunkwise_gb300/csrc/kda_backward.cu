@@ -82,12 +82,6 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
     w.y = *reinterpret_cast<const uint32_t*>(&b);
     *reinterpret_cast<uint2*>(p) = w;
 }
-template <typename T>
-__device__ __forceinline__ float ld1(const T* p);
-template <>
-__device__ __forceinline__ float ld1<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 // two adjacent elements (p even-aligned)
 template <typename T>
 __device__ __forceinline__ float2 ld2(const T* p);

@@ -53,8 +53,6 @@ struct PrefillArgs {
     // of every sequence; piece_len = 0 means all chunks in one launch pair.
     int32_t piece_begin = 0;
     int32_t piece_len = 0;
-    // piece mode: every pass-2 CTA adds 1 here when it starts (workspace word)
-    uint32_t* started = nullptr;
     // state snapshots (two-pass path): sorted (sequence, position) entries
     const int32_t* snap_seq = nullptr;
     const int32_t* snap_pos = nullptr;
@@ -95,8 +93,11 @@ cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_
                                  int64_t max_chunks, bool out_f32, cudaStream_t stream);
 // The two passes separately, for the piecewise schedule.  Pass 1's grid is
 // `units` x H CTAs: units = chunk slots of the whole batch (piece_len = 0) or
-// num_seqs x piece_len (piece mode).  Pass 2 has num_seqs x H x 2 CTAs.
-cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units, cudaStream_t stream);
+// num_seqs x piece_len (piece mode); with beside_previous it is launched as a
+// programmatic dependent of the previous launch on `stream` (a scan piece,
+// whose CTAs release it once all of them run).  Pass 2 has num_seqs x H x 2 CTAs.
+cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units,
+                              cudaStream_t stream, bool beside_previous);
 // tm_g: TMA map of the output gate (required with KDA_FUSE_OUT_GATE, else unused / NULL).
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
                               cudaStream_t stream);

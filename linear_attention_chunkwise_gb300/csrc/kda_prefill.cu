@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid < C && tid < t_end - t_begin) beta_next = p.beta[(t_begin + tid) * H + h];
 
     uint32_t ph[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    auto wait_bar = [&](int i) {
-        if (!mbar_wait(&bars[i], ph[i], kWaitLimit)) {
+    auto wait_bar = [&](int i) {  // on expiry the phase is waited for again (drain) before going on
+        if (!mbar_wait_pipe(&bars[i], ph[i])) {
             *abort_s = 1;
             if (p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
         }
@@ -443,11 +443,11 @@ __global__ void __launch_bounds__(NT, 1)
     const bool aborted = *abort_s != 0;
     if (tid == 0) {
         mma_commit(&bars[BAR_FIN]);
-        (void)mbar_wait(&bars[BAR_FIN], 0, kWaitLimit);
-        if (aborted) {
-            if (fl_la) (void)mbar_wait(&bars[BAR_LA], ph[BAR_LA], kWaitLimit);
-            if (fl_qk) (void)mbar_wait(&bars[BAR_QK], ph[BAR_QK], kWaitLimit);
-            if (fl_v) (void)mbar_wait(&bars[BAR_V], ph[BAR_V], kWaitLimit);
+        (void)mbar_wait(&bars[BAR_FIN], 0, kDrainLimit);
+        if (aborted) {  // copies issued after the last wait on their barrier
+            if (fl_la) (void)mbar_wait(&bars[BAR_LA], ph[BAR_LA], kDrainLimit);
+            if (fl_qk) (void)mbar_wait(&bars[BAR_QK], ph[BAR_QK], kDrainLimit);
+            if (fl_v) (void)mbar_wait(&bars[BAR_V], ph[BAR_V], kDrainLimit);
         }
     }
     if (p.S_final && !aborted) {

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(NT, 3)
     // Only thread 0 waits on each mbarrier; the others sleep in the block barrier that follows
     // (a spinning wait would take issue slots from the other CTAs on the SM).
     bool ok = true;
-    if (tid == 0) ok = mbar_wait(&bars[0], 0, kWaitLimit);
+    if (tid == 0) ok = mbar_wait_pipe(&bars[0], 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(NT, 3)
         bulk_commit();
     }
     if (tid == 0) {
-        ok = mbar_wait(&bars[1], 0, kWaitLimit) && ok;
+        ok = mbar_wait_pipe(&bars[1], 0) && ok;
         bulk_wait_read();  // Qh and Kb have been read: their space becomes scratch
     }
     __syncthreads();
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(NT, 3)
                      s > 0);
         mma_commit(&bars[1]);
     }
-    if (tid == 0) ok = mbar_wait(&bars[1], 1, kWaitLimit) && ok;
+    if (tid == 0) ok = mbar_wait_pipe(&bars[1], 1) && ok;
     __syncthreads();
     tc_fence_after();
     if (qw < 2) {  // -W -> rows 0..63 of OP_A
@@ -507,7 +507,9 @@ __global__ void __launch_bounds__(NTS, 1)
     const int slice = blockIdx.x % NSLICE;
     const int h = (blockIdx.x / NSLICE) % H;
     const int pos = blockIdx.x / (NSLICE * H);
-    if (p.started && tid == 0) atomicAdd(p.started, 1u);  // before any early exit: the host gates on it
+    // A pass-1 launch queued behind this one as its programmatic dependent may start once every CTA of
+    // this grid has reached here: it then only takes the SMs the scan leaves idle.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (co[N + 1] == 0) return;  // malformed cu_seqlens: nothing is written
     const int seq = p.order ? p.order[pos] : pos;
     const int nch_seq = co[seq + 1] - co[seq];
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(NTS, 1)
     }
     uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] (and evbar[i]) in bit i
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
-        if (!mbar_wait(bar, ph, kWaitLimit)) *abort_s = 1;
+        if (!mbar_wait_pipe(bar, ph)) *abort_s = 1;
         ph ^= 1u;
     };
     // fused output gate: y = o / sqrt(mean o^2 + eps) * weight * gate for chunk cf, whose O rows sit in
@@ -658,7 +660,7 @@ __global__ void __launch_bounds__(NTS, 1)
         const float sc = rsqrtf((own_pending + rx[bf * 64 + rr]) * (1.f / D) + p.rms_eps);
         float* a = o_pend;
         const int64_t tf = t_begin + static_cast<int64_t>(cf) * C;
-        if (!mbar_wait(&gbar[bf], (ph_g >> bf) & 1u, kWaitLimit)) *abort_s = 1;
+        if (!mbar_wait_pipe(&gbar[bf], (ph_g >> bf) & 1u)) *abort_s = 1;
         ph_g ^= 1u << bf;
         if (tid == 64) gate_pending = -1;
         if (tf + rr < t_end) {
@@ -685,6 +687,7 @@ __global__ void __launch_bounds__(NTS, 1)
     const uint64_t d_sm = sdesc_sw128(smem_u32(sm + L::OP_SM), 8192, 1024);
     const uint64_t d_u = sdesc_sw128(smem_u32(sm + L::OP_U), 8192, 1024);
 
+    int c_stop = nch;  // the step the loop stopped at (nch when it ran to the end)
     for (int c = 0; c < nch; ++c) {
         const int b = c & 1;
         uint8_t* set = sm + b * L::SET;
@@ -697,13 +700,13 @@ __global__ void __launch_bounds__(NTS, 1)
         const uint32_t par = (ph_load >> b) & 1u;
         ph_load ^= 1u << b;
         if (Lc < C) {  // rows of v past the sequence end -> 0
-            if (!mbar_wait(&bars[b], par, kWaitLimit)) *abort_s = 1;
+            if (!mbar_wait_pipe(&bars[b], par)) *abort_s = 1;
             for (int e = tid; e < (C - Lc) * 8; e += NTS) {
                 const int r = Lc + (e >> 3);
                 *reinterpret_cast<uint4*>(set + L::S_V + sw128_chunk(r, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        if (!mbar_wait(&evbar[b], par, kWaitLimit)) *abort_s = 1;
+        if (!mbar_wait_pipe(&evbar[b], par)) *abort_s = 1;
         {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks PC*cq/8 ..)
             const float sc = evs[rho];
 #pragma unroll
@@ -715,10 +718,13 @@ __global__ void __launch_bounds__(NTS, 1)
             }
         }
         fence_async_smem();
-        if (Lc == C && tid == 0 && !mbar_wait(&bars[b], par, kWaitLimit)) *abort_s = 1;
+        if (Lc == C && tid == 0 && !mbar_wait_pipe(&bars[b], par)) *abort_s = 1;
         tc_fence_before();
         __syncthreads();
-        if (*abort_s) break;  // a bounded wait expired: every thread sees it after the barrier
+        if (*abort_s) {  // a bounded wait expired: every thread sees it after the barrier
+            c_stop = c;
+            break;
+        }
         // shared-memory descriptors; a K-step adds its byte offset / 16 to the start-address field
         const uint64_t d_a = sdesc_sw128(smem_u32(set + L::S_A), 16, 1024);
         const uint64_t d_kb = sdesc_sw128(smem_u32(set + L::S_KB), 8192, 1024);
@@ -827,13 +833,19 @@ __global__ void __launch_bounds__(NTS, 1)
     if (OG && qw >= 2 && *abort_s == 0)  // the last chunk's output gate
         og_finish(nch - 1, 32 * (qw - 2) + lane);
     if (OG && tid == 64 && gate_pending >= 0)  // a wind-down left a gate copy in flight: let it land
-        (void)mbar_wait(&gbar[gate_pending & 1], (ph_g >> (gate_pending & 1)) & 1u, kWaitLimit);
+        (void)mbar_wait(&gbar[gate_pending & 1], (ph_g >> (gate_pending & 1)) & 1u, kDrainLimit);
     __syncthreads();
     const bool ok = *abort_s == 0;
     if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
     if (tid == 0) {  // every MMA and copy this CTA issued has landed before it exits
         mma_commit(&bars[4]);
-        (void)mbar_wait(&bars[4], 0, kWaitLimit);
+        (void)mbar_wait(&bars[4], 0, kDrainLimit);
+        // a step's loads are waited for (to completion) in that step; the next chunk's are issued
+        // after the step's barrier, so only a stop at step 0 leaves chunk 1's (issued up front) in flight
+        if (c_stop == 0 && nch > 1) {
+            (void)mbar_wait(&evbar[1], 0, kDrainLimit);
+            (void)mbar_wait(&bars[1], 0, kDrainLimit);
+        }
     }
     if (p.S_final && ok)  // staged in operand set 0: every copy into it has been consumed
         store_state_rows<PC>(p.S_final + ((static_cast<size_t>(seq) * H + h) * D + 32 * qw) * D + j0 + PC * cq, S,
@@ -872,7 +884,7 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
 }
 
 cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool beside_previous) {
     static int cfg_prep[64];
     cudaError_t err = set_smem(kda_chunk_prep_kernel, PrepSmem::ALLOC, cfg_prep);
     if (err != cudaSuccess) return err;
@@ -882,8 +894,19 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
     if (err != cudaSuccess) return err;
     const long long prep_ctas = static_cast<long long>(units) * a.H;
     if (prep_ctas > 0) {
-        kda_chunk_prep_kernel<<<static_cast<unsigned>(prep_ctas), NT, PrepSmem::ALLOC, stream>>>(tm_q, tm_k, a);
-        err = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(prep_ctas));
+        cfg.blockDim = dim3(NT);
+        cfg.dynamicSmemBytes = PrepSmem::ALLOC;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        if (beside_previous) {  // programmatic dependent of the previous launch (a scan piece): it reads
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // nothing that one writes
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        err = cudaLaunchKernelEx(&cfg, kda_chunk_prep_kernel, tm_q, tm_k, a);
     }
     return err;
 }
@@ -891,7 +914,7 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                  const CUtensorMap* tm_g, const PrefillArgs& a,
                                  int64_t max_chunks, bool out_f32, cudaStream_t stream) {
-    const cudaError_t err = launch_chunk_prep(tm_q, tm_k, a, max_chunks, stream);
+    const cudaError_t err = launch_chunk_prep(tm_q, tm_k, a, max_chunks, stream, false);
     if (err != cudaSuccess) return err;
     return launch_chunk_scan(tm_v, tm_g, a, out_f32, stream);
 }

@@ -1,0 +1,88 @@
+"""The prefill kernels' wind-down after an expired on-chip wait, exercised without a fault.
+
+Every on-chip wait of the prefill kernels is bounded.  When a pipeline wait (for a copy or a
+tensor-core product the next step needs) expires, the kernel sets KDA_DEV_TIMEOUT, waits for that
+same operation again with a separate drain limit before anything reuses its buffers, stops its
+loop, waits for every copy and product of its own still in flight, releases TMEM and returns.
+
+A second copy of the library built with KDA_PIPE_WAIT_CYCLES=0 makes every pipeline wait that is
+not already complete on its first poll expire; the drain waits keep their normal limit.  Nothing
+stalls on purpose: every awaited copy and product completes as usual.  Each test calls that copy
+through the C ABI, checks that the call returns and the status word carries KDA_DEV_TIMEOUT, then
+runs the normal library in the same process and checks its result against the fp64 oracle.
+"""
+import ctypes
+import os
+
+import pytest
+import torch
+
+import linear_attention_chunkwise_gb300 as kda
+from linear_attention_chunkwise_gb300 import _binding, _build, synth
+from tests.conftest import cuda_ok
+from tests.gpu_util import TOL, host, oracle_prefill_heads, rell2
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+WAIT_DIR = os.path.join(_build.BUILD_DIR, "pipe_wait_0")
+
+
+@pytest.fixture(scope="module")
+def wait_lib():
+    path = _build.build(extra_flags=["-DKDA_PIPE_WAIT_CYCLES=0"], lib_path=os.path.join(WAIT_DIR, "libkda_pipe_wait_0.so"),
+                        build_dir=WAIT_DIR)
+    return _binding.load_library(path)  # its own handle: the normal library stays the package's
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _call(lib, p, path, fusion=None):
+    T, H, _ = p.q.shape
+    N = len(p.lengths)
+    o = torch.full_like(p.q, 7.0)
+    sf = torch.full((N, H, 128, 128), 7.0, dtype=torch.float32, device="cuda")
+    wsb = (kda.kda_prefill_workspace_bytes if path == "two_pass" else kda.kda_prefill_min_workspace_bytes)(
+        p.q.dtype, N, T, H)
+    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (_ptr(p.q), _ptr(p.k), _ptr(p.v), kda.KDA_DTYPE_BF16, _ptr(p.log_alpha), _ptr(p.beta), _ptr(p.S0),
+            _ptr(p.cu_seqlens), N, T, H, 128, 128, _ptr(o), _ptr(sf))
+    if fusion is None:
+        rc = lib.kda_prefill(*args, _ptr(work), work.numel(), _ptr(status), stream)
+    else:
+        fz = fusion.c_struct()
+        rc = lib.kda_prefill_ex(*args, ctypes.byref(fz), _ptr(work), work.numel(), _ptr(status), stream)
+    torch.cuda.synchronize()
+    return rc, int(status.item())
+
+
+def _check_normal_call(p):
+    o, sf = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0)
+    torch.cuda.synchronize()
+    cu = p.cu_seqlens.cpu().tolist()
+    for n, (_, o_ref, sf_ref) in enumerate(oracle_prefill_heads(p)):
+        assert rell2(host(o[cu[n]:cu[n + 1]]), o_ref) < TOL
+        assert rell2(host(sf[n]), sf_ref) < TOL
+
+
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_expired_waits_report_timeout_and_the_next_call_is_exact(wait_lib, path):
+    p = synth.prefill_inputs([300, 77, 130], 3, s0_std=0.02, seed=811, device="cuda")
+    rc, status = _call(wait_lib, p, path)
+    assert rc == kda.KDA_OK
+    assert status & kda.KDA_DEV_TIMEOUT
+    _check_normal_call(p)
+
+
+def test_expired_waits_in_the_cluster_output_gate(wait_lib):
+    """The fused output gate runs the scan as 2-CTA clusters that exchange row sums; both CTAs wind
+    down and meet at the final cluster barrier."""
+    p = synth.prefill_inputs([300, 77], 2, s0_std=0.02, seed=812, device="cuda")
+    gate = torch.randn(p.q.shape, device="cuda").to(p.q.dtype)
+    rc, status = _call(wait_lib, p, "two_pass", kda.Fusion(out_gate=gate))
+    assert rc == kda.KDA_OK
+    assert status & kda.KDA_DEV_TIMEOUT
+    _check_normal_call(p)
