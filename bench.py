@@ -281,11 +281,14 @@ class CopyOverlap:
         self.cs.wait_stream(self.d2h)
 
 
-def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.25):
+def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.1):
     """(pass-1 launches, scan launches) of the library's piecewise prefill schedule for one sequence
-    of seq_chunks chunks: scan pieces of max(min_piece, ceil(n / max_pieces)) chunks, pass 1 a lead
-    of sq + lag * sq * (pieces - 1) chunks, then equal shares."""
-    sq = max(min_piece, -(-seq_chunks // max_pieces))
+    of seq_chunks chunks: the piece count from pieces of max(min_piece, ceil(n / max_pieces)) chunks,
+    then equal pieces of sq chunks; pass 1 a lead of sq + lag * sq * (pieces - 1) chunks, then
+    equal shares."""
+    sq0 = max(min_piece, -(-seq_chunks // max_pieces))
+    n0 = -(-seq_chunks // sq0)
+    sq = -(-seq_chunks // n0)
     pieces = -(-seq_chunks // sq)
     if pieces <= 1:
         return 1, 1

@@ -360,7 +360,9 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
             return KDA_ERR_CUDA;
         // chunks of the longest possible sequence bound the pieces
         const int64_t seq_chunks = (total_tokens + kda::kChunk - 1) / kda::kChunk;
-        const int64_t sq = std::max<int64_t>(kScanPieceChunks, (seq_chunks + kMaxScanPieces - 1) / kMaxScanPieces);
+        // piece count from the smallest piece, then equal pieces (128 chunks: 43, 43, 42)
+        const int64_t sq0 = std::max<int64_t>(kScanPieceChunks, (seq_chunks + kMaxScanPieces - 1) / kMaxScanPieces);
+        const int64_t sq = (seq_chunks + (seq_chunks + sq0 - 1) / sq0 - 1) / ((seq_chunks + sq0 - 1) / sq0);
         const int64_t pieces = (seq_chunks + sq - 1) / sq;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         const bool piecewise = S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&

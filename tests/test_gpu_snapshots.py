@@ -73,11 +73,12 @@ def test_snapshots_varlen_match_oracle_prefixes(dtype):
 
 
 def test_snapshots_across_pieces_of_a_long_sequence():
-    # one sequence, two heads: the scan runs piecewise (48 chunks per piece); entries sit on
-    # both sides of the piece boundary and at the ragged end
+    # one sequence, two heads: 129 chunks, so the scan runs in three pieces of 43 chunks
+    # (2752 tokens); entries sit on both sides of both piece boundaries and at the ragged end
     L = 64 * 64 * 2 + 37
     p = synth.prefill_inputs([L], 2, s0_std=0.02, seed=612, device="cuda")
-    entries = [(0, 64), (0, 4032), (0, 4096), (0, 4160), (0, 8192), (0, L)]
+    entries = [(0, 64), (0, 2688), (0, 2752), (0, 2816), (0, 4096), (0, 5440), (0, 5504), (0, 5568), (0, 8192),
+               (0, L)]
     o, sf, ss, st = _run(p, entries)
     assert st == 0
     for i, (n, pos) in enumerate(entries):
