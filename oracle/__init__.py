@@ -206,3 +206,46 @@ def kda_prefill_backward_fused(q, k, v, log_alpha, beta, cu_seqlens, S0, dO, dS_
     if beta_sigmoid:
         db = db * bh * (1.0 - bh)
     return dq, dk, dv, dla, db, ds0
+
+
+def rmsnorm_gate_backward(o, g, dy, w=None, eps: float = 0.0):
+    """Gradient of y = rmsnorm_gate(o, g, w, eps) for L = <y, dy> (fp64), over the last axis of n entries:
+      y_j = o_j r w_j g_j,  r = (sum_k o_k^2 / n + eps)^(-1/2),  so  dr/do_m = -r^3 o_m / n  and
+      do_m = r w_m g_m dy_m - (r^3 o_m / n) sum_j dy_j o_j w_j g_j
+      dg_j = dy_j o_j r w_j
+      dw_j = the sum over every other axis of dy_j o_j r g_j
+    Returns (do, dg, dw); dw is None when w is None (w = ones)."""
+    o = np.asarray(o, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    n = o.shape[-1]
+    w64 = np.ones(n) if w is None else np.asarray(w, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    wgdy = w64 * g * dy
+    do = r * wgdy - (r ** 3 / n) * o * np.sum(wgdy * o, axis=-1, keepdims=True)
+    dg = dy * o * r * w64
+    dw = None if w is None else np.sum((dy * o * r * g).reshape(-1, n), axis=0)
+    return do, dg, dw
+
+
+def kda_prefill_backward_gated(q, k, v, log_alpha, beta, cu_seqlens, S0, dY, dS_final, gate, rms_weight=None,
+                               rms_eps: float = 0.0, l2norm_qk=False, beta_sigmoid=False, l2_eps: float = 0.0,
+                               nthreads: int = 0, lib=None):
+    """Gradient of the prefill whose output passes through the output gate of "kimi delta attn from first
+    principles" (aryagxr), "KDA has three gates": y = rmsnorm_gate(o, gate, rms_weight, rms_eps), for
+    L = <y, dY> + <S_final, dS_final>, optionally with the fused prologue of kda_prefill_backward_fused.
+    The forward o is recomputed by kda_prefill (on the prologue's outputs), the gate's backward gives
+    dL/do, and kda_prefill_backward_fused carries it through the recurrence.
+    Returns (dq, dk, dv, dlog_alpha, dbeta, dS0, dgate, drms_weight) in float64 (drms_weight None when
+    rms_weight is None)."""
+    q64 = np.asarray(q, dtype=np.float64)
+    k64 = np.asarray(k, dtype=np.float64)
+    b64 = np.asarray(beta, dtype=np.float64)
+    qh = l2_normalize(q64, l2_eps) if l2norm_qk else q64
+    kh = l2_normalize(k64, l2_eps) if l2norm_qk else k64
+    bh = sigmoid(b64) if beta_sigmoid else b64
+    o, _ = kda_prefill(qh, kh, v, log_alpha, bh, cu_seqlens, S0, nthreads=nthreads, lib=lib)
+    do, dg, dw = rmsnorm_gate_backward(o, gate, dY, rms_weight, rms_eps)
+    grads = kda_prefill_backward_fused(q, k, v, log_alpha, beta, cu_seqlens, S0, do, dS_final, l2norm_qk=l2norm_qk,
+                                       beta_sigmoid=beta_sigmoid, l2_eps=l2_eps, nthreads=nthreads, lib=lib)
+    return tuple(grads) + (dg, dw)
