@@ -93,9 +93,9 @@ typedef enum {
  *                        * rms_weight * out_gate instead of o
  *
  * rms_weight: [dv] fp32 device (NULL = all ones); out_gate: [tokens, H, dv]
- * in qkv_dtype, device, 16-byte aligned (required with KDA_FUSE_OUT_GATE;
- * tokens = total_tokens for prefill, N for a decode step, N x T for
- * kda_decode_multi_ex).  l2_eps, rms_eps >= 0.
+ * in qkv_dtype, device, 16-byte aligned (required with KDA_FUSE_OUT_GATE
+ * unless tokens = 0; tokens = total_tokens for prefill, N for a decode step,
+ * N x T for kda_decode_multi_ex).  l2_eps, rms_eps >= 0.
  * The state and S_final are those of the normalised q, k and sigmoid beta.
  */
 #define KDA_FUSE_L2NORM_QK 0x1u
@@ -280,7 +280,8 @@ KDA_API kda_status kda_prefill_backward(const void *q, const void *k, const void
  * writes the normalised q, k (in qkv_dtype) and sigmoid beta into the
  * workspace, runs the plain backward on them, and applies the chain rule in
  * place.  KDA_FUSE_OUT_GATE returns KDA_ERR_UNSUPPORTED (the output gate's
- * backward is not built); fusion NULL or flags 0 is kda_prefill_backward.
+ * backward needs two more outputs: kda_prefill_backward_gated); fusion NULL
+ * or flags 0 is kda_prefill_backward.
  *
  * Workspace: >= kda_prefill_backward_ex_workspace_bytes(...) (the plain
  * figure plus (2 x 128 x sizeof(qkv_dtype) + 12) bytes per (token, head)).
@@ -296,6 +297,47 @@ KDA_API kda_status kda_prefill_backward_ex(const void *q, const void *k, const v
                                            float *grad_v, float *grad_log_alpha, float *grad_beta,
                                            float *grad_S0, const kda_fusion *fusion, void *workspace,
                                            size_t workspace_bytes, int32_t *device_status, kda_stream_t stream);
+
+/*
+ * kda_prefill_backward_gated -- kda_prefill_backward_ex for the layer output
+ * y = o / sqrt(mean_c o_c^2 + rms_eps) * rms_weight * out_gate of
+ * kda_prefill_ex with KDA_FUSE_OUT_GATE (the output gate of "kimi delta attn
+ * from first principles" (aryagxr), section "KDA has three gates").  With
+ * r = (sum_c o_c^2 / 128 + rms_eps)^(-1/2), w = rms_weight, g = out_gate and
+ * dy = grad_y = dL/dy per (token, head) row:
+ *     dL/do_c = r w_c g_c dy_c - (r^3 o_c / 128) sum_j dy_j o_j w_j g_j
+ *     grad_out_gate_c  = dy_c o_c r w_c
+ *     grad_rms_weight_c = sum over all (token, head) rows of dy_c o_c r g_c
+ * and dL/do feeds the chunkwise backward in place of grad_o.  The o here is
+ * the chunkwise forward's own (rerun inside the call, rounded to qkv_dtype
+ * as kda_prefill_ex would output it); dL/do is rounded to qkv_dtype, as
+ * grad_o is given to kda_prefill_backward.
+ *
+ *   grad_y           [total_tokens, H, dv] qkv_dtype device (dL/dy)
+ *   grad_out_gate    [total_tokens, H, dv] fp32 out, 16-byte aligned
+ *   grad_rms_weight  [dv] fp32 out, or NULL (not computed); summed over
+ *                    rows in a fixed order (bitwise repeatable)
+ *   fusion           required, with KDA_FUSE_OUT_GATE set (else
+ *                    KDA_ERR_INVALID_ARG) and out_gate, rms_weight, rms_eps
+ *                    as given to the forward; KDA_FUSE_L2NORM_QK and
+ *                    KDA_FUSE_BETA_SIGMOID act as in kda_prefill_backward_ex.
+ *
+ * Workspace: >= kda_prefill_backward_gated_workspace_bytes(...) (the _ex
+ * figure rounded up to 256 bytes, plus 592 x 128 x 4 bytes of partial sums).
+ * grad_out_gate and grad_rms_weight overlap nothing (KDA_ERR_INVALID_ARG).
+ * Other arguments, errors and overlap rules as kda_prefill_backward_ex.
+ */
+KDA_API size_t kda_prefill_backward_gated_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
+                                                          int64_t total_tokens, int32_t H, int32_t dk, int32_t dv);
+KDA_API kda_status kda_prefill_backward_gated(const void *q, const void *k, const void *v, kda_dtype qkv_dtype,
+                                              const float *log_alpha, const float *beta, const float *S0,
+                                              const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                              int32_t H, int32_t dk, int32_t dv, const void *grad_y,
+                                              const float *grad_S_final, float *grad_q, float *grad_k,
+                                              float *grad_v, float *grad_log_alpha, float *grad_beta,
+                                              float *grad_S0, float *grad_out_gate, float *grad_rms_weight,
+                                              const kda_fusion *fusion, void *workspace, size_t workspace_bytes,
+                                              int32_t *device_status, kda_stream_t stream);
 
 /*
  * kda_decode_step -- one fused recurrent step for N sequences

@@ -2,9 +2,9 @@
 
 Python names mirror the C ABI in include/kda.h:
   kda_prefill, kda_prefill_snapshots, kda_prefill_ex, kda_prefill_backward, kda_prefill_backward_ex,
-  kda_decode_step, kda_decode_step_ex, kda_decode_multi, kda_decode_multi_ex,
+  kda_prefill_backward_gated, kda_decode_step, kda_decode_step_ex, kda_decode_multi, kda_decode_multi_ex,
   kda_prefill_workspace_bytes, kda_prefill_backward_workspace_bytes,
-  kda_prefill_backward_ex_workspace_bytes, kda_status_string.
+  kda_prefill_backward_ex_workspace_bytes, kda_prefill_backward_gated_workspace_bytes, kda_status_string.
 The library must be built first (``__graft_entry__.build()`` or
 ``python -m linear_attention_chunkwise_gb300._build``); there is no fallback.
 """
@@ -34,6 +34,8 @@ from ._binding import (  # noqa: F401
     kda_prefill_backward,
     kda_prefill_backward_ex,
     kda_prefill_backward_ex_workspace_bytes,
+    kda_prefill_backward_gated,
+    kda_prefill_backward_gated_workspace_bytes,
     kda_prefill_backward_workspace_bytes,
     kda_prefill_ex,
     kda_prefill_min_workspace_bytes,

@@ -62,7 +62,8 @@ EXPORTED_SYMBOLS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspa
                     "kda_prefill_min_workspace_bytes", "kda_prefill", "kda_decode_step", "kda_decode_multi",
                     "kda_prefill_noalloc", "kda_prefill_snapshots", "kda_prefill_ex", "kda_decode_step_ex",
                     "kda_decode_multi_ex", "kda_prefill_backward_workspace_bytes", "kda_prefill_backward",
-                    "kda_prefill_backward_ex_workspace_bytes", "kda_prefill_backward_ex")
+                    "kda_prefill_backward_ex_workspace_bytes", "kda_prefill_backward_ex",
+                    "kda_prefill_backward_gated_workspace_bytes", "kda_prefill_backward_gated")
 
 _lock = threading.Lock()
 _lib = None
@@ -121,6 +122,11 @@ def load_library(path: str | None = None):
         lib.kda_prefill_backward_ex.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P, P,
                                                 P, P, P, P, P, P, FP, P, sz, P, P]
         lib.kda_prefill_backward_ex.restype = ctypes.c_int
+        lib.kda_prefill_backward_gated_workspace_bytes.argtypes = [ctypes.c_int, i32, i64, i32, i32, i32]
+        lib.kda_prefill_backward_gated_workspace_bytes.restype = sz
+        lib.kda_prefill_backward_gated.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, i32, i64, i32, i32, i32, P,
+                                                   P, P, P, P, P, P, P, P, P, FP, P, sz, P, P]
+        lib.kda_prefill_backward_gated.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, P, P, P]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_multi.argtypes = [P, P, P, ctypes.c_int, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P, P, P]
@@ -290,6 +296,13 @@ def kda_prefill_backward_ex_workspace_bytes(qkv_dtype, num_seqs: int, total_toke
                                                                       int(H), int(dk), int(dv)))
 
 
+def kda_prefill_backward_gated_workspace_bytes(qkv_dtype, num_seqs: int, total_tokens: int, H: int,
+                                               dk: int = 128, dv: int = 128) -> int:
+    code = qkv_dtype if isinstance(qkv_dtype, int) else _dtype_code(qkv_dtype)
+    return int(load_library().kda_prefill_backward_gated_workspace_bytes(code, int(num_seqs), int(total_tokens),
+                                                                         int(H), int(dk), int(dv)))
+
+
 def kda_prefill_backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=None, grad_S_final=None, *,
                          need_grad_S0=True, grads=None, workspace=None, device_status=None, stream=None):
     """Gradient of kda_prefill for L = <o, grad_o> + <S_final, grad_S_final> (see include/kda.h).
@@ -314,8 +327,24 @@ def kda_prefill_backward_ex(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0=Non
                      workspace, device_status, stream, fusion)
 
 
+def kda_prefill_backward_gated(q, k, v, log_alpha, beta, cu_seqlens, grad_y, S0=None, grad_S_final=None, *,
+                               fusion, need_grad_S0=True, need_grad_rms_weight=True, grads=None, workspace=None,
+                               device_status=None, stream=None):
+    """Gradient of kda_prefill_ex's gated output y = RMSNorm(o) * rms_weight * out_gate (see include/kda.h).
+
+    `fusion` must carry out_gate (and rms_weight, rms_eps as given to the forward); its prologue flags act
+    as in kda_prefill_backward_ex.  grad_y: [T, H, 128] in the dtype of q.  Returns (grad_q, grad_k,
+    grad_v, grad_log_alpha, grad_beta, grad_S0, grad_out_gate, grad_rms_weight), all fp32; grad_S0 and
+    grad_rms_weight are None when not asked for.  `grads` may pass those eight tensors in.
+    """
+    if fusion is None or fusion.out_gate is None:
+        raise ValueError("kda_prefill_backward_gated needs a fusion with out_gate")
+    return _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_y, S0, grad_S_final, need_grad_S0, grads,
+                     workspace, device_status, stream, fusion, gated=True, need_grad_w=need_grad_rms_weight)
+
+
 def _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0, grad_S_final, need_grad_S0, grads, workspace,
-              device_status, stream, fusion):
+              device_status, stream, fusion, gated=False, need_grad_w=False):
     lib = load_library()
     dev = q.device
     _check(q, "q", device=dev)
@@ -337,21 +366,33 @@ def _backward(q, k, v, log_alpha, beta, cu_seqlens, grad_o, S0, grad_S_final, ne
         grads = (torch.empty((T, H, dk), **f32), torch.empty((T, H, dk), **f32), torch.empty((T, H, dv), **f32),
                  torch.empty((T, H, dk), **f32), torch.empty((T, H), **f32),
                  torch.empty((N, H, dk, dv), **f32) if need_grad_S0 else None)
-    if len(grads) != 6:
-        raise ValueError("grads must hold six tensors (the last may be None)")
-    for t, n in zip(grads, ("grad_q", "grad_k", "grad_v", "grad_log_alpha", "grad_beta", "grad_S0")):
+        if gated:
+            grads += (torch.empty((T, H, dv), **f32), torch.empty((dv,), **f32) if need_grad_w else None)
+    names = ("grad_q", "grad_k", "grad_v", "grad_log_alpha", "grad_beta", "grad_S0") + (
+        ("grad_out_gate", "grad_rms_weight") if gated else ())
+    if len(grads) != len(names):
+        raise ValueError(f"grads must hold {len(names)} tensors")
+    for t, n in zip(grads, names):
         _check(t, n, torch.float32, dev)
     fused = fusion is not None
-    query = lib.kda_prefill_backward_ex_workspace_bytes if fused else lib.kda_prefill_backward_workspace_bytes
+    query = (lib.kda_prefill_backward_gated_workspace_bytes if gated else
+             lib.kda_prefill_backward_ex_workspace_bytes if fused else lib.kda_prefill_backward_workspace_bytes)
     need = int(query(code, N, T, H, dk, dv))
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", torch.uint8, dev)
     _check(device_status, "device_status", torch.int32, dev)
-    gq, gk, gv, gla, gb, gs0 = grads
+    gq, gk, gv, gla, gb, gs0 = grads[:6]
     args = [_ptr(q), _ptr(k), _ptr(v), code, _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens), N, T, H, dk,
             dv, _ptr(grad_o), _ptr(grad_S_final), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gla), _ptr(gb), _ptr(gs0)]
     tail = [_ptr(workspace), workspace.numel(), _ptr(device_status), _stream_handle(stream)]
+    if gated:
+        name = "kda_prefill_backward_gated"
+        fz = _check_fusion(fusion, q, T)
+        st = lib.kda_prefill_backward_gated(*args, _ptr(grads[6]), _ptr(grads[7]), ctypes.byref(fz), *tail)
+        if st != KDA_OK:
+            raise KdaError(name, st, kda_status_string(st))
+        return tuple(grads)
     if fused:
         name = "kda_prefill_backward_ex"
         fz = _check_fusion(fusion, q, T)

@@ -184,13 +184,15 @@ namespace {
 
 // Fusion options: validated copy (flags 0 when `f` is NULL).  Returns false on
 // unknown flags, a negative eps, a missing / misaligned out_gate or weight.
-bool fusion_ok(const kda_fusion* f, kda::DecodeFusion& out) {
+// `rows`: whether the call has any (token, head) rows; without them out_gate, like every other
+// zero-size array, may be NULL.
+bool fusion_ok(const kda_fusion* f, kda::DecodeFusion& out, bool rows) {
     out = kda::DecodeFusion();
     if (!f) return true;
     constexpr uint32_t known = KDA_FUSE_L2NORM_QK | KDA_FUSE_BETA_SIGMOID | KDA_FUSE_OUT_GATE;
     if (f->flags & ~known) return false;
     if (!(f->l2_eps >= 0.f) || !(f->rms_eps >= 0.f)) return false;
-    if ((f->flags & KDA_FUSE_OUT_GATE) && (!f->out_gate || !aligned(f->out_gate, 16))) return false;
+    if ((f->flags & KDA_FUSE_OUT_GATE) && ((rows && !f->out_gate) || !aligned(f->out_gate, 16))) return false;
     if (f->rms_weight && !aligned(f->rms_weight, 4)) return false;
     out.flags = f->flags;
     out.l2_eps = f->l2_eps;
@@ -214,7 +216,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
                         int32_t* device_status, kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     kda::DecodeFusion fz;
-    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
+    if (!fusion_ok(fusion, fz, total_tokens > 0)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -499,18 +501,35 @@ size_t kda_prefill_backward_ex_workspace_bytes(kda_dtype qkv_dtype, int32_t num_
     return plain == 0 ? 0 : bwd_prologue_layout(qkv_dtype, total_tokens, H, plain).total;
 }
 
+size_t kda_prefill_backward_gated_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs, int64_t total_tokens,
+                                                  int32_t H, int32_t dk, int32_t dv) {
+    const size_t ex = kda_prefill_backward_ex_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
+    return ex == 0 ? 0 : round_up(ex, kAlign) + kda::outgate_partial_bytes();
+}
+
 }  // extern "C"
 
 namespace {
 
-// The backward of kda_prefill, optionally through the fused prologue `pre` (flags 0 = plain inputs).
+// The output gate of a gated backward: grad_o is then dL/dy for y = RMSNorm(o) * rms_weight * out_gate.
+struct Gate {
+    const void* out_gate = nullptr;
+    const float* rms_weight = nullptr;  // NULL: ones
+    float rms_eps = 0.f;
+    float* grad_out_gate = nullptr;
+    float* grad_rms_weight = nullptr;  // NULL: not computed
+};
+
+// The backward of kda_prefill, optionally through the fused prologue (pre_flags 0 = plain inputs) and the
+// output gate (gate NULL = none).
 kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
                          const float* log_alpha, const float* beta, const float* S0,
                          const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
                          int32_t dk, int32_t dv, const void* grad_o, const float* grad_S_final,
                          float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
                          float* grad_beta, float* grad_S0, void* workspace, size_t workspace_bytes,
-                         int32_t* device_status, kda_stream_t stream_, uint32_t pre_flags, float l2_eps) {
+                         int32_t* device_status, kda_stream_t stream_, uint32_t pre_flags, float l2_eps,
+                         const Gate* gate = nullptr) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || total_tokens > INT32_MAX - 64) return KDA_ERR_INVALID_ARG;
@@ -518,11 +537,18 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     const size_t plain_need = kda_prefill_backward_workspace_bytes(qkv_dtype, num_seqs, total_tokens, H, dk, dv);
     if (plain_need == 0 || !sizes_ok(num_seqs, H, kHeadDim, kHeadDim * 4)) return KDA_ERR_INVALID_ARG;
     const BwdPrologueLayout pl = bwd_prologue_layout(qkv_dtype, total_tokens, H, plain_need);
-    const size_t need = pre_flags ? pl.total : plain_need;
+    const size_t gate_part = round_up(pl.total, kAlign);
+    const size_t need = gate ? gate_part + kda::outgate_partial_bytes() : pre_flags ? pl.total : plain_need;
     if (!cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
     const bool have_tokens = total_tokens > 0;
     if (have_tokens && (!q || !k || !v || !log_alpha || !beta || !grad_o || !grad_q || !grad_k || !grad_v ||
                         !grad_log_alpha || !grad_beta))
+        return KDA_ERR_INVALID_ARG;
+    if (gate && have_tokens && (!gate->out_gate || !gate->grad_out_gate || !aligned(gate->out_gate, 16) ||
+                                !aligned(gate->grad_out_gate, 16)))
+        return KDA_ERR_INVALID_ARG;
+    if (gate && ((gate->rms_weight && !aligned(gate->rms_weight, 4)) ||
+                 (gate->grad_rms_weight && !aligned(gate->grad_rms_weight, 4)) || !(gate->rms_eps >= 0.f)))
         return KDA_ERR_INVALID_ARG;
     if (have_tokens && (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
                         !aligned(beta, 4) || !aligned(grad_o, 16) || !aligned(grad_q, 16) || !aligned(grad_k, 16) ||
@@ -548,7 +574,9 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
                          range_of(cu_seqlens, static_cast<size_t>(num_seqs + 1) * 4),
                          range_of(grad_o, nqk * es),
                          range_of(grad_S_final, grad_S_final ? nst * 4 : 0),
-                         range_of(device_status, device_status ? 4 : 0)};
+                         range_of(device_status, device_status ? 4 : 0),
+                         range_of(gate ? gate->out_gate : nullptr, gate ? nqk * es : 0),
+                         range_of(gate ? gate->rms_weight : nullptr, gate && gate->rms_weight ? kHeadDim * 4 : 0)};
     const Range r_ws = range_of(workspace, need);
     const Range outs[] = {range_of(grad_q, have_tokens ? nqk * 4 : 0),
                           range_of(grad_k, have_tokens ? nqk * 4 : 0),
@@ -556,7 +584,10 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
                           range_of(grad_log_alpha, have_tokens ? nqk * 4 : 0),
                           range_of(grad_beta, have_tokens ? nb * 4 : 0),
                           range_of(grad_S0, grad_S0 ? nst * 4 : 0),
-                          r_ws};
+                          r_ws,
+                          range_of(gate ? gate->grad_out_gate : nullptr, gate && have_tokens ? nqk * 4 : 0),
+                          range_of(gate ? gate->grad_rms_weight : nullptr,
+                                   gate && gate->grad_rms_weight ? kHeadDim * 4 : 0)};
     constexpr size_t n_outs = sizeof(outs) / sizeof(outs[0]);
     for (size_t i = 0; i < n_outs; ++i) {
         for (const Range& in : ins)
@@ -605,6 +636,11 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
                                        H, dk, dv, ws + lay.o, nullptr, snap, nullptr, workspace, fwd.total, nullptr,
                                        stream_);
     if (fs != KDA_OK) return fs;
+    // 2b. output gate: dL/do over the forward's o, in place (o is dead after this), dL/dgate and dL/dweight
+    if (gate && kda::launch_bwd_outgate(f32_io, ws + lay.o, gate->out_gate, grad_o, gate->rms_weight, gate->rms_eps,
+                                        ws + lay.o, gate->grad_out_gate, gate->grad_rms_weight,
+                                        reinterpret_cast<float*>(ws + gate_part), rows, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
     // 3. prep, scan of the adjoint over chunks, value and key kernels
     kda::BackwardArgs a;
     a.q = qc;
@@ -617,7 +653,7 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     a.order = reinterpret_cast<const int32_t*>(ws);  // the prefill's schedule
     a.chunk_off = chunk_off;
     a.ckpt = ckpt;
-    a.dO = grad_o;
+    a.dO = gate ? static_cast<const void*>(ws + lay.o) : grad_o;
     a.dS_final = grad_S_final;
     a.dq = grad_q;
     a.dk = grad_k;
@@ -662,11 +698,33 @@ kda_status kda_prefill_backward_ex(const void* q, const void* k, const void* v, 
                                    float* grad_beta, float* grad_S0, const kda_fusion* fusion, void* workspace,
                                    size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
     kda::DecodeFusion fz;
-    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
+    if (!fusion_ok(fusion, fz, total_tokens > 0)) return KDA_ERR_INVALID_ARG;
     if (fz.flags & KDA_FUSE_OUT_GATE) return KDA_ERR_UNSUPPORTED;
     return backward_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
                          grad_o, grad_S_final, grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0, workspace,
                          workspace_bytes, device_status, stream, fz.flags, fz.l2_eps);
+}
+
+kda_status kda_prefill_backward_gated(const void* q, const void* k, const void* v, kda_dtype qkv_dtype,
+                                      const float* log_alpha, const float* beta, const float* S0,
+                                      const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H,
+                                      int32_t dk, int32_t dv, const void* grad_y, const float* grad_S_final,
+                                      float* grad_q, float* grad_k, float* grad_v, float* grad_log_alpha,
+                                      float* grad_beta, float* grad_S0, float* grad_out_gate,
+                                      float* grad_rms_weight, const kda_fusion* fusion, void* workspace,
+                                      size_t workspace_bytes, int32_t* device_status, kda_stream_t stream) {
+    kda::DecodeFusion fz;
+    if (!fusion || !fusion_ok(fusion, fz, total_tokens > 0) || !(fz.flags & KDA_FUSE_OUT_GATE))
+        return KDA_ERR_INVALID_ARG;
+    Gate g;
+    g.out_gate = fz.out_gate;
+    g.rms_weight = fz.rms_weight;
+    g.rms_eps = fz.rms_eps;
+    g.grad_out_gate = grad_out_gate;
+    g.grad_rms_weight = grad_rms_weight;
+    return backward_impl(q, k, v, qkv_dtype, log_alpha, beta, S0, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
+                         grad_y, grad_S_final, grad_q, grad_k, grad_v, grad_log_alpha, grad_beta, grad_S0, workspace,
+                         workspace_bytes, device_status, stream, fz.flags & ~KDA_FUSE_OUT_GATE, fz.l2_eps, &g);
 }
 
 }  // extern "C"
@@ -679,7 +737,7 @@ kda_status decode_impl(const void* q, const void* k, const void* v, kda_dtype qk
                        kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     kda::DecodeFusion fz;
-    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
+    if (!fusion_ok(fusion, fz, N > 0)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (N < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
@@ -751,7 +809,7 @@ kda_status decode_multi_impl(const void* q, const void* k, const void* v, kda_dt
                              kda_stream_t stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     kda::DecodeFusion fz;
-    if (!fusion_ok(fusion, fz)) return KDA_ERR_INVALID_ARG;
+    if (!fusion_ok(fusion, fz, N > 0 && T > 0)) return KDA_ERR_INVALID_ARG;
     if (qkv_dtype != KDA_DTYPE_BF16 && qkv_dtype != KDA_DTYPE_F32) return KDA_ERR_UNSUPPORTED;
     if (N < 0 || T < 0 || H <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
     if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;

@@ -832,6 +832,72 @@ __global__ void kda_bwd_epilogue_kernel(const IoT* __restrict__ q, const IoT* __
     }
 }
 
+// ============================================================== output gate ==
+// kda_prefill_backward_gated: the output gate of "kimi delta attn from first principles" (aryagxr),
+// "KDA has three gates", y = o r w g with r = (sum_j o_j^2 / 128 + eps)^(-1/2), differentiated for
+// L = <y, dY>:
+//   do_m = r w_m g_m dY_m - (r^3 o_m / 128) sum_j dY_j o_j w_j g_j,   dg_j = dY_j o_j r w_j,
+//   dw_j = sum over (token, head) rows of dY_j o_j r g_j.
+// One warp per (token, head) row, 4 channels per lane, rows grid-strided over a fixed grid so that
+// dw's per-block partial sums (and their fixed-order sum in kda_bwd_outgate_sum_kernel) are
+// bitwise repeatable.  do is written in the input dtype (the chunkwise backward reads dO in it); it may
+// overwrite o in place, since each warp holds its whole row in registers before it stores.
+constexpr int kGateBlocks = 592;  // 4 x 148 blocks of 8 warps
+
+template <typename IoT>
+__global__ void __launch_bounds__(256) kda_bwd_outgate_kernel(const IoT* o, const IoT* __restrict__ g,
+                                                              const IoT* __restrict__ dy,
+                                                              const float* __restrict__ w, float eps,
+                                                              IoT* dout, float* __restrict__ dg,
+                                                              float* __restrict__ dw_part, int64_t rows) {
+    __shared__ float4 part[8][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 wv = w ? make_float4(w[4 * lane], w[4 * lane + 1], w[4 * lane + 2], w[4 * lane + 3])
+                        : make_float4(1.f, 1.f, 1.f, 1.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp; row < rows;
+         row += static_cast<int64_t>(gridDim.x) * 8) {
+        const size_t off = static_cast<size_t>(row) * D + 4 * lane;
+        const float4 ov = ld4(o + off), gv = ld4(g + off), yv = ld4(dy + off);
+        const float4 a = make_float4(wv.x * gv.x * yv.x, wv.y * gv.y * yv.y, wv.z * gv.z * yv.z, wv.w * gv.w * yv.w);
+        float ss = ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w;
+        float dot = a.x * ov.x + a.y * ov.y + a.z * ov.z + a.w * ov.w;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+            dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+        }
+        const float r = rsqrtf(ss * (1.f / D) + eps);
+        const float c = r * r * r * (1.f / D) * dot;
+        st4(dout + off, make_float4(r * a.x - c * ov.x, r * a.y - c * ov.y, r * a.z - c * ov.z, r * a.w - c * ov.w));
+        *reinterpret_cast<float4*>(dg + off) =
+            make_float4(yv.x * ov.x * r * wv.x, yv.y * ov.y * r * wv.y, yv.z * ov.z * r * wv.z, yv.w * ov.w * r * wv.w);
+        acc.x = fmaf(yv.x * ov.x, r * gv.x, acc.x);
+        acc.y = fmaf(yv.y * ov.y, r * gv.y, acc.y);
+        acc.z = fmaf(yv.z * ov.z, r * gv.z, acc.z);
+        acc.w = fmaf(yv.w * ov.w, r * gv.w, acc.w);
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = part[0][lane];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            const float4 u = part[i][lane];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        *reinterpret_cast<float4*>(dw_part + static_cast<size_t>(blockIdx.x) * D + 4 * lane) = t;
+    }
+}
+
+// dw = the sum of the per-block partials, in block order (one thread per channel).
+__global__ void kda_bwd_outgate_sum_kernel(const float* __restrict__ dw_part, int nparts, float* __restrict__ dw) {
+    const int c = threadIdx.x;
+    float t = 0.f;
+    for (int b = 0; b < nparts; ++b) t += dw_part[static_cast<size_t>(b) * D + c];
+    dw[c] = t;
+}
+
 // Snapshot entries for every chunk end of every sequence: entry chunk_off[n] + c - 1 is the state
 // after chunk c - 1 of sequence n (c = 1 .. nch_n; the last is the final state).  Entries past the
 // batch's chunk count are sentinels (sequence N) that no scan CTA takes.
@@ -920,6 +986,29 @@ cudaError_t launch_bwd_epilogue(bool f32_io, const void* q, const void* k, const
         kda_bwd_epilogue_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), bh, inv, dq, dk, dbeta,
             rows, flags);
+    return cudaGetLastError();
+}
+
+size_t outgate_partial_bytes() { return static_cast<size_t>(kGateBlocks) * D * 4; }
+
+cudaError_t launch_bwd_outgate(bool f32_io, const void* o, const void* g, const void* dy, const float* w, float eps,
+                               void* dout, float* dg, float* dw, float* dw_part, int64_t rows, cudaStream_t stream) {
+    if (rows > 0) {
+        if (f32_io)
+            kda_bwd_outgate_kernel<float><<<kGateBlocks, 256, 0, stream>>>(
+                static_cast<const float*>(o), static_cast<const float*>(g), static_cast<const float*>(dy), w, eps,
+                static_cast<float*>(dout), dg, dw_part, rows);
+        else
+            kda_bwd_outgate_kernel<__nv_bfloat16><<<kGateBlocks, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(g),
+                static_cast<const __nv_bfloat16*>(dy), w, eps, static_cast<__nv_bfloat16*>(dout), dg, dw_part, rows);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    if (dw) {
+        if (rows > 0) kda_bwd_outgate_sum_kernel<<<1, D, 0, stream>>>(dw_part, kGateBlocks, dw);
+        else if (cudaMemsetAsync(dw, 0, D * sizeof(float), stream) != cudaSuccess) return cudaGetLastError();
+    }
     return cudaGetLastError();
 }
 

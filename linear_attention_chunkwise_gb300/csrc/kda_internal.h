@@ -140,6 +140,12 @@ cudaError_t launch_bwd_prologue(bool f32_io, const void* q, const void* k, const
 cudaError_t launch_bwd_epilogue(bool f32_io, const void* q, const void* k, const float* bh, const float* inv,
                                 float* dq, float* dk, float* dbeta, int64_t rows, uint32_t flags,
                                 cudaStream_t stream);
+// Backward of the output gate y = RMSNorm(o) * w * g for one grad_y (dy): dout = dL/do in the input dtype,
+// dg = dL/dg fp32 [rows, 128], dw = dL/dw fp32 [128] (NULL: not computed) summed in a fixed order
+// through dw_part (outgate_partial_bytes() of workspace).  w NULL means ones.
+size_t outgate_partial_bytes();
+cudaError_t launch_bwd_outgate(bool f32_io, const void* o, const void* g, const void* dy, const float* w, float eps,
+                               void* dout, float* dg, float* dw, float* dw_part, int64_t rows, cudaStream_t stream);
 // prep, scan, value and key kernels; chunk_slots bounds the batch's chunk count.
 cudaError_t launch_backward(const BackwardArgs& a, bool f32_io, int64_t chunk_slots, cudaStream_t stream);
 

@@ -323,7 +323,7 @@ PLAIN_BWD_WS = 128 * 2 * 128 * 64  # offset of the workspace in the fake layout 
     (dict(flags=0x8), {}, kda.KDA_ERR_INVALID_ARG),                                    # unknown flag
     (dict(flags=kda.KDA_FUSE_L2NORM_QK, l2_eps=-1.0), {}, kda.KDA_ERR_INVALID_ARG),     # negative eps
     (dict(flags=kda.KDA_FUSE_OUT_GATE), {}, kda.KDA_ERR_INVALID_ARG),                   # gate missing
-    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GATE), {}, kda.KDA_ERR_UNSUPPORTED),           # gate's backward not built
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GATE), {}, kda.KDA_ERR_UNSUPPORTED),           # kda_prefill_backward_gated's
     (dict(flags=kda.KDA_FUSE_L2NORM_QK | kda.KDA_FUSE_BETA_SIGMOID), dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
     (dict(flags=kda.KDA_FUSE_BETA_SIGMOID), dict(gq=BASE + 2 * 128 * 2 * 128), kda.KDA_ERR_INVALID_ARG),  # = k
 ])
@@ -343,3 +343,83 @@ def test_backward_ex_workspace_covers_the_prologue_copies(lib):
     # and the call stops only at the device check (no GPU here)
     for none in (None, _fusion(flags=0)):
         assert _backward_ex(lib, none, gs0=in_tail, wsb=plain) == kda.KDA_ERR_CUDA
+
+
+def test_backward_gated_workspace_bytes(lib):
+    # the _ex workspace rounded up to 256 bytes, then 592 blocks x 128 fp32 partial sums of dL/dweight
+    up = lambda x: -(-x // 256) * 256
+    for dt in (kda.KDA_DTYPE_BF16, kda.KDA_DTYPE_F32):
+        for T, H, N in ((128, 2, 1), (1000, 32, 16), (0, 4, 3)):
+            ex = kda.kda_prefill_backward_ex_workspace_bytes(dt, N, T, H)
+            assert kda.kda_prefill_backward_gated_workspace_bytes(dt, N, T, H) == up(ex) + 592 * 128 * 4
+    assert kda.kda_prefill_backward_gated_workspace_bytes(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
+    assert kda.kda_prefill_backward_gated_workspace_bytes(kda.KDA_DTYPE_BF16, 1, 10, 2, 128, 64) == 0
+
+
+GTOK = 128 * 2 * 128  # elements per [T, H, 128] tensor of the fake gated layout below
+
+
+def _backward_gated(lib, fz, **over):
+    T, H, N = 128, 2, 1
+    tok = GTOK
+    need = kda.kda_prefill_backward_gated_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H)
+    a = dict(q=BASE, k=BASE + 2 * tok, v=BASE + 4 * tok, dtype=0, la=BASE + 6 * tok, beta=BASE + 10 * tok,
+             S0=None, cu=BASE + 11 * tok, N=N, T=T, H=H, dk=128, dv=128, dY=BASE + 12 * tok, dSf=None,
+             gq=BASE + 20 * tok, gk=BASE + 24 * tok, gv=BASE + 28 * tok, gla=BASE + 32 * tok, gb=BASE + 36 * tok,
+             gs0=BASE + 40 * tok, gg=BASE + 52 * tok, gw=BASE + 58 * tok, ws=BASE + 64 * tok, wsb=need,
+             status=None)
+    a.update(over)
+    P = lambda x: None if x is None else _fake(x)
+    return lib.kda_prefill_backward_gated(
+        P(a["q"]), P(a["k"]), P(a["v"]), a["dtype"], P(a["la"]), P(a["beta"]), P(a["S0"]), P(a["cu"]), a["N"],
+        a["T"], a["H"], a["dk"], a["dv"], P(a["dY"]), P(a["dSf"]), P(a["gq"]), P(a["gk"]), P(a["gv"]), P(a["gla"]),
+        P(a["gb"]), P(a["gs0"]), P(a["gg"]), P(a["gw"]), None if fz is None else ctypes.byref(fz), P(a["ws"]),
+        a["wsb"], P(a["status"]), None)
+
+
+GGATE = BASE + 48 * GTOK      # bf16 [T, H, 128]: [48, 50) x GTOK bytes
+GWEIGHT = BASE + 60 * GTOK    # fp32 [128]
+
+
+@pytest.mark.parametrize("fz,over,expect", [
+    (None, {}, kda.KDA_ERR_INVALID_ARG),                                                       # no fusion
+    (dict(flags=kda.KDA_FUSE_L2NORM_QK), {}, kda.KDA_ERR_INVALID_ARG),                          # no gate flag
+    (dict(flags=kda.KDA_FUSE_OUT_GATE), {}, kda.KDA_ERR_INVALID_ARG),                           # gate missing
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE, rms_eps=-1.0), {}, kda.KDA_ERR_INVALID_ARG),    # negative eps
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gg=None), kda.KDA_ERR_INVALID_ARG),       # no grad_out_gate
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gg=BASE + 52 * GTOK + 4), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gg=GGATE), kda.KDA_ERR_INVALID_ARG),      # = out_gate
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gg=BASE + 12 * GTOK), kda.KDA_ERR_INVALID_ARG),  # = grad_y
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE, w=GWEIGHT), dict(gw=GWEIGHT), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gw=BASE + 54 * GTOK), kda.KDA_ERR_INVALID_ARG),  # in dgate
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(gw=BASE + 58 * GTOK + 2), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(dk=64), kda.KDA_ERR_UNSUPPORTED),
+    (dict(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE), dict(dtype=5), kda.KDA_ERR_UNSUPPORTED),
+])
+def test_backward_gated_rejects_bad_arguments(lib, fz, over, expect):
+    assert _backward_gated(lib, None if fz is None else _fusion(**fz), **over) == expect
+
+
+def test_backward_gated_workspace_covers_the_partials(lib):
+    """The _ex figure is too small, and the partial sums' tail is checked for overlap; a call that passes
+    every argument check stops at the device check (no GPU here)."""
+    N, T, H = 1, 128, 2
+    ex = kda.kda_prefill_backward_ex_workspace_bytes(kda.KDA_DTYPE_BF16, N, T, H)
+    fz = _fusion(flags=kda.KDA_FUSE_OUT_GATE, g=GGATE, w=GWEIGHT)
+    assert _backward_gated(lib, fz, wsb=ex) == kda.KDA_ERR_WORKSPACE
+    ws = BASE + 64 * GTOK
+    assert _backward_gated(lib, fz, gw=ws + -(-ex // 256) * 256 + 4096) == kda.KDA_ERR_INVALID_ARG
+    assert _backward_gated(lib, fz) == kda.KDA_ERR_CUDA
+    assert _backward_gated(lib, fz, gw=None) == kda.KDA_ERR_CUDA
+    fz2 = _fusion(flags=kda.KDA_FUSE_OUT_GATE | kda.KDA_FUSE_L2NORM_QK | kda.KDA_FUSE_BETA_SIGMOID, g=GGATE)
+    assert _backward_gated(lib, fz2) == kda.KDA_ERR_CUDA
+
+
+def test_out_gate_may_be_null_without_tokens(lib):
+    """With no (token, head) rows the gate, like every zero-size array, may be NULL: the call passes every
+    argument check and stops at the device check (no GPU here); with tokens it is required."""
+    fz = _fusion(flags=kda.KDA_FUSE_OUT_GATE)
+    empty = dict(T=0, q=None, k=None, v=None, la=None, beta=None, dY=None, gq=None, gk=None, gv=None, gla=None,
+                 gb=None, gg=None)
+    assert _backward_gated(lib, fz, **empty) == kda.KDA_ERR_CUDA
+    assert _backward_gated(lib, fz) == kda.KDA_ERR_INVALID_ARG

@@ -7,7 +7,11 @@ Here the CUDA path is compared with it element by element, all six gradients
 varlen batches with empty, one-token and ragged sequences; several head
 counts; fp32 and bf16 inputs; no grad_S_final; bitwise repeatability; and the
 8k-token 32-head workload on two sampled heads (heads are independent, so the oracle on
-those heads alone gives their exact gradients).
+those heads alone gives their exact gradients).  The same for the backward through
+the fused prologue (kda_prefill_backward_ex) and through the output gate
+(kda_prefill_backward_gated: eight gradients, the gate's and the RMSNorm weight's
+included, against oracle.kda_prefill_backward_gated, itself pinned by finite
+differences in tests/test_oracle_gate_pins.py).
 """
 import numpy as np
 import pytest
@@ -226,3 +230,109 @@ def test_backward_ex_rejects_the_output_gate():
     with pytest.raises(kda.KdaError) as e:
         kda.kda_prefill_backward_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, p.S0, fusion=fz)
     assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- output gate --
+RMS_EPS = 1e-5
+GATED_NAMES = NAMES + ("out_gate", "rms_weight")
+
+
+def _gate(p, seed, weight=True):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    T, H, d = p.q.shape
+    gate = torch.randn((T, H, d), generator=g, device="cuda").to(p.q.dtype)
+    w = (1.0 + 0.5 * torch.randn(d, generator=g, device="cuda")) if weight else None
+    return gate, w
+
+
+def _gated_oracle(p, dY, dSf, gate, w, l2norm_qk, beta_sigmoid, heads=None):
+    """Oracle gradients of the gated output; w None is passed as ones so that dL/dweight comes back."""
+    hidx = torch.arange(p.q.shape[1], device="cuda") if heads is None else torch.tensor(heads, device="cuda")
+    sel = lambda t: None if t is None else host(t.index_select(1, hidx))
+    return oracle.kda_prefill_backward_gated(sel(p.q), sel(p.k), sel(p.v), sel(p.log_alpha), sel(p.beta),
+                                             p.cu_seqlens.cpu().numpy(), sel(p.S0), sel(dY), sel(dSf), sel(gate),
+                                             np.ones(128) if w is None else host(w), RMS_EPS, l2norm_qk=l2norm_qk,
+                                             beta_sigmoid=beta_sigmoid, l2_eps=L2_EPS)
+
+
+def _compare_gated(got, ref, heads=None, tol=TOL, with_dw=True):
+    _compare(got[:6], ref[:6], heads, tol)
+    g = host(got[6] if heads is None else got[6].index_select(1, torch.tensor(heads, device=got[6].device)))
+    assert np.all(np.isfinite(g))
+    assert rell2(g, ref[6]) <= tol, ("out_gate", rell2(g, ref[6]))
+    if with_dw:
+        assert rell2(host(got[7]), ref[7]) <= tol, ("rms_weight", rell2(host(got[7]), ref[7]))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_backward_gated_matches_oracle(dtype):
+    """Prologue and output gate together, varlen with empty, one-token and ragged sequences."""
+    p = _raw([300, 0, 64, 1, 129, 200], H=2, dtype=dtype, seed=71)
+    dY, dSf = _cotangents(p, 72)
+    gate, w = _gate(p, 73)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS, out_gate=gate, rms_weight=w, rms_eps=RMS_EPS)
+    got = kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dY, p.S0, dSf,
+                                         fusion=fz, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _compare_gated(got, _gated_oracle(p, dY, dSf, gate, w, True, True))
+
+
+def test_backward_gated_plain_inputs_unit_weight():
+    """Output gate alone (q, k unit-norm, beta in (0, 1)), rms_weight NULL = ones, no grad_S_final."""
+    p = synth.prefill_inputs([190, 70, 5], H=3, s0_std=0.02, seed=74)
+    dY, _ = _cotangents(p, 75, with_final=False)
+    gate, _ = _gate(p, 76, weight=False)
+    fz = kda.Fusion(out_gate=gate, rms_eps=RMS_EPS)
+    got = kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dY, p.S0, None,
+                                         fusion=fz)
+    torch.cuda.synchronize()
+    _compare_gated(got, _gated_oracle(p, dY, None, gate, None, False, False))
+
+
+def test_backward_gated_is_deterministic_and_skips_weight():
+    p = _raw([500, 77], H=4, dtype=torch.bfloat16, seed=77)
+    dY, dSf = _cotangents(p, 78)
+    gate, w = _gate(p, 79)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS, out_gate=gate, rms_weight=w, rms_eps=RMS_EPS)
+    run = lambda need_w: kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dY,
+                                                        p.S0, dSf, fusion=fz, need_grad_rms_weight=need_w)
+    a, b, c = run(True), run(True), run(False)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert c[7] is None
+    for x, y in zip(a[:7], c[:7]):
+        assert torch.equal(x, y)
+
+
+def test_backward_gated_no_tokens():
+    """No tokens: the gate's gradients are empty, dL/dweight is zero, grad_S0 is grad_S_final carried back."""
+    p = synth.prefill_inputs([0, 0], H=2, s0_std=0.02, seed=80)
+    dY = torch.empty((0, 2, 128), dtype=p.q.dtype, device="cuda")
+    dSf = torch.randn((2, 2, 128, 128), device="cuda")
+    gate = torch.empty((0, 2, 128), dtype=p.q.dtype, device="cuda")  # NULL pointer: allowed without tokens
+    w = torch.ones(128, device="cuda")
+    fz = kda.Fusion(out_gate=gate, rms_weight=w, rms_eps=RMS_EPS)
+    got = kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dY, p.S0, dSf,
+                                         fusion=fz)
+    torch.cuda.synchronize()
+    assert got[6].numel() == 0
+    assert torch.equal(got[7], torch.zeros(128, device="cuda"))
+    assert torch.equal(got[5], dSf)
+
+
+def test_backward_gated_8k_sampled_heads():
+    """The 8192-token, 32-head bf16 workload with prologue and gate; heads 0 and 31 against the oracle
+    (dL/dweight sums over every head, so it is checked on the 4-head case above, not here)."""
+    p = _raw([8192], H=32, dtype=torch.bfloat16, seed=81)
+    dY, dSf = _cotangents(p, 82)
+    gate, w = _gate(p, 83)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS, out_gate=gate, rms_weight=w, rms_eps=RMS_EPS)
+    got = kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dY, p.S0, dSf,
+                                         fusion=fz)
+    torch.cuda.synchronize()
+    heads = [0, 31]
+    _compare_gated(got, _gated_oracle(p, dY, dSf, gate, w, True, True, heads), heads, with_dw=False)
