@@ -28,30 +28,6 @@ namespace pf {
 constexpr int C = kChunk;    // 64
 constexpr int D = kHeadDim;  // 128
 constexpr int NT = 256;      // threads per CTA
-// Bounded waits.  A pipeline wait (for a copy or MMA the next step needs) gives up after
-// KDA_PIPE_WAIT_CYCLES; the kernel then reports KDA_DEV_TIMEOUT and winds down.  Before anything
-// reuses the buffers of the operation it gave up on, and before the CTA releases TMEM or shared
-// memory, it waits for that operation again with kDrainLimit, so no copy or MMA of its own is
-// abandoned in flight.  (A test build sets KDA_PIPE_WAIT_CYCLES to 0 to exercise the wind-down.)
-#ifndef KDA_PIPE_WAIT_CYCLES
-#define KDA_PIPE_WAIT_CYCLES 4000000000LL
-#endif
-constexpr long long kWaitLimit = KDA_PIPE_WAIT_CYCLES;  // ~2 s of SM clock by default
-constexpr long long kDrainLimit = 4000000000LL;          // ~2 s of SM clock
-
-// A pipeline wait that, when it expires, waits for the same phase again with the drain limit
-// (the operation the caller depends on has then landed); returns false when the pipeline limit
-// expired.  With a pipeline limit of 0 the first poll does not suspend the thread (try_wait may
-// sleep until the phase completes), so every phase not already complete counts as expired.
-__device__ __forceinline__ bool mbar_wait_pipe(uint64_t* bar, uint32_t parity) {
-    if constexpr (kWaitLimit == 0) {
-        if (mbar_test(bar, parity)) return true;
-    } else {
-        if (mbar_wait(bar, parity, kWaitLimit)) return true;
-    }
-    (void)mbar_wait(bar, parity, kDrainLimit);
-    return false;
-}
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint32_t tmem_lane(int quarter) { return static_cast<uint32_t>(32 * quarter) << 16; }

@@ -39,14 +39,7 @@ constexpr uint32_t kBlobM = 57344;      // M
 constexpr uint32_t kBlobEv = 65536;     // exp(gm) | exp(gC) | exp(gC - gm), f32 [3][128]
 static_assert(kBlobEv + 1536 == kPrefillBlobBytes, "blob layout");
 
-// ---- bulk copies (non-tensor), 16-byte aligned, sizes multiple of 16 ----
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
+// ---- bulk copy shared -> global (non-tensor), 16-byte aligned, sizes multiple of 16 ----
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
                  "r"(smem_u32(src)), "r"(bytes)

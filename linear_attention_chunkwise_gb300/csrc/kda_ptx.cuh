@@ -66,6 +66,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     return true;
 }
 
+// Bounded waits.  A pipeline wait (for a copy or MMA the next step needs) gives up after
+// KDA_PIPE_WAIT_CYCLES; the kernel then reports KDA_DEV_TIMEOUT and winds down.  Before anything
+// reuses the buffers of the operation it gave up on, and before the CTA releases TMEM or shared
+// memory, it waits for that operation again with kDrainLimit, so no copy or MMA of its own is
+// abandoned in flight.  (A test build sets KDA_PIPE_WAIT_CYCLES to 0 to exercise the wind-down.)
+#ifndef KDA_PIPE_WAIT_CYCLES
+#define KDA_PIPE_WAIT_CYCLES 4000000000LL
+#endif
+constexpr long long kWaitLimit = KDA_PIPE_WAIT_CYCLES;  // ~2 s of SM clock by default
+constexpr long long kDrainLimit = 4000000000LL;          // ~2 s of SM clock
+
+// A pipeline wait that, when it expires, waits for the same phase again with the drain limit
+// (the operation the caller depends on has then landed); returns false when the pipeline limit
+// expired.  With a pipeline limit of 0 the first poll does not suspend the thread (try_wait may
+// sleep until the phase completes), so every phase not already complete counts as expired.
+__device__ __forceinline__ bool mbar_wait_pipe(uint64_t* bar, uint32_t parity) {
+    if constexpr (kWaitLimit == 0) {
+        if (mbar_test(bar, parity)) return true;
+    } else {
+        if (mbar_wait(bar, parity, kWaitLimit)) return true;
+    }
+    (void)mbar_wait(bar, parity, kDrainLimit);
+    return false;
+}
 // ------------------------------------------------------------------ TMA ----
 // 3-D tiled load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
@@ -74,6 +98,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, size a multiple of 16),
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

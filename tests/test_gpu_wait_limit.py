@@ -86,3 +86,32 @@ def test_expired_waits_in_the_cluster_output_gate(wait_lib):
     assert rc == kda.KDA_OK
     assert status & kda.KDA_DEV_TIMEOUT
     _check_normal_call(p)
+
+
+def test_expired_wait_in_the_multi_token_decode(wait_lib):
+    """The multi-token decode waits (bounded) for the bulk copy of each unit's state; its first wait
+    follows the copy's issue at once, so with the zero limit it expires, the CTA drains that copy and
+    returns with KDA_DEV_TIMEOUT.  A normal call afterwards matches the oracle."""
+    import numpy as np
+    import oracle
+    N, H, T = 64, 4, 3
+    d = synth.decode_inputs(N, H, T, seed=813, device="cuda")
+    tm = lambda x: x.transpose(0, 1).contiguous()
+    q, k, v, la, b = tm(d.q), tm(d.k), tm(d.v), tm(d.log_alpha), tm(d.beta)
+    S = d.S.clone()
+    o = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = wait_lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), kda.KDA_DTYPE_BF16, _ptr(la), _ptr(b), _ptr(S), N,
+                                   None, N, T, H, 128, 128, _ptr(o), None, _ptr(status), stream)
+    torch.cuda.synchronize()
+    assert rc == kda.KDA_OK
+    assert int(status.item()) & kda.KDA_DEV_TIMEOUT
+    S = d.S.clone()
+    S_ref = host(S).astype(np.float64)
+    o_ref = np.stack([oracle.kda_decode_step(host(d.q[t]), host(d.k[t]), host(d.v[t]), host(d.log_alpha[t]),
+                                             host(d.beta[t]), S_ref, None) for t in range(T)], axis=1)
+    o = kda.kda_decode_multi(q, k, v, la, b, S, None)
+    torch.cuda.synchronize()
+    assert rell2(host(o), o_ref) < TOL
+    assert rell2(host(S), S_ref) < 1e-5
