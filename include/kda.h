@@ -77,6 +77,9 @@ typedef enum {
 #define KDA_DEV_BAD_SLOT 0x2        /* state_indices entry outside [0, num_slots) */
 #define KDA_DEV_TIMEOUT 0x4         /* an on-chip wait hit its iteration limit */
 #define KDA_DEV_BAD_SNAPSHOT 0x8    /* kda_prefill_snapshots: a (sequence, position) entry is invalid */
+#define KDA_DEV_BOUNDS 0x10         /* only in a library built with KDA_DEBUG_BOUNDS: a kernel derived a
+                                       sequence, chunk, token or snapshot range outside its buffer and
+                                       skipped that work (never set by a release build) */
 
 /*
  * Fused prologue / epilogue (kda_prefill_ex, kda_decode_step_ex,

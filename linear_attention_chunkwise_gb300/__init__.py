@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     KDA_DEV_BAD_CU_SEQLENS,
     KDA_DEV_BAD_SLOT,
     KDA_DEV_BAD_SNAPSHOT,
+    KDA_DEV_BOUNDS,
     KDA_DEV_TIMEOUT,
     KDA_DTYPE_BF16,
     KDA_DTYPE_F32,

@@ -27,6 +27,7 @@ KDA_DEV_BAD_CU_SEQLENS = 0x1
 KDA_DEV_BAD_SLOT = 0x2
 KDA_DEV_TIMEOUT = 0x4
 KDA_DEV_BAD_SNAPSHOT = 0x8
+KDA_DEV_BOUNDS = 0x10  # only from a library built with KDA_DEBUG_BOUNDS
 KDA_FUSE_L2NORM_QK = 0x1
 KDA_FUSE_BETA_SIGMOID = 0x2
 KDA_FUSE_OUT_GATE = 0x4

@@ -340,6 +340,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     a.order = order;
     a.chunk_off = two_pass ? reinterpret_cast<const int32_t*>(ws + two.table) : nullptr;
     a.blobs = two_pass ? ws + two.blobs : nullptr;
+    a.blob_units = two_pass ? static_cast<int64_t>(max_chunks(num_seqs, total_tokens)) * H : 0;
     a.o = o;
     a.S_final = S_final;
     a.device_status = device_status;
@@ -624,7 +625,7 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, chunk_off, device_status, nullptr, nullptr, 0,
                                 stream) != cudaSuccess ||
         kda::launch_ckpt_entries(cu_seqlens, chunk_off, num_seqs, static_cast<int32_t>(lay.entries), snap_seq,
-                                 snap_pos, stream) != cudaSuccess)
+                                 snap_pos, device_status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     // 2. the chunkwise prefill records those states (its own table pass rebuilds the same chunk table)
     Snapshots snap;
@@ -664,6 +665,9 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     a.rec = reinterpret_cast<float*>(ws + fwd.copies);  // the forward's copies and images are dead now
     a.xbuf = reinterpret_cast<float*>(ws + lay.xbuf);
     a.u_scratch = grad_q;
+    a.device_status = device_status;
+    a.total_tokens = total_tokens;
+    a.chunk_slots = lay.entries;
     a.num_seqs = num_seqs;
     a.H = H;
     if (kda::launch_backward(a, f32_io, lay.entries, stream) != cudaSuccess) return KDA_ERR_CUDA;

@@ -238,7 +238,9 @@ __device__ __forceinline__ bool chunk_pos(const BackwardArgs& a, int gc, ChunkPo
     p.c = gc - a.chunk_off[p.n];
     p.t0 = static_cast<int64_t>(a.cu_seqlens[p.n]) + static_cast<int64_t>(p.c) * C;
     p.L = static_cast<int>(a.cu_seqlens[p.n + 1] - p.t0 < C ? a.cu_seqlens[p.n + 1] - p.t0 : C);
-    return true;
+    return KDA_BOUNDS(p.n >= 0 && p.n < a.num_seqs && p.c >= 0 && gc < a.chunk_slots && p.t0 >= 0 && p.L >= 1 &&
+                          p.t0 + p.L <= a.total_tokens,
+                      a.device_status);
 }
 // state at the start of chunk (n, c): S0 (or zero) for the first chunk, else the snapshot after chunk c-1
 __device__ __forceinline__ const float* chunk_start_state(const BackwardArgs& a, const ChunkPos& p, int gc, int h) {
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
     if (a.chunk_off[N + 1] == 0) return;
     const int unit = blockIdx.x;  // (rank of the sequence, longest first) x H x slices
     const int n = a.order[unit / (H * kSlices)], h = (unit / kSlices) % H, c0 = (unit % kSlices) * NCS;
+    if (!KDA_BOUNDS(n >= 0 && n < N && h < H, a.device_status)) return;
     float *XS = sm + L::XS, *DY = sm + L::DY;
     const size_t sidx = (static_cast<size_t>(n) * H + h) * D * D;
     // X rows 16 warp + g (+8), columns 8 j + 2 t (+1) of this CTA's slice
@@ -422,6 +425,11 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
             X[j][e] = a.dS_final ? a.dS_final[sidx + frow(16 * warp, lane, e) * D + c0 + fcol(0, lane, j, e)] : 0.f;
     const int base = a.chunk_off[n], nch = a.chunk_off[n + 1] - base;
     const int64_t tb = a.cu_seqlens[n], te = a.cu_seqlens[n + 1];
+    if (!KDA_BOUNDS(base >= 0 && nch >= 0 && base + nch <= a.chunk_slots && tb >= 0 && te >= tb &&
+                        te <= a.total_tokens && static_cast<int64_t>(nch) * C >= te - tb &&
+                        static_cast<int64_t>(nch) * C < te - tb + C,
+                    a.device_status))
+        return;
     auto rec_of = [&](int c) { return a.rec + (static_cast<size_t>(base + c) * H + h) * kRecFloats; };
     if (nch > 0) scan_fetch(sm, rec_of(nch - 1), c0, tid);
     cp_commit();
@@ -903,7 +911,8 @@ __global__ void kda_bwd_outgate_sum_kernel(const float* __restrict__ dw_part, in
 // batch's chunk count are sentinels (sequence N) that no scan CTA takes.
 __global__ void kda_ckpt_entries_kernel(const int32_t* __restrict__ cu_seqlens,
                                         const int32_t* __restrict__ chunk_off, int32_t N, int32_t max_entries,
-                                        int32_t* __restrict__ snap_seq, int32_t* __restrict__ snap_pos) {
+                                        int32_t* __restrict__ snap_seq, int32_t* __restrict__ snap_pos,
+                                        int32_t* device_status) {
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n > N) return;
     const bool valid = chunk_off[N + 1] != 0;
@@ -917,6 +926,7 @@ __global__ void kda_ckpt_entries_kernel(const int32_t* __restrict__ cu_seqlens,
     if (!valid) return;
     const int len = cu_seqlens[n + 1] - cu_seqlens[n];
     const int base = chunk_off[n], nch = chunk_off[n + 1] - base;
+    if (!KDA_BOUNDS(base >= 0 && nch >= 0 && base + nch <= max_entries, device_status)) return;
     for (int c = 1; c <= nch; ++c) {
         snap_seq[base + c - 1] = n;
         snap_pos[base + c - 1] = min(c * C, len);
@@ -951,10 +961,10 @@ cudaError_t launch_all(const BackwardArgs& a, int64_t chunk_slots, cudaStream_t 
 size_t backward_record_bytes() { return static_cast<size_t>(kRecFloats) * 4; }
 
 cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_off, int32_t N, int32_t max_entries,
-                                int32_t* snap_seq, int32_t* snap_pos, cudaStream_t stream) {
+                                int32_t* snap_seq, int32_t* snap_pos, int32_t* device_status, cudaStream_t stream) {
     const int threads = 128, blocks = (N + 1 + threads - 1) / threads;
     kda_ckpt_entries_kernel<<<blocks, threads, 0, stream>>>(cu_seqlens, chunk_off, N, max_entries, snap_seq,
-                                                            snap_pos);
+                                                            snap_pos, device_status);
     return cudaGetLastError();
 }
 

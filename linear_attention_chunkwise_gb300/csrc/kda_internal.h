@@ -10,6 +10,23 @@
 
 namespace kda {
 
+// Debug builds (-DKDA_DEBUG_BOUNDS): before it touches memory, every CTA checks the ranges it derives
+// from cu_seqlens, the schedule, the chunk table and snapshot entries (sequence, head, chunk and token
+// ranges, snapshot entries) against the sizes of the buffers they index.  A range outside its buffer
+// sets KDA_DEV_BOUNDS in the status word and the CTA skips that work; nothing traps.  Release builds
+// compile the checks away (the condition is not evaluated).
+#ifdef KDA_DEBUG_BOUNDS
+#define KDA_BOUNDS(cond, status) (::kda::bounds_check((cond), (status)))
+#else
+#define KDA_BOUNDS(cond, status) true
+#endif
+#ifdef __CUDACC__
+__device__ __forceinline__ bool bounds_check(bool ok, int32_t* status) {
+    if (!ok && status) atomicOr(status, KDA_DEV_BOUNDS);
+    return ok;
+}
+#endif
+
 constexpr int kChunk = 64;   // chunk length of the prefill
 constexpr int kHeadDim = 128;  // dk = dv
 
@@ -49,6 +66,7 @@ struct PrefillArgs {
     int64_t total_tokens;
     int32_t num_seqs;
     int32_t H;
+    int64_t blob_units = 0;  // two-pass path: (chunk, head) images the workspace holds
     // Two-pass path run in pieces: chunks [piece_begin, piece_begin + piece_len)
     // of every sequence; piece_len = 0 means all chunks in one launch pair.
     int32_t piece_begin = 0;
@@ -126,13 +144,16 @@ struct BackwardArgs {
     float* rec = nullptr;        // per-(chunk, head) records of the prep kernel (backward_record_bytes each)
     float* xbuf = nullptr;       // adjoint of the state after every chunk, indexed like ckpt
     float* u_scratch = nullptr;  // [T, H, 128] rows u_t between the value and key kernels (may be dq)
+    int32_t* device_status = nullptr;
+    int64_t total_tokens = 0;
+    int64_t chunk_slots = 0;     // chunk entries of ckpt, xbuf and rec
     int32_t num_seqs = 0;
     int32_t H = 0;
 };
 size_t backward_record_bytes();
 // Snapshot entries at every chunk end (and sentinels up to max_entries) from the chunk table.
 cudaError_t launch_ckpt_entries(const int32_t* cu_seqlens, const int32_t* chunk_off, int32_t N, int32_t max_entries,
-                                int32_t* snap_seq, int32_t* snap_pos, cudaStream_t stream);
+                                int32_t* snap_seq, int32_t* snap_pos, int32_t* device_status, cudaStream_t stream);
 // Fused prologue of the backward (q, k L2 norms, sigmoid beta into copies; inv = 1/norm of q and k
 // per (token, head)) and the chain rule through it afterwards, in place on dq, dk, dbeta.
 cudaError_t launch_bwd_prologue(bool f32_io, const void* q, const void* k, const float* beta, void* qh, void* kh,

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int pos = blockIdx.x / H;
     const int h = blockIdx.x - pos * H;
     const int seq = p.order ? p.order[pos] : pos;
+    if (!KDA_BOUNDS(pos < p.num_seqs && seq >= 0 && seq < p.num_seqs, p.device_status)) return;
 
     const int64_t t_begin = p.cu_seqlens[seq];
     const int64_t t_end = p.cu_seqlens[seq + 1];

@@ -228,6 +228,10 @@ __global__ void __launch_bounds__(NT, 3)
     const int64_t rem = p.cu_seqlens[seq + 1] - t0;
     const int Lc = static_cast<int>(rem < C ? rem : C);
     uint8_t* const blob = p.blobs + (static_cast<size_t>(j) * H + h) * kPrefillBlobBytes;
+    if (!KDA_BOUNDS(seq >= 0 && seq < N && h < H && j >= 0 && (static_cast<int64_t>(j) + 1) * H <= p.blob_units &&
+                        t0 >= 0 && Lc >= 1 && t0 + Lc <= p.total_tokens,
+                    p.device_status))
+        return;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);  // 0: q/k, 1: mma
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
@@ -540,6 +544,14 @@ __global__ void __launch_bounds__(NTS, 1)
     }
     const int64_t seq_len = static_cast<int64_t>(p.cu_seqlens[seq + 1]) - p.cu_seqlens[seq];
     int next_snap = si < se ? p.snap_pos[si] : INT_MAX;
+    // (both CTAs of an output-gate cluster share seq and h, so they leave here together)
+    if (!KDA_BOUNDS(seq >= 0 && seq < N && h < H && t_begin >= 0 && t_end <= p.total_tokens && seq_len >= 0 &&
+                        static_cast<int64_t>(nch_seq) * C >= seq_len && static_cast<int64_t>(nch_seq) * C < seq_len + C &&
+                        cb >= 0 && nch >= 0 && cb + nch <= nch_seq && jb >= 0 &&
+                        (static_cast<int64_t>(jb) + nch) * H <= p.blob_units && 0 <= si && si <= se &&
+                        se <= p.num_snaps,
+                    p.device_status))
+        return;
 
     // state: row rho, columns [j0 + PC*cq, +PC)
     const int rho = 32 * qw + lane;

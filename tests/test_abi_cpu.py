@@ -423,3 +423,12 @@ def test_out_gate_may_be_null_without_tokens(lib):
                  gb=None, gg=None)
     assert _backward_gated(lib, fz, **empty) == kda.KDA_ERR_CUDA
     assert _backward_gated(lib, fz) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_header_bit_constants_match_the_binding():
+    """Every KDA_DEV_* and KDA_FUSE_* bit the header defines has the same value in the Python binding."""
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    defs = dict(re.findall(r"#define\s+(KDA_(?:DEV|FUSE)_\w+)\s+(0x[0-9a-fA-F]+)u?", src))
+    assert {"KDA_DEV_BAD_CU_SEQLENS", "KDA_DEV_BOUNDS", "KDA_FUSE_OUT_GATE"} <= set(defs)
+    for name, val in defs.items():
+        assert getattr(kda, name) == int(val, 16), name
