@@ -121,10 +121,11 @@ KDA_API const char *kda_status_string(kda_status s);
 /*
  * Workspace (device bytes, 256-byte aligned start) for kda_prefill's
  * two-pass path (the fast one): the sequence schedule, the chunk table, bf16
- * copies of q, k, v when qkv_dtype is KDA_DTYPE_F32, and 67,072 bytes per
+ * copies of q, k, v when qkv_dtype is KDA_DTYPE_F32, 67,072 bytes per
  * (chunk, head) of prepared operands, counting ceil(total_tokens/64) +
- * num_seqs chunks -- about 1.05 KB per token and head.  Returns 0 for
- * invalid arguments.
+ * num_seqs chunks -- about 1.05 KB per token and head -- and one fp32 state
+ * per (sequence, head), 64 KB each, that carries the state between the scan's
+ * pieces when the call passes no S_final.  Returns 0 for invalid arguments.
  */
 KDA_API size_t kda_prefill_workspace_bytes(kda_dtype qkv_dtype, int32_t num_seqs,
                                    int64_t total_tokens, int32_t H,

@@ -113,7 +113,7 @@ size_t esize_of(kda_dtype t) { return t == KDA_DTYPE_F32 ? 4 : 2; }
 // fp32 inputs][per-(chunk, head) operand images].  Single-pass path:
 // [schedule][bf16 q,k,v if fp32 inputs].
 struct WsLayout {
-    size_t table = 0, copies = 0, blobs = 0, total = 0;
+    size_t table = 0, copies = 0, blobs = 0, carry = 0, total = 0;
 };
 size_t copies_bytes(kda_dtype t, int64_t T, int32_t H) {
     if (t != KDA_DTYPE_F32) return 0;
@@ -126,7 +126,9 @@ WsLayout split_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
     w.table = round_up(static_cast<size_t>(N > 0 ? N : 1) * 4, kAlign);
     w.copies = w.table + round_up(static_cast<size_t>(N + 2) * 4, kAlign);  // chunk table
     w.blobs = w.copies + copies_bytes(t, T, H);
-    w.total = w.blobs + static_cast<size_t>(max_chunks(N, T)) * H * kda::kPrefillBlobBytes;
+    // the state carried between scan pieces when the caller asks for no S_final
+    w.carry = round_up(w.blobs + static_cast<size_t>(max_chunks(N, T)) * H * kda::kPrefillBlobBytes, kAlign);
+    w.total = w.carry + static_cast<size_t>(N) * H * kHeadDim * kHeadDim * 4;
     return w;
 }
 WsLayout fused_layout(kda_dtype t, int32_t N, int64_t T, int32_t H) {
@@ -368,7 +370,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const int64_t sq = (seq_chunks + (seq_chunks + sq0 - 1) / sq0 - 1) / ((seq_chunks + sq0 - 1) / sq0);
         const int64_t pieces = (seq_chunks + sq - 1) / sq;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        const bool piecewise = S_final && pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
+        const bool piecewise = pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
                                cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
         if (!piecewise)
             return kda::launch_prefill_split(tm_q, tm_k, tm_v, og ? &tm_g : nullptr, a,
@@ -382,6 +384,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const int64_t lead = std::min<int64_t>(
             seq_chunks, sq + static_cast<int64_t>(kPrepLag * static_cast<double>(sq * (pieces - 1)) + 0.999));
         const int64_t share = (seq_chunks - lead + pieces - 2) / (pieces - 1);
+        if (!S_final) a.S_final = reinterpret_cast<float*>(ws + two.carry);  // the pieces' state carry
         bool ok = true;
         int64_t prepared = 0;  // chunks [0, prepared) of every sequence have their images (or are queued)
         for (int64_t j = 0; j < pieces && ok; ++j) {

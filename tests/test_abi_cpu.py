@@ -46,10 +46,14 @@ def test_workspace_bytes(lib):
     # single-pass path: schedule (+ bf16 copies of fp32 inputs)
     assert kda.kda_prefill_min_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256
     assert kda.kda_prefill_min_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2) == 256 + 3 * 256 * 2 * 128 * 2
-    # two-pass path: schedule + chunk table + (copies) + (ceil(T/64) + N) chunks x H operand images
-    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == 256 + 256 + (16 + 16) * 32 * BLOB
+    # two-pass path: schedule + chunk table + (copies) + (ceil(T/64) + N) chunks x H operand images, then
+    # (256-byte aligned) one fp32 state per (sequence, head) carried between scan pieces
+    up = lambda x: -(-x // 256) * 256
+    STATE = 128 * 128 * 4
+    assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_BF16, 16, 1000, 32) == \
+        up(256 + 256 + (16 + 16) * 32 * BLOB) + 16 * 32 * STATE
     assert kda.kda_prefill_workspace_bytes(kda.KDA_DTYPE_F32, 1, 256, 2) == \
-        256 + 256 + 3 * 256 * 2 * 128 * 2 + (4 + 1) * 2 * BLOB
+        up(256 + 256 + 3 * 256 * 2 * 128 * 2 + (4 + 1) * 2 * BLOB) + 2 * STATE
     for fn in (kda.kda_prefill_workspace_bytes, kda.kda_prefill_min_workspace_bytes):
         assert fn(kda.KDA_DTYPE_BF16, -1, 10, 2) == 0
         assert fn(7, 1, 10, 2) == 0

@@ -190,7 +190,7 @@ def test_prefill_piecewise_two_sequences(alias):
     assert int(status.item()) == 0
     p.S0 = S0_copy  # the oracle starts from the original states
     check_against_oracle(p, o, sf, [[0, 3], [1, 2]])
-    # the same batch in one launch pair (no S_final -> no piecewise schedule) gives the same o
+    # without S_final the pieces carry the state in the workspace instead: the same o
     o1, _ = kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, S0_copy, return_final=False)
     torch.cuda.synchronize()
     assert torch.equal(o, o1)
