@@ -327,12 +327,15 @@ def bench_prefill(cx: Ctx, args):
         step()
     cx.barrier()
     ev0, ev1 = cx.events()
-    with ClockSampler(cx.dev) as clk:
-        ev0.record(cx.stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(cx.stream)
-        cx.barrier()
+    # clocks are sampled from the timed steps through the end-to-end, variant and chain timings below
+    # (the same kernels), so that a short timed region still gets many samples
+    clk = ClockSampler(cx.dev)
+    clk.__enter__()
+    ev0.record(cx.stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(cx.stream)
+    cx.barrier()
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms = cx.max_over_ranks(ms_local)
     tokens_per_step = T * cx.ws
@@ -408,6 +411,20 @@ def bench_prefill(cx: Ctx, args):
             S_snap=ss, workspace=work, stream=cx.stream)),
     }
     del gate, ss
+    # the limit that binds this workload: the scan's serial chain over the sequence's 128 chunks.  The
+    # same sequence with one head runs that chain with the GPU otherwise idle (pass 1 and the other heads'
+    # chains are what the 32-head call adds); its time is the chain's floor for this sequence.
+    p1 = synth.prefill_inputs(c["lengths"], 1, D, c["dtype"], c["lo"], c["s0_std"],
+                              synth.workload_seed(PREFILL_WORKLOAD) + 1000 * cx.rank + 1, cx.dev)
+    o1 = torch.empty_like(p1.q)
+    sf1 = torch.empty((1, 1, D, D), dtype=torch.float32, device=cx.dev)
+    chain_us = variant_us(lambda: kda.kda_prefill(p1.q, p1.k, p1.v, p1.log_alpha, p1.beta, p1.cu_seqlens, None,
+                                                  o=o1, S_final=sf1, stream=cx.stream), n=20)
+    del p1, o1, sf1
+    clk.__exit__(None, None, None)
+    chain = {"us": chain_us, "frac": round(chain_us / (ms * 1e3), 4),
+             "what": "the same 8192-token sequence with 1 head: the scan's 128-chunk serial chain with the GPU "
+                     "otherwise idle; frac = that floor / this call's time"}
     # kernels per call: schedule + chunk table + the pass-1 and scan launches of the piecewise
     # schedule (one sequence here, so the scan leaves SMs idle), else one prep + one scan
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
@@ -418,6 +435,7 @@ def bench_prefill(cx: Ctx, args):
         "ms": ms,
         "launches": (2 + n_prep + n_scan) * args.steps,
         "variants": variants,
+        "chain_bound": chain,
         "tokens": T,
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                      "frac": round(achieved_gbs / pk["hbm"], 4),
@@ -432,7 +450,7 @@ def bench_prefill(cx: Ctx, args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "overlap": "H2D of step i+1 and D2H of step i-1 run beside step i (two buffer sets, "
                            "copy streams ordered by events)"},
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window="the timed steps, then the end-to-end, variant and chain timings"),
     }
 
 
@@ -775,6 +793,7 @@ def run_ours(args):
                        "parallelism": f"independent problem per GPU x{cx.ws}"},
             "roofline": pf["roofline"], "tensor": pf["tensor"], "e2e": pf["e2e"],
             "gpu_launches": pf["launches"], "clocks": pf["clocks"], "prefill_variants": pf["variants"],
+            "chain_bound": pf["chain_bound"],
         })
     if dc is not None:
         out["decode"] = dc

@@ -22,7 +22,7 @@ def _fake_prefill(cx, args):
             "tensor": {"achieved": 1.0, "peak": 2.0, "unit": "TFLOP/s", "frac": 0.5},
             "e2e": {"value": 1.0, "unit": "Mtok/s", "h2d_bytes_per_step": 10, "d2h_bytes_per_step": 5},
             "launches": 8, "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
-            "variants": {"plain_us": 500.0}}
+            "variants": {"plain_us": 500.0}, "chain_bound": {"us": 250.0, "frac": 0.5, "what": "chain"}}
 
 
 def test_our_arm_json_line(monkeypatch, capsys):
@@ -54,3 +54,4 @@ def test_our_arm_json_line(monkeypatch, capsys):
     assert d["gpu_launches"] > 0
     assert "decode" in d and "backward" in d
     assert set(d["prefill_workloads"]) == {"varlen_prefill", "long_prefill_1m"}
+    assert d["chain_bound"]["us"] > 0 and 0 < d["chain_bound"]["frac"]
