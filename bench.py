@@ -644,7 +644,7 @@ def bench_prefill_workload(cx: Ctx, args, name: str, calls: int):
 
 def bench_prefill_fused(cx: Ctx, args):
     """The 8k prefill through kda_prefill_ex with every fusion: q/k L2 norm, sigmoid beta and the
-    output RMSNorm x gate (2-CTA cluster scan).  Device-resident inputs, CUDA events."""
+    output RMSNorm x gate (one pass after the scan).  Device-resident inputs, CUDA events."""
     torch = cx.torch
     import linear_attention_chunkwise_gb300 as kda
     from linear_attention_chunkwise_gb300 import synth

@@ -88,7 +88,10 @@ typedef enum {
  * L2-normalised ("KDA Architecture"),
  * the update gate beta as a sigmoid of its projection, and the output gate
  * (RMSNorm of o_t, then an elementwise product with g_t) ("KDA has three
- * gates").  Done inside the kernels, they save the caller a pass over HBM.
+ * gates").  The prologue runs inside the kernels (pass 1 of the prefill, the
+ * decode kernels); the output gate runs inside the decode kernels and, for
+ * the prefill, as one pass over o and the gate after the scan (the row's
+ * mean square is taken from the row it scales).
  *
  *   KDA_FUSE_L2NORM_QK   q, k <- x / sqrt(sum_c x_c^2 + l2_eps), per (token, head)
  *   KDA_FUSE_BETA_SIGMOID  beta holds logits b; beta = 1 / (1 + exp(-b)) is used

@@ -324,13 +324,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         !make_map(&tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_tokens ? static_cast<const void*>(log_alpha) : dummy,
                   kHeadDim, Hh, T, kHeadDim, kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
         return KDA_ERR_CUDA;
-    // output gate [T, H, dv] in the dtype of o, read by the scan in 128-byte boxes (64 bf16 / 32 fp32 columns)
-    CUtensorMap tm_g;
     const bool og = (fz.flags & KDA_FUSE_OUT_GATE) != 0;
-    if (og && !make_map(&tm_g, qkv_dtype == KDA_DTYPE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        es, have_tokens ? fz.out_gate : dummy, kHeadDim, Hh, T, qkv_dtype == KDA_DTYPE_F32 ? 32 : 64,
-                        kda::kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
-        return KDA_ERR_CUDA;
 
     if (kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -350,15 +344,21 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     a.snap_pos = snap.pos;
     a.num_snaps = snap.count;
     a.S_snap = snap.S;
-    a.fuse_flags = fz.flags;
     a.l2_eps = fz.l2_eps;
-    a.rms_eps = fz.rms_eps;
-    a.rms_weight = fz.rms_weight;
-    a.out_gate = fz.out_gate;
     a.total_tokens = total_tokens;
     a.num_seqs = num_seqs;
     a.H = H;
     const bool out_f32 = qkv_dtype == KDA_DTYPE_F32;
+    // pass 1 applies the prologue; the output gate runs after the scan, in place on o (one pass over o
+    // and the gate: cheaper than exchanging row sums between the two dv slices inside the scan)
+    a.fuse_flags = fz.flags & ~KDA_FUSE_OUT_GATE;
+    auto out_gate = [&](bool ok) {
+        if (!ok) return KDA_ERR_CUDA;
+        if (og && kda::launch_out_gate(out_f32, o, fz.out_gate, fz.rms_weight, fz.rms_eps, total_tokens * H,
+                                       stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        return KDA_OK;
+    };
     if (two_pass) {
         if (kda::launch_chunk_table(cu_seqlens, num_seqs, total_tokens, reinterpret_cast<int32_t*>(ws + two.table),
                                     device_status, snap.seq, snap.pos, snap.count, stream) != cudaSuccess)
@@ -373,11 +373,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const bool piecewise = pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
                                cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
         if (!piecewise)
-            return kda::launch_prefill_split(tm_q, tm_k, tm_v, og ? &tm_g : nullptr, a,
-                                             max_chunks(num_seqs, total_tokens), out_f32,
-                                             stream) == cudaSuccess
-                       ? KDA_OK
-                       : KDA_ERR_CUDA;
+            return out_gate(kda::launch_prefill_split(tm_q, tm_k, tm_v, a, max_chunks(num_seqs, total_tokens), out_f32,
+                                                      stream) == cudaSuccess);
         // Scan piece j covers chunks [j sq, (j+1) sq).  Pass 1's first launch prepares a lead of L0
         // chunks; its launch j (j >= 1) prepares the next share of the rest beside scan piece j-1.  L0
         // makes up for pass 1 being slower on the SMs the scan leaves than the scan is per chunk.
@@ -400,9 +397,9 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
             }
             a.piece_begin = static_cast<int32_t>(j * sq);
             a.piece_len = static_cast<int32_t>(scan_end - j * sq);
-            ok = ok && kda::launch_chunk_scan(tm_v, og ? &tm_g : nullptr, a, out_f32, stream) == cudaSuccess;
+            ok = ok && kda::launch_chunk_scan(tm_v, a, out_f32, stream) == cudaSuccess;
         }
-        return ok ? KDA_OK : KDA_ERR_CUDA;
+        return out_gate(ok);
     } else if (kda::launch_prefill_fused(tm_q, tm_k, tm_v, tm_la, a, out_f32, stream) != cudaSuccess) {
         return KDA_ERR_CUDA;
     }

@@ -76,13 +76,10 @@ struct PrefillArgs {
     const int32_t* snap_pos = nullptr;
     int32_t num_snaps = 0;
     float* S_snap = nullptr;
-    // fused prologue (KDA_FUSE_* bits; pass 1 applies them) and epilogue
-    // (KDA_FUSE_OUT_GATE: pass 2 runs as 2-CTA clusters, one per (sequence, head))
+    // fused prologue (KDA_FUSE_L2NORM_QK, KDA_FUSE_BETA_SIGMOID: pass 1 applies them; the output
+    // gate runs after the scan, launch_out_gate)
     uint32_t fuse_flags = 0;
     float l2_eps = 0.f;
-    float rms_eps = 0.f;
-    const float* rms_weight = nullptr;
-    const void* out_gate = nullptr;
 };
 
 // Bytes per (chunk, head) of the two-pass path's operand images:
@@ -107,8 +104,7 @@ cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int6
                                int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
                                int32_t num_snaps, cudaStream_t stream);
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap* tm_g, const PrefillArgs& a,
-                                 int64_t max_chunks, bool out_f32, cudaStream_t stream);
+                                 const PrefillArgs& a, int64_t max_chunks, bool out_f32, cudaStream_t stream);
 // The two passes separately, for the piecewise schedule.  Pass 1's grid is
 // `units` x H CTAs: units = chunk slots of the whole batch (piece_len = 0) or
 // num_seqs x piece_len (piece mode); with beside_previous it is launched as a
@@ -116,9 +112,10 @@ cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_
 // whose CTAs release it once all of them run).  Pass 2 has num_seqs x H x 2 CTAs.
 cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const PrefillArgs& a, int64_t units,
                               cudaStream_t stream, bool beside_previous);
-// tm_g: TMA map of the output gate (required with KDA_FUSE_OUT_GATE, else unused / NULL).
-cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
-                              cudaStream_t stream);
+// y = RMSNorm(o) * w * gate in place on o ([rows, 128], the input dtype), w NULL = ones.
+cudaError_t launch_out_gate(bool f32_io, void* o, const void* gate, const float* w, float eps, int64_t rows,
+                            cudaStream_t stream);
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream);
 
 // Reverse-mode gradient of the prefill (kda_backward.cu).  Gradients are fp32,
 // [T, H, 128] for q/k/v/log_alpha, [T, H] for beta, [N, H, 128, 128] for S0.

@@ -53,49 +53,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* r) {
     else tmem_ld16(taddr, r);
 }
 
-// ---- 2-CTA cluster exchange (fused output gate) ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-// Asynchronous 4-byte store into a peer CTA's shared memory that counts its bytes on the peer's
-// mbarrier (complete_tx), the way a TMA load does: the reader needs no release / acquire fences.
-__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar_addr) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
-                 "r"(__float_as_uint(v)), "r"(bar_addr)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Bounded spin on an mbarrier phase with test_wait (never suspends the thread): for phases that
-// complete from another CTA, where a suspended try_wait may sleep past the completion.
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long long limit_cycles) {
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (clock64() - t0 > limit_cycles) return false;
-    }
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
@@ -376,22 +333,13 @@ struct ScanSmem {
     static constexpr uint32_t OP_SM = 2 * SET;   // [128 rows][128 B]: Sm slice
     static constexpr uint32_t OP_U = OP_SM + 16384;  // [64 rows][128 B]: U slice
     static constexpr uint32_t BARS = OP_U + 8192;    // 5 x u64: load0, load1, c1, c2, fin
-    static constexpr uint32_t RXBAR = BARS + 40;     // 2 x u64: peer's row partials landed (by chunk parity)
-    static constexpr uint32_t TMEM_SLOT = RXBAR + 16;
+    static constexpr uint32_t TMEM_SLOT = BARS + 40;
     static constexpr uint32_t ABORT = TMEM_SLOT + 4;
-    static constexpr uint32_t OSQ = ABORT + 4;       // f32 [2][64]: sum of o^2 per O row, per column half
-    static constexpr uint32_t RX = OSQ + 512;        // f32 [2][64]: the peer CTA's row sums, by chunk parity
-    static constexpr uint32_t EVBAR = RX + 512;      // 2 x u64: a set's exp vectors landed (by chunk parity)
+    static constexpr uint32_t EVBAR = ABORT + 4;     // 2 x u64: a set's exp vectors landed (by chunk parity)
     static constexpr uint32_t TOTAL = EVBAR + 16;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
-    // fused output gate only: the gate tiles of two chunks (TMA, 128B-swizzled rows of 128 B:
-    // one 64-column box for bf16, two 32-column boxes for fp32) and their barriers
-    static constexpr uint32_t GATE = (TOTAL + 1023) / 1024 * 1024;
-    static constexpr uint32_t GBAR = GATE + 2 * 16384;
-    static constexpr uint32_t WRMS = GBAR + 16;      // f32 [64]: RMSNorm weight of this CTA's columns
-    static constexpr uint32_t ALLOC_OG = WRMS + 256 + 1024;
 };
-static_assert(ScanSmem::ALLOC_OG <= 232448, "scan shared memory (output gate) over the per-CTA limit");
+static_assert(ScanSmem::EVBAR % 8 == 0 && ScanSmem::BARS % 8 == 0, "mbarriers are 8-byte aligned");
 // per-warp staging inside a consumed operand set: the state slice (128 rows x 64 fp32 over all warps)
 // fits the [-W; Qh] tile, the output rows (64 rows x 64 columns, at most fp32) the Kb tile
 static_assert(128 * 64 * 4 <= ScanSmem::S_KB - ScanSmem::S_A, "state stage over the [-W; Qh] tile");
@@ -481,16 +429,12 @@ __device__ __forceinline__ void store_out_rows(OutT* dst, int64_t row_stride, in
     __syncwarp();
 }
 
-// OG (fused output gate): the two dv slices of a (sequence, head) run as one
-// 2-CTA cluster and swap per-row sums of o^2 through distributed shared
-// memory, so each writes y = o / sqrt(mean o^2 + eps) * weight * gate.
 // NTS threads in NTS/128 column groups (256: two groups of 32 state columns per thread; 512: four
 // of 16).  Thread (warp w): lane quarter qw = w % 4 (state rows 32 qw + lane, the TMEM lanes it may
 // read), column group cq = w / 4.
-template <typename OutT, bool OG, int NTS>
+template <typename OutT, int NTS>
 __global__ void __launch_bounds__(NTS, 1)
-    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                          const PrefillArgs p) {
+    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
     using L = ScanSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -544,7 +488,6 @@ __global__ void __launch_bounds__(NTS, 1)
     }
     const int64_t seq_len = static_cast<int64_t>(p.cu_seqlens[seq + 1]) - p.cu_seqlens[seq];
     int next_snap = si < se ? p.snap_pos[si] : INT_MAX;
-    // (both CTAs of an output-gate cluster share seq and h, so they leave here together)
     if (!KDA_BOUNDS(seq >= 0 && seq < N && h < H && t_begin >= 0 && t_end <= p.total_tokens && seq_len >= 0 &&
                         static_cast<int64_t>(nch_seq) * C >= seq_len && static_cast<int64_t>(nch_seq) * C < seq_len + C &&
                         cb >= 0 && nch >= 0 && cb + nch <= nch_seq && jb >= 0 &&
@@ -577,25 +520,14 @@ __global__ void __launch_bounds__(NTS, 1)
     uint64_t* evbar = reinterpret_cast<uint64_t*>(sm + L::EVBAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEM_SLOT);
     volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
-    uint64_t* rxbar = reinterpret_cast<uint64_t*>(sm + L::RXBAR);
-    uint64_t* gbar = reinterpret_cast<uint64_t*>(sm + L::GBAR);
     if (tid == 0) {
         *abort_s = 0;
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         mbar_init(&evbar[0], 1);
         mbar_init(&evbar[1], 1);
-        if (OG) {
-            mbar_init(&rxbar[0], 1);  // this CTA's arrive.expect_tx + the peer's 64 async stores
-            mbar_init(&rxbar[1], 1);
-            mbar_init(&gbar[0], 1);
-            mbar_init(&gbar[1], 1);
-            prefetch_tmap(&tm_g);
-        }
         fence_mbar_init();
         prefetch_tmap(&tm_v);
     }
-    if (OG && tid < NV)
-        reinterpret_cast<float*>(sm + L::WRMS)[tid] = p.rms_weight ? p.rms_weight[slice * NV + tid] : 1.f;
     for (int e = tid; e < 2 * 512; e += NTS)  // zero rows of both [Tb | 0 | M] tiles
         reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp == 0) {
@@ -610,12 +542,6 @@ __global__ void __launch_bounds__(NTS, 1)
     const uint32_t tq = tmem + tmem_lane(qw);
     constexpr uint32_t TM_X = 0;    // + 64 * parity
     constexpr uint32_t TM_DS = 128;
-    // fused output gate: peer CTA rank and the shared-memory addresses this CTA writes there
-    const uint32_t peer = OG ? (cluster_ctarank() ^ 1u) : 0u;
-    uint32_t ph_rx = 0;  // phase parity of rxbar[i] in bit i (registers, not a runtime-indexed array)
-    float* osq = reinterpret_cast<float*>(sm + L::OSQ);
-    const float* rx = reinterpret_cast<const float*>(sm + L::RX);
-    if (OG) cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
 
     auto issue_loads = [&](int c) {
         uint8_t* set = sm + (c & 1) * L::SET;
@@ -639,55 +565,6 @@ __global__ void __launch_bounds__(NTS, 1)
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
         if (!mbar_wait_pipe(bar, ph)) *abort_s = 1;
         ph ^= 1u;
-    };
-    // fused output gate: y = o / sqrt(mean o^2 + eps) * weight * gate for chunk cf, whose O rows sit in
-    // X[cf & 1] and whose row sums are own_pending (this CTA) + RX[cf & 1] (the peer's)
-    float own_pending = 0.f;
-    float o_pend[PC];  // the O row of the chunk awaiting its output gate (this thread's PC columns)
-    // gate tile of chunk cf -> GATE[cf & 1] (issued by tid 64 one step before og_finish(cf) reads it)
-    constexpr int kGateBoxes = static_cast<int>(sizeof(OutT) / 2);  // 128-byte boxes per 64 columns
-    uint32_t ph_g = 0;  // parity of gbar[i] in bit i
-    int gate_pending = -1;  // tid 64: the chunk whose gate load is in flight and not yet consumed
-    auto issue_gate = [&](int cf) {
-        uint64_t* bar = &gbar[cf & 1];
-        mbar_arrive_expect_tx(bar, kGateBoxes * 8192);
-        const int32_t z = static_cast<int32_t>(t_begin + static_cast<int64_t>(cf) * C);
-#pragma unroll
-        for (int bx = 0; bx < kGateBoxes; ++bx)
-            tma_load_3d(sm + L::GATE + (cf & 1) * 16384 + bx * 8192, &tm_g, bar, j0 + bx * (64 / kGateBoxes), h, z);
-        gate_pending = cf;
-    };
-    auto og_finish = [&](int cf, int rr) {
-        const int bf = cf & 1;
-        if (tid == 64) mbar_arrive_expect_tx(&rxbar[bf], 64 * 4);  // the peer's 64 row sums
-        if (!mbar_spin(&rxbar[bf], (ph_rx >> bf) & 1u, kWaitLimit)) *abort_s = 1;
-        ph_rx ^= 1u << bf;
-        const float sc = rsqrtf((own_pending + rx[bf * 64 + rr]) * (1.f / D) + p.rms_eps);
-        float* a = o_pend;
-        const int64_t tf = t_begin + static_cast<int64_t>(cf) * C;
-        if (!mbar_wait_pipe(&gbar[bf], (ph_g >> bf) & 1u)) *abort_s = 1;
-        ph_g ^= 1u << bf;
-        if (tid == 64) gate_pending = -1;
-        if (tf + rr < t_end) {
-            const int64_t row = (tf + rr) * H + h;
-            // this thread's PC gate values (columns c0 .. c0+PC-1 of the slice): 16-byte chunks of a
-            // 128B-swizzled 128-byte row (one 64-column box for bf16, two 32-column boxes for fp32)
-            constexpr int kPerChunk = static_cast<int>(16 / sizeof(OutT));
-            constexpr int kBoxCols = 64 / kGateBoxes;
-            const int c0 = PC * cq;
-            uint4 gv[PC / kPerChunk];
-            const uint8_t* grow = sm + L::GATE + bf * 16384 + (c0 / kBoxCols) * 8192;
-#pragma unroll
-            for (int i = 0; i < PC / kPerChunk; ++i)
-                gv[i] = *reinterpret_cast<const uint4*>(grow + sw128_chunk(rr, (c0 % kBoxCols) / kPerChunk + i));
-            const OutT* g = reinterpret_cast<const OutT*>(gv);
-            const float* w = reinterpret_cast<const float*>(sm + L::WRMS) + c0;
-#pragma unroll
-            for (int e = 0; e < PC; ++e) a[e] = a[e] * sc * w[e] * static_cast<float>(g[e]);
-            OutT* dst = static_cast<OutT*>(p.o) + row * static_cast<int64_t>(D) + j0 + c0;
-#pragma unroll
-            for (int ch = 0; ch < PC / 8; ++ch) store_out8<OutT>(dst + 8 * ch, a + 8 * ch);
-        }
     };
     const uint64_t d_sm = sdesc_sw128(smem_u32(sm + L::OP_SM), 8192, 1024);
     const uint64_t d_u = sdesc_sw128(smem_u32(sm + L::OP_U), 8192, 1024);
@@ -798,47 +675,20 @@ __global__ void __launch_bounds__(NTS, 1)
             }
         }
         if (qw >= 2) {  // O rows -> global
-            const int rr = 32 * (qw - 2) + lane;
-            if (OG) {
-                // fused output gate, one chunk behind: finish chunk c-1 (its O rows are still in
-                // X[(c-1)&1] and the peer's row sums have had a whole step to arrive), then send
-                // this chunk's row sums of o^2 to the peer without waiting
-                if (c > 0) og_finish(c - 1, rr);
-                if (tid == 64) issue_gate(c);
-                tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, o_pend);
-                tmem_ld_wait();
-                float ps = 0.f;
-#pragma unroll
-                for (int e = 0; e < PC; ++e) ps = fmaf(o_pend[e], o_pend[e], ps);
-                osq[cq * 64 + rr] = ps;
-                bar_sync_named(1, 64 * CQ);  // the O warps
-                own_pending = 0.f;
-#pragma unroll
-                for (int q2 = 0; q2 < CQ; ++q2) own_pending += osq[q2 * 64 + rr];
-                if (cq == 0)
-                    st_async_cluster_f32(mapa_shared(smem_u32(sm + L::RX + (b * 64 + rr) * 4), peer), own_pending,
-                                         mapa_shared(smem_u32(&rxbar[b]), peer));
-            } else {
-                float a[PC];
-                tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
-                tmem_ld_wait();
-                // staged in this chunk's Kb tile (its MMAs have completed; every load of the set
-                // rewrites it), beside the [-W; Qh] tile the state snapshot may use -- never in the
-                // zero rows of [Tb | 0 | M], which are written once
-                const int row0 = 32 * (qw - 2);
-                store_out_rows<OutT, PC>(
-                    static_cast<OutT*>(p.o) + ((t0 + row0) * H + h) * static_cast<int64_t>(D) + j0 + PC * cq,
-                    static_cast<int64_t>(H) * D, Lc - row0, a, set + L::S_KB + ((qw - 2) + 2 * cq) * (32 * PC * 4),
-                    lane);
-            }
+            float a[PC];
+            tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
+            tmem_ld_wait();
+            // staged in this chunk's Kb tile (its MMAs have completed; every load of the set
+            // rewrites it), beside the [-W; Qh] tile the state snapshot may use -- never in the
+            // zero rows of [Tb | 0 | M], which are written once
+            const int row0 = 32 * (qw - 2);
+            store_out_rows<OutT, PC>(
+                static_cast<OutT*>(p.o) + ((t0 + row0) * H + h) * static_cast<int64_t>(D) + j0 + PC * cq,
+                static_cast<int64_t>(H) * D, Lc - row0, a, set + L::S_KB + ((qw - 2) + 2 * cq) * (32 * PC * 4),
+                lane);
         }
         tc_fence_before();
     }
-    __syncthreads();
-    if (OG && qw >= 2 && *abort_s == 0)  // the last chunk's output gate
-        og_finish(nch - 1, 32 * (qw - 2) + lane);
-    if (OG && tid == 64 && gate_pending >= 0)  // a wind-down left a gate copy in flight: let it land
-        (void)mbar_wait(&gbar[gate_pending & 1], (ph_g >> (gate_pending & 1)) & 1u, kDrainLimit);
     __syncthreads();
     const bool ok = *abort_s == 0;
     if (!ok && tid == 0 && p.device_status) atomicOr(p.device_status, KDA_DEV_TIMEOUT);
@@ -858,7 +708,6 @@ __global__ void __launch_bounds__(NTS, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
-    if (OG) cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
 }
 
 // Sets one function attribute on first use per device.
@@ -917,51 +766,83 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 }
 
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const CUtensorMap* tm_g, const PrefillArgs& a,
-                                 int64_t max_chunks, bool out_f32, cudaStream_t stream) {
+                                 const PrefillArgs& a, int64_t max_chunks, bool out_f32, cudaStream_t stream) {
     const cudaError_t err = launch_chunk_prep(tm_q, tm_k, a, max_chunks, stream, false);
     if (err != cudaSuccess) return err;
-    return launch_chunk_scan(tm_v, tm_g, a, out_f32, stream);
+    return launch_chunk_scan(tm_v, a, out_f32, stream);
 }
 
-template <typename OutT, bool OG>
-cudaError_t launch_scan_t(const CUtensorMap& tm_v, const CUtensorMap& tm_g, const PrefillArgs& a, unsigned ctas,
-                          cudaStream_t stream) {
+template <typename OutT>
+cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigned ctas, cudaStream_t stream) {
     constexpr int NTS = 256;  // 512 threads (16 columns each) measured no faster: the chunk is not epilogue-bound
     static int configured[64];
-    const uint32_t smem = OG ? ScanSmem::ALLOC_OG : ScanSmem::ALLOC;
-    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, OG, NTS>, smem, configured);
+    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, NTS>, ScanSmem::ALLOC, configured);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(NTS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (OG) {  // the two dv slices of a (sequence, head) are adjacent CTAs: one cluster
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, kda_chunk_scan_kernel<OutT, OG, NTS>, tm_v, tm_g, a);
+    kda_chunk_scan_kernel<OutT, NTS><<<ctas, NTS, ScanSmem::ALLOC, stream>>>(tm_v, a);
+    return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap* tm_g, const PrefillArgs& a, bool out_f32,
-                              cudaStream_t stream) {
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
     const unsigned n = static_cast<unsigned>(scan_ctas);
-    const bool og = (a.fuse_flags & KDA_FUSE_OUT_GATE) != 0;
-    if (og && !tm_g) return cudaErrorInvalidValue;
-    const CUtensorMap& g = og ? *tm_g : tm_v;  // unused without the output gate
-    if (out_f32)
-        return og ? launch_scan_t<float, true>(tm_v, g, a, n, stream)
-                  : launch_scan_t<float, false>(tm_v, g, a, n, stream);
-    return og ? launch_scan_t<__nv_bfloat16, true>(tm_v, g, a, n, stream)
-              : launch_scan_t<__nv_bfloat16, false>(tm_v, g, a, n, stream);
+    return out_f32 ? launch_scan_t<float>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16>(tm_v, a, n, stream);
 }
+
+// ============================================================ output gate ==
+// y = o / sqrt(mean_c o_c^2 + eps) * w * g, in place on o, after the scan: the output gate of "kimi
+// delta attn from first principles" (aryagxr), "KDA has three gates".  One warp per (token, head)
+// row, 4 channels per lane; the row's mean square is taken from the row itself, so the scan needs
+// no cross-slice exchange.  Grid-stride over the rows.
+namespace {
+__device__ __forceinline__ float4 og_ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 og_ld4(const __nv_bfloat16* p) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u), __uint_as_float(r.y << 16),
+                       __uint_as_float(r.y & 0xffff0000u));
+}
+__device__ __forceinline__ void og_st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void og_st4(__nv_bfloat16* p, float4 v) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+}
+
+template <typename IoT>
+__global__ void __launch_bounds__(256) kda_out_gate_kernel(IoT* o, const IoT* __restrict__ g,
+                                                           const float* __restrict__ w, float eps, int64_t rows) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 wv = w ? make_float4(w[4 * lane], w[4 * lane + 1], w[4 * lane + 2], w[4 * lane + 3])
+                        : make_float4(1.f, 1.f, 1.f, 1.f);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp; row < rows;
+         row += static_cast<int64_t>(gridDim.x) * 8) {
+        const size_t off = static_cast<size_t>(row) * kHeadDim + 4 * lane;
+        const float4 ov = og_ld4(o + off), gv = og_ld4(g + off);
+        float ss = ov.x * ov.x + ov.y * ov.y + ov.z * ov.z + ov.w * ov.w;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+        const float r = rsqrtf(ss * (1.f / kHeadDim) + eps);
+        og_st4(o + off, make_float4(ov.x * r * wv.x * gv.x, ov.y * r * wv.y * gv.y, ov.z * r * wv.z * gv.z,
+                                    ov.w * r * wv.w * gv.w));
+    }
+}
+}  // namespace
+
+cudaError_t launch_out_gate(bool f32_io, void* o, const void* gate, const float* w, float eps, int64_t rows,
+                            cudaStream_t stream) {
+    if (rows <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const int64_t need = (rows + 7) / 8;
+    const unsigned blocks = static_cast<unsigned>(need < 8LL * sms ? need : 8LL * sms);
+    if (f32_io)
+        kda_out_gate_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<float*>(o), static_cast<const float*>(gate),
+                                                               w, eps, rows);
+    else
+        kda_out_gate_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+            static_cast<__nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(gate), w, eps, rows);
+    return cudaGetLastError();
+}
+
 
 }  // namespace kda

@@ -12,7 +12,7 @@ Each case runs the same call through the release library and the checked one: th
 match and carry no KDA_DEV_BOUNDS, and every output must be bitwise equal (the checks change nothing
 when nothing is out of range).  The cases cover the layouts the kernels index differently: packed
 varlen batches with empty and one-token sequences, the piecewise schedule of long sequences, the
-single-pass path, snapshots, the fused prologue and the clustered output gate, decode with permuted
+single-pass path, snapshots, the fused prologue and the output gate, decode with permuted
 and bad slots, multi-token decode over several token batches, the backward (plain, fused, gated),
 and a malformed cu_seqlens.
 """
@@ -89,7 +89,7 @@ def test_prefill_snapshots(libs):
                                                            pos, p.S0, device_status=s)) == 0
 
 
-def test_prefill_fused_prologue_and_clustered_gate(libs):
+def test_prefill_fused_prologue_and_output_gate(libs):
     p = synth.prefill_inputs([300, 77, 0, 4100], 2, s0_std=0.02, seed=904, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(905)
     gate = torch.randn(p.q.shape, generator=g, device="cuda").to(p.q.dtype)

@@ -4,9 +4,8 @@ Inputs are raw (q, k not normalised, beta given as logits); the oracle applies
 its plain definitions (oracle.l2_normalize, oracle.sigmoid,
 oracle.rmsnorm_gate) to the exact input values, runs the recurrence in fp64,
 and the GPU result must match within the rel-L2 bound.  The output gate in
-prefill runs the scan as 2-CTA clusters (the row norm spans both dv slices):
-covered on varlen batches, a long single sequence (scan pieces) and the 8k
-workload.
+prefill runs after the scan as one pass over o and the gate: covered on varlen
+batches, a long single sequence (scan pieces) and the 8k workload.
 """
 import numpy as np
 import pytest

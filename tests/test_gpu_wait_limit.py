@@ -77,9 +77,9 @@ def test_expired_waits_report_timeout_and_the_next_call_is_exact(wait_lib, path)
     _check_normal_call(p)
 
 
-def test_expired_waits_in_the_cluster_output_gate(wait_lib):
-    """The fused output gate runs the scan as 2-CTA clusters that exchange row sums; both CTAs wind
-    down and meet at the final cluster barrier."""
+def test_expired_waits_with_the_output_gate(wait_lib):
+    """With the output gate the scan's waits expire the same way, and the gate's pass after the scan
+    (which waits on nothing) still runs to the end of the call."""
     p = synth.prefill_inputs([300, 77], 2, s0_std=0.02, seed=812, device="cuda")
     gate = torch.randn(p.q.shape, device="cuda").to(p.q.dtype)
     rc, status = _call(wait_lib, p, "two_pass", kda.Fusion(out_gate=gate))
