@@ -79,6 +79,7 @@ int sm_count() {
 constexpr int64_t kScanPieceChunks = 48;  // smallest scan piece (chunks per sequence); each piece costs a few us
 constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
 constexpr double kPrepLag = 0.1;           // lead of pass 1, as a fraction of the chunks scanned after piece 0
+constexpr double kPrepLagPrologue = 0.2;   // the same with the fused prologue (a slower pass 1; 8k: 345 -> 337 us)
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -379,7 +380,8 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         // chunks; its launch j (j >= 1) prepares the next share of the rest beside scan piece j-1.  L0
         // makes up for pass 1 being slower on the SMs the scan leaves than the scan is per chunk.
         const int64_t lead = std::min<int64_t>(
-            seq_chunks, sq + static_cast<int64_t>(kPrepLag * static_cast<double>(sq * (pieces - 1)) + 0.999));
+            seq_chunks, sq + static_cast<int64_t>((a.fuse_flags ? kPrepLagPrologue : kPrepLag) *
+                                                      static_cast<double>(sq * (pieces - 1)) + 0.999));
         const int64_t share = (seq_chunks - lead + pieces - 2) / (pieces - 1);
         if (!S_final) a.S_final = reinterpret_cast<float*>(ws + two.carry);  // the pieces' state carry
         bool ok = true;
