@@ -743,7 +743,34 @@ def bench_backward(cx: Ctx, args):
     ev1.record(cx.stream)
     cx.stream.synchronize()
     ms_fused = ev0.elapsed_time(ev1) / n
-    del work, grads
+    del work
+
+    # through the output gate as well (kda_prefill_backward_gated): dL/dy in, dL/dgate and dL/dweight out
+    gate = torch.randn(p.q.shape, generator=g, device=cx.dev).to(p.q.dtype)
+    wrms = torch.ones(D, **f32)
+    fzg = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=1e-6, out_gate=gate, rms_weight=wrms, rms_eps=1e-5)
+    work = torch.empty(kda.kda_prefill_backward_gated_workspace_bytes(torch.bfloat16, 1, T, H), dtype=torch.uint8,
+                       device=cx.dev)
+    grads_g = grads + (torch.empty((T, H, D), **f32), torch.empty((D,), **f32))
+
+    def call_gated():
+        kda.kda_prefill_backward_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, dO, None, dSf, fusion=fzg,
+                                       grads=grads_g, workspace=work, stream=cx.stream)
+
+    for _ in range(3):
+        call_gated()
+    ev0.record(cx.stream)
+    for _ in range(n):
+        call_gated()
+    ev1.record(cx.stream)
+    cx.stream.synchronize()
+    ms_gated = ev0.elapsed_time(ev1) / n
+    del work, grads, grads_g, gate
+    # kernels per call: chunk table + snapshot entries, the internal forward (schedule + chunk table + its
+    # pass-1 and scan launches), then prep, adjoint scan, value and key
+    sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
+    n_prep, n_scan = piecewise_launches(-(-T // 64)) if H * 2 <= sms else (1, 1)
+    launches = 2 + (2 + n_prep + n_scan) + 4
     return {
         "workload": "KDA prefill backward B=1 H=32 T=8192 d=128, bf16 q/k/v/grad_o, fp32 gates, S0=0, "
                     "grad_S_final given; fp32 gradients of q, k, v, log_alpha, beta, S0",
@@ -759,9 +786,12 @@ def bench_backward(cx: Ctx, args):
                    "unit": "TFLOP/s", "frac": round(achieved_tf / (pk["bf16"] * TF32_OVER_BF16), 4),
                    "flops_per_launch": flops_per_call, "dtype": "tf32 (fp32 operands rounded), fp32 accumulate",
                    "peak_source": pk["src"] + " bf16 burst x nominal tf32/bf16 ratio 1.1/2.25"},
-        "gpu_launches_per_call": 10,
-        "fused_prologue": {"ms_per_call": round(ms_fused, 3), "gpu_launches_per_call": 12,
+        "gpu_launches_per_call": launches,
+        "fused_prologue": {"ms_per_call": round(ms_fused, 3), "gpu_launches_per_call": launches + 2,
                            "what": "kda_prefill_backward_ex, L2 norm of q, k and sigmoid beta fused"},
+        "gated": {"ms_per_call": round(ms_gated, 3), "gpu_launches_per_call": launches + 4,
+                  "what": "kda_prefill_backward_gated: the prologue and the output gate RMSNorm(o) x weight x gate "
+                          "(dL/dgate, dL/dweight out)"},
         "clocks": clk.summary(),
     }
 
