@@ -52,9 +52,10 @@ TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rate
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + PREFILL_BYTES_PER_TOKEN_HEAD  # 132,612
 METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s & % HBM (H=32, d=128)"
 # sources whose ncu DRAM counters profiles/ncu_traffic.json records (null once they change)
-PREFILL_SOURCES = ["kda_api.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh"]
-DECODE_SOURCES = ["kda_decode.cu"]
-BACKWARD_SOURCES = ["kda_api.cu", "kda_backward.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh"]
+PREFILL_SOURCES = ["kda_api.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh", "kda_internal.h"]
+DECODE_SOURCES = ["kda_decode.cu", "kda_ptx.cuh", "kda_internal.h"]
+BACKWARD_SOURCES = ["kda_api.cu", "kda_backward.cu", "kda_prefill_split.cu", "kda_prefill_common.cuh", "kda_ptx.cuh",
+                    "kda_internal.h"]
 
 
 def dist_env():
@@ -516,7 +517,8 @@ def bench_decode(cx: Ctx, args):
              "state_gbs": round(cx.ws * n_units * 2 * STATE_BYTES / (m_ms * 1e-3) / 1e9, 1),
              "bytes_per_launch": n_units * (2 * STATE_BYTES + T_MULTI * PREFILL_BYTES_PER_TOKEN_HEAD),
              "hbm_frac": round(n_units * (2 * STATE_BYTES + T_MULTI * PREFILL_BYTES_PER_TOKEN_HEAD)
-                               / (m_ms * 1e-3) / 1e9 / cx.peaks["hbm"], 4)}
+                               / (m_ms * 1e-3) / 1e9 / cx.peaks["hbm"], 4),
+             "traffic": ncu_traffic("kda_decode_multi_kernel", DECODE_SOURCES)}
     del dm, mq, mk, mv, mla, mb, mo
 
     # decode step with the fused prologue / epilogue (L2 norm of q, k; sigmoid beta; RMSNorm x gate)
