@@ -255,7 +255,7 @@ KDA_API kda_status kda_prefill_ex(const void *q, const void *k, const void *v, k
  * (sequence, head), and dense per-chunk products for everything else.  The
  * gradients are those of the fp32 recurrence on the given inputs; the only
  * bf16 step is the chunkwise forward that supplies the chunk-start states.
- * Results are bitwise repeatable.  grad_q doubles as scratch during the call.
+ * Results are bitwise repeatable.
  *
  * Workspace: >= kda_prefill_backward_workspace_bytes(...) device bytes,
  * 256-byte aligned (KDA_ERR_WORKSPACE below it).  Pointers: 16-byte aligned

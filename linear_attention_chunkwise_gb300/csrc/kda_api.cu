@@ -666,7 +666,6 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     a.dS0 = grad_S0;
     a.rec = reinterpret_cast<float*>(ws + fwd.copies);  // the forward's copies and images are dead now
     a.xbuf = reinterpret_cast<float*>(ws + lay.xbuf);
-    a.u_scratch = grad_q;
     a.device_status = device_status;
     a.total_tokens = total_tokens;
     a.chunk_slots = lay.entries;

@@ -24,12 +24,11 @@
 // and X walks back over chunks as X <- Diag(e^{gC}) X + Diag(e^{gm}) (Qh^T dO + Kh^T dY),
 // dS0 = X before the first chunk.
 //
-// Kernels (all 256 threads, fp32 products on the CUDA cores from shared memory):
+// Kernels (all 256 threads; products on fp32 shared tiles as tf32 mma.sync, fp32 accumulation):
 //   prep      per (chunk, head): the X-independent pieces -> a per-chunk record
 //   scan      per (sequence, head, 32 state columns): the walk of X; writes dv = -dY
 //             and X after every chunk
-//   value     per (chunk, head): U (kept in the grad_q buffer until the key kernel), dbeta
-//   key       per (chunk, head): dq, dk, dlog_alpha
+//   value+key per (chunk, head): U, dbeta, then dq, dk, dlog_alpha (U, dO, dY kept in shared memory)
 // The chunk-start states come from the chunkwise prefill (a snapshot after every chunk).
 #include <cuda_bf16.h>
 
@@ -499,176 +498,32 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
     }
 }
 
-// ================================================================ value =========
-struct ValueL {
+// ========================================================== value + key =========
+// One CTA per (chunk, head) runs the value products (U, R, du, dbeta) and then the key products (dq, dk,
+// dlog alpha): U, dO and dY stay in shared memory between them instead of a round trip through global
+// memory, and the chunk's q, k, log alpha and states are fetched by one CTA, not two.
+struct ValueKeyL {
     static constexpr int T0 = 0, T1 = TILE, T2 = 2 * TILE, T3 = 3 * TILE;
     static constexpr int P0 = 4 * TILE, P1 = P0 + PTILE;
-    static constexpr int ST = P1 + PTILE;        // [32][LDW] state slab, or Tb [64][LDN]
-    static constexpr int VB = ST + PTILE;        // egm[128], egcm[128], dbeta halves [2][64]
+    static constexpr int ST = P1 + PTILE;        // [32][LDW] state slab or Tb [64][LDN]; then [128][LDS] slabs
+    static constexpr int VB = ST + 128 * LDS;    // egm[128], egcm[128], dbeta halves [2][64] / boundary terms
     static constexpr int FLOATS = VB + 384;
 };
-static_assert(32 * LDW <= PTILE, "state slab fits the Tb slot");
+static_assert(32 * LDW <= 128 * LDS && C * LDN <= 128 * LDS, "the value phase's slabs fit the ST slot");
 
+// The key products of one (chunk, head), with dO in T0, U in T1 and dY in T2 already resident; T3
+// takes the gates, ST the state and adjoint column slabs ([128][LDS]).  Ends with dq, dk, dlog alpha.
 template <typename IoT>
-__global__ void __launch_bounds__(BT, 1) kda_bwd_value_kernel(const BackwardArgs a) {
-    extern __shared__ __align__(16) float sm[];
-    using L = ValueL;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos& p, int gc, int h, float* T0, float* T1,
+                                          float* T2, float* T3, float* P0, float* P1, float* ST, float* egm,
+                                          float* egcm, float* bnd, int tid) {
+    const int lane = tid & 31, warp = tid >> 5;
     const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
-    const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
-    ChunkPos p;
-    if (!chunk_pos(a, gc, p)) return;
-    float *T0 = sm + L::T0, *T1 = sm + L::T1, *T2 = sm + L::T2, *T3 = sm + L::T3, *P0 = sm + L::P0,
-          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128, *dbh = egcm + 128;
-    const IoT* k = static_cast<const IoT*>(a.k);
-
-    load_tile(T1, k, p.t0, p.L, H, h, tid);
-    load_tile(T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
-    chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
-    __syncthreads();
-    for (int e = tid; e < C * D; e += BT) {  // T0 = Kh, T1 = Kb, T2 = Qh
-        const int r = e >> 7, i = e & 127;
-        const float x = T3[r * LDW + i] - T3[(C / 2 - 1) * LDW + i];
-        const float ep = expf(x), kv = T1[r * LDW + i];
-        T0[r * LDW + i] = kv * ep;
-        T1[r * LDW + i] = kv * expf(-x);
-        T2[r * LDW + i] *= ep;
-    }
-    __syncthreads();
-    {   // P0 = Lm = strict lower (Kh Kb^T), P1 = Mm = lower (Qh Kb^T)
-        float al[4][4], am[4][4];
-        zero(al);
-        zero(am);
-        mma16<4, AR, BN>(al, T0, LDW, T1, LDW, D, r0, c64, lane);
-        mma16<4, AR, BN>(am, T2, LDW, T1, LDW, D, r0, c64, lane);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = frow(r0, lane, e), s = fcol(c64, lane, j, e);
-                P0[r * LDN + s] = s < r ? al[j][e] : 0.f;
-                P1[r * LDN + s] = s <= r ? am[j][e] : 0.f;
-            }
-    }
-    // Kh Sm, the start state streamed in 32-row slabs
-    float acc[8][4];
-    zero(acc);
-    const float* S = chunk_start_state(a, p, gc, h);
-    if (S) {
-        for (int i0 = 0; i0 < D; i0 += 32) {
-            __syncthreads();
-            load_state_rows<32>(ST, S, i0, egm, tid);
-            __syncthreads();
-            mma16<8, AR, BK>(acc, T0 + i0, LDW, ST, LDW, 32, r0, c128, lane);
-        }
-    }
-    __syncthreads();  // T2 (Qh) and ST are read no more
-    load_tile(T2, static_cast<const IoT*>(a.v), p.t0, p.L, H, h, tid);
-    {
-        const float* tbg = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats + kRecTb;
-#pragma unroll
-        for (int it = 0; it < C * (C / 4) / BT; ++it) {
-            const int e = tid + it * BT, r = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(ST + r * LDN + c4) = *reinterpret_cast<const float4*>(tbg + r * C + c4);
-        }
-    }
-    __syncthreads();
-    float rr[8][4];  // Y1 = V - Kh Sm (own elements), later R
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-            rr[j][e] = T2[r * LDW + i] - acc[j][e];
-        }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) T2[frow(r0, lane, e) * LDW + fcol(c128, lane, j, e)] = rr[j][e];
-    __syncthreads();
-    zero(acc);
-    mma16<8, AR, BK>(acc, ST, LDN, T2, LDW, C, r0, c128, lane);  // U = Tb Y1
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
-            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-            const float2 u = make_float2(acc[j][e], acc[j][e + 1]);
-            *reinterpret_cast<float2*>(T3 + r * LDW + i) = u;
-            if (r < p.L) *reinterpret_cast<float2*>(a.u_scratch + (static_cast<size_t>(p.t0 + r) * H + h) * D + i) = u;
-        }
-    __syncthreads();
-    zero(acc);
-    mma16<8, AR, BK>(acc, P0, LDN, T3, LDW, C, r0, c128, lane);  // Lm U
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) rr[j][e] -= acc[j][e];  // R
-    __syncthreads();  // T2, T3 and ST are read no more
-    load_tile(T2, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
-    load_tile(T3, a.dv, p.t0, p.L, H, h, tid, -1.f);  // dY = -dv
-    __syncthreads();
-    zero(acc);
-    mma16<8, AC, BK>(acc, P1, LDN, T2, LDW, C, r0, c128, lane);  // Mm^T dO
-    mma16<8, AC, BK>(acc, P0, LDN, T3, LDW, C, r0, c128, lane);  // + Lm^T dY
-    {   // + Kb Xc, X streamed in 32-row slabs
-        const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
-        for (int i0 = 0; i0 < D; i0 += 32) {
-            __syncthreads();
-            load_state_rows<32>(ST, X, i0, egcm, tid);
-            __syncthreads();
-            mma16<8, AR, BK>(acc, T1 + i0, LDW, ST, LDW, 32, r0, c128, lane);
-        }
-    }
-    // dbeta_t = <du_t, r_t>: rows g, g + 8 of the warp; columns over the 4 threads of a group
-    // and the two warps (warp, warp + 4) that share the rows
-    float s_lo = 0.f, s_hi = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        s_lo = fmaf(acc[j][0], rr[j][0], fmaf(acc[j][1], rr[j][1], s_lo));
-        s_hi = fmaf(acc[j][2], rr[j][2], fmaf(acc[j][3], rr[j][3], s_hi));
-    }
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, off);
-        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, off);
-    }
-    if ((lane & 3) == 0) {
-        dbh[(warp >> 2) * 64 + frow(r0, lane, 0)] = s_lo;
-        dbh[(warp >> 2) * 64 + frow(r0, lane, 2)] = s_hi;
-    }
-    __syncthreads();
-    if (tid < p.L) a.dbeta[(p.t0 + tid) * H + h] = dbh[tid] + dbh[64 + tid];
-}
-
-// ================================================================ key ===========
-struct KeyL {
-    static constexpr int T0 = 0, T1 = TILE, T2 = 2 * TILE, T3 = 3 * TILE;
-    static constexpr int P0 = 4 * TILE, P1 = P0 + PTILE;
-    static constexpr int ST = P1 + PTILE;        // [128][LDS] state column slab
-    static constexpr int VB = ST + 128 * LDS;    // egm[128], egcm[128], bnd[128]
-    static constexpr int FLOATS = VB + 384;
-};
-
-template <typename IoT>
-__global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a) {
-    extern __shared__ __align__(16) float sm[];
-    using L = KeyL;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
-    const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
-    ChunkPos p;
-    if (!chunk_pos(a, gc, p)) return;
-    float *T0 = sm + L::T0, *T1 = sm + L::T1, *T2 = sm + L::T2, *T3 = sm + L::T3, *P0 = sm + L::P0,
-          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128, *bnd = egcm + 128;
+    const int H = a.H;
     const IoT* q = static_cast<const IoT*>(a.q);
     const IoT* k = static_cast<const IoT*>(a.k);
     const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
 
-    load_tile(T0, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
-    load_tile(T1, a.u_scratch, p.t0, p.L, H, h, tid);
-    load_tile(T2, a.dv, p.t0, p.L, H, h, tid, -1.f);  // dY
     chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
     {   // boundary term of the last row: rowsum(S_next * X), S_next = the snapshot after this chunk
         const float* Sn = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D;
@@ -775,6 +630,144 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_key_kernel(const BackwardArgs a
             a.dla[(static_cast<size_t>(p.t0 + r) * H + h) * D + tid] = s;
         }
     }
+}
+
+
+template <typename IoT>
+__global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const BackwardArgs a) {
+    extern __shared__ __align__(16) float sm[];
+    using L = ValueKeyL;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
+    const int gc = blockIdx.x, h = blockIdx.y, H = a.H;
+    ChunkPos p;
+    if (!chunk_pos(a, gc, p)) return;
+    float *T0 = sm + L::T0, *T1 = sm + L::T1, *T2 = sm + L::T2, *T3 = sm + L::T3, *P0 = sm + L::P0,
+          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128, *dbh = egcm + 128;
+    const IoT* k = static_cast<const IoT*>(a.k);
+
+    load_tile(T1, k, p.t0, p.L, H, h, tid);
+    load_tile(T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
+    chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
+    __syncthreads();
+    for (int e = tid; e < C * D; e += BT) {  // T0 = Kh, T1 = Kb, T2 = Qh
+        const int r = e >> 7, i = e & 127;
+        const float x = T3[r * LDW + i] - T3[(C / 2 - 1) * LDW + i];
+        const float ep = expf(x), kv = T1[r * LDW + i];
+        T0[r * LDW + i] = kv * ep;
+        T1[r * LDW + i] = kv * expf(-x);
+        T2[r * LDW + i] *= ep;
+    }
+    __syncthreads();
+    {   // P0 = Lm = strict lower (Kh Kb^T), P1 = Mm = lower (Qh Kb^T)
+        float al[4][4], am[4][4];
+        zero(al);
+        zero(am);
+        mma16<4, AR, BN>(al, T0, LDW, T1, LDW, D, r0, c64, lane);
+        mma16<4, AR, BN>(am, T2, LDW, T1, LDW, D, r0, c64, lane);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(r0, lane, e), s = fcol(c64, lane, j, e);
+                P0[r * LDN + s] = s < r ? al[j][e] : 0.f;
+                P1[r * LDN + s] = s <= r ? am[j][e] : 0.f;
+            }
+    }
+    // Kh Sm, the start state streamed in 32-row slabs
+    float acc[8][4];
+    zero(acc);
+    const float* S = chunk_start_state(a, p, gc, h);
+    if (S) {
+        for (int i0 = 0; i0 < D; i0 += 32) {
+            __syncthreads();
+            load_state_rows<32>(ST, S, i0, egm, tid);
+            __syncthreads();
+            mma16<8, AR, BK>(acc, T0 + i0, LDW, ST, LDW, 32, r0, c128, lane);
+        }
+    }
+    __syncthreads();  // T2 (Qh) and ST are read no more
+    load_tile(T2, static_cast<const IoT*>(a.v), p.t0, p.L, H, h, tid);
+    {
+        const float* tbg = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats + kRecTb;
+#pragma unroll
+        for (int it = 0; it < C * (C / 4) / BT; ++it) {
+            const int e = tid + it * BT, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4*>(ST + r * LDN + c4) = *reinterpret_cast<const float4*>(tbg + r * C + c4);
+        }
+    }
+    __syncthreads();
+    float rr[8][4];  // Y1 = V - Kh Sm (own elements), later R
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
+            rr[j][e] = T2[r * LDW + i] - acc[j][e];
+        }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) T2[frow(r0, lane, e) * LDW + fcol(c128, lane, j, e)] = rr[j][e];
+    __syncthreads();
+    zero(acc);
+    mma16<8, AR, BK>(acc, ST, LDN, T2, LDW, C, r0, c128, lane);  // U = Tb Y1
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
+            const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
+            const float2 u = make_float2(acc[j][e], acc[j][e + 1]);
+            *reinterpret_cast<float2*>(T3 + r * LDW + i) = u;  // U stays in T3 for the key phase
+        }
+    __syncthreads();
+    zero(acc);
+    mma16<8, AR, BK>(acc, P0, LDN, T3, LDW, C, r0, c128, lane);  // Lm U
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rr[j][e] -= acc[j][e];  // R
+    __syncthreads();  // T0 (Kh), T2 and ST are read no more
+    load_tile(T2, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
+    load_tile(T0, a.dv, p.t0, p.L, H, h, tid, -1.f);  // dY = -dv
+    __syncthreads();
+    zero(acc);
+    mma16<8, AC, BK>(acc, P1, LDN, T2, LDW, C, r0, c128, lane);  // Mm^T dO
+    mma16<8, AC, BK>(acc, P0, LDN, T0, LDW, C, r0, c128, lane);  // + Lm^T dY
+    {   // + Kb Xc, X streamed in 32-row slabs
+        const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
+        for (int i0 = 0; i0 < D; i0 += 32) {
+            __syncthreads();
+            load_state_rows<32>(ST, X, i0, egcm, tid);
+            __syncthreads();
+            mma16<8, AR, BK>(acc, T1 + i0, LDW, ST, LDW, 32, r0, c128, lane);
+        }
+    }
+    // dbeta_t = <du_t, r_t>: rows g, g + 8 of the warp; columns over the 4 threads of a group
+    // and the two warps (warp, warp + 4) that share the rows
+    float s_lo = 0.f, s_hi = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        s_lo = fmaf(acc[j][0], rr[j][0], fmaf(acc[j][1], rr[j][1], s_lo));
+        s_hi = fmaf(acc[j][2], rr[j][2], fmaf(acc[j][3], rr[j][3], s_hi));
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        s_lo += __shfl_xor_sync(0xffffffffu, s_lo, off);
+        s_hi += __shfl_xor_sync(0xffffffffu, s_hi, off);
+    }
+    if ((lane & 3) == 0) {
+        dbh[(warp >> 2) * 64 + frow(r0, lane, 0)] = s_lo;
+        dbh[(warp >> 2) * 64 + frow(r0, lane, 2)] = s_hi;
+    }
+    __syncthreads();
+    if (tid < p.L) a.dbeta[(p.t0 + tid) * H + h] = dbh[tid] + dbh[64 + tid];
+    __syncthreads();  // dbh, Kb (T1), Mm and Lm are read no more
+
+    // ---- key phase: dq, dk, dlog alpha.  dO (T2), U (T3) and dY (T0) are resident; the tiles are
+    // renamed to the key products' roles: K0 = dO, K1 = U, K2 = dY, K3 = the gates (into Kb's tile)
+    key_phase<IoT>(a, p, gc, h, T2, T3, T0, T1, P0, P1, ST, egm, egcm, egcm + 128, tid);
 }
 
 // ============================================================ fused prologue ==
@@ -951,9 +944,7 @@ cudaError_t launch_all(const BackwardArgs& a, int64_t chunk_slots, cudaStream_t 
     if (scan_ctas > 0 &&
         (err = launch_smem(kda_bwd_scan_kernel<IoT>, dim3(scan_ctas), ScanL::FLOATS * 4, a, stream)) != cudaSuccess)
         return err;
-    if ((err = launch_smem(kda_bwd_value_kernel<IoT>, per_chunk, ValueL::FLOATS * 4, a, stream)) != cudaSuccess)
-        return err;
-    return launch_smem(kda_bwd_key_kernel<IoT>, per_chunk, KeyL::FLOATS * 4, a, stream);
+    return launch_smem(kda_bwd_value_key_kernel<IoT>, per_chunk, ValueKeyL::FLOATS * 4, a, stream);
 }
 
 }  // namespace

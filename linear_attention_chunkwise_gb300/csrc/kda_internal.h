@@ -140,7 +140,6 @@ struct BackwardArgs {
     float* dS0 = nullptr;
     float* rec = nullptr;        // per-(chunk, head) records of the prep kernel (backward_record_bytes each)
     float* xbuf = nullptr;       // adjoint of the state after every chunk, indexed like ckpt
-    float* u_scratch = nullptr;  // [T, H, 128] rows u_t between the value and key kernels (may be dq)
     int32_t* device_status = nullptr;
     int64_t total_tokens = 0;
     int64_t chunk_slots = 0;     // chunk entries of ckpt, xbuf and rec
