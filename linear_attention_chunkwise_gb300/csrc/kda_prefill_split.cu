@@ -793,7 +793,8 @@ cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, boo
 // y = o / sqrt(mean_c o_c^2 + eps) * w * g, in place on o, after the scan: the output gate of "kimi
 // delta attn from first principles" (aryagxr), "KDA has three gates".  One warp per (token, head)
 // row, 4 channels per lane; the row's mean square is taken from the row itself, so the scan needs
-// no cross-slice exchange.  Grid-stride over the rows.
+// no cross-slice exchange.  Grid-stride over the rows (8k: 30.6 us at 65 % of DRAM peak; loading four
+// rows per warp before reducing any measured slower, 8k with the gate 344 -> 360 us).
 namespace {
 __device__ __forceinline__ float4 og_ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ float4 og_ld4(const __nv_bfloat16* p) {
