@@ -322,15 +322,17 @@ __global__ void __launch_bounds__(NT, 3)
 // =========================================================== pass 2 ======
 constexpr int NV = 64;  // dv columns per scan CTA
 
-struct ScanSmem {
-    // one operand set per chunk parity
+// NSET operand sets: two (chunk c + 1's copies land while chunk c runs; one CTA per SM) or one
+// (the copies follow the chunk's last use of the set; two CTAs per SM, each hiding the other's waits)
+template <int NSET>
+struct ScanSmemT {
     static constexpr uint32_t SET = 83968;       // 82 KB
     static constexpr uint32_t S_A = 0;           // [2 blk][128 rows][128 B]: [-W; Qh]
     static constexpr uint32_t S_KB = 32768;      // [2 blk][64 rows][128 B]: Kb
     static constexpr uint32_t S_A3 = 49152;      // [Tb | zeros | M] x 64 rows x 128 B
     static constexpr uint32_t S_V = 73728;       // [64 rows][128 B]: v slice (TMA, swizzled)
     static constexpr uint32_t S_EV = 81920;      // f32 [3][128]
-    static constexpr uint32_t OP_SM = 2 * SET;   // [128 rows][128 B]: Sm slice
+    static constexpr uint32_t OP_SM = NSET * SET;  // [128 rows][128 B]: Sm slice
     static constexpr uint32_t OP_U = OP_SM + 16384;  // [64 rows][128 B]: U slice
     static constexpr uint32_t BARS = OP_U + 8192;    // 5 x u64: load0, load1, c1, c2, fin
     static constexpr uint32_t TMEM_SLOT = BARS + 40;
@@ -339,7 +341,10 @@ struct ScanSmem {
     static constexpr uint32_t TOTAL = EVBAR + 16;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
+using ScanSmem = ScanSmemT<2>;
 static_assert(ScanSmem::EVBAR % 8 == 0 && ScanSmem::BARS % 8 == 0, "mbarriers are 8-byte aligned");
+// two one-set CTAs (and the 1 KB the runtime reserves for each) in the SM's 228 KB
+static_assert(2 * (ScanSmemT<1>::ALLOC + 1024) <= 233472, "two one-set scan CTAs per SM");
 // per-warp staging inside a consumed operand set: the state slice (128 rows x 64 fp32 over all warps)
 // fits the [-W; Qh] tile, the output rows (64 rows x 64 columns, at most fp32) the Kb tile
 static_assert(128 * 64 * 4 <= ScanSmem::S_KB - ScanSmem::S_A, "state stage over the [-W; Qh] tile");
@@ -432,10 +437,10 @@ __device__ __forceinline__ void store_out_rows(OutT* dst, int64_t row_stride, in
 // NTS threads in NTS/128 column groups (256: two groups of 32 state columns per thread; 512: four
 // of 16).  Thread (warp w): lane quarter qw = w % 4 (state rows 32 qw + lane, the TMEM lanes it may
 // read), column group cq = w / 4.
-template <typename OutT, int NTS>
-__global__ void __launch_bounds__(NTS, 1)
+template <typename OutT, int NTS, int NSET>
+__global__ void __launch_bounds__(NTS, 3 - NSET)
     kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
-    using L = ScanSmem;
+    using L = ScanSmemT<NSET>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(NTS, 1)
         fence_mbar_init();
         prefetch_tmap(&tm_v);
     }
-    for (int e = tid; e < 2 * 512; e += NTS)  // zero rows of both [Tb | 0 | M] tiles
+    for (int e = tid; e < NSET * 512; e += NTS)  // zero rows of every set's [Tb | 0 | M] tile
         reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp == 0) {
         tmem_alloc(tmem_slot, 256);
@@ -544,12 +549,13 @@ __global__ void __launch_bounds__(NTS, 1)
     constexpr uint32_t TM_DS = 128;
 
     auto issue_loads = [&](int c) {
-        uint8_t* set = sm + (c & 1) * L::SET;
-        uint64_t* bar = &bars[c & 1];
+        const int sb = c % NSET;
+        uint8_t* set = sm + sb * L::SET;
+        uint64_t* bar = &bars[sb];
         const uint8_t* blob = p.blobs + (static_cast<size_t>(jb + c) * H + h) * kPrefillBlobBytes;
         // the exp vectors first, on their own barrier: the state conversion needs only them
-        mbar_arrive_expect_tx(&evbar[c & 1], 1536);
-        bulk_g2s(set + L::S_EV, blob + kBlobEv, 1536, &evbar[c & 1]);
+        mbar_arrive_expect_tx(&evbar[sb], 1536);
+        bulk_g2s(set + L::S_EV, blob + kBlobEv, 1536, &evbar[sb]);
         mbar_arrive_expect_tx(bar, kLoadBytes - 1536);
         bulk_g2s(set + L::S_A, blob + kBlobA, 32768, bar);
         bulk_g2s(set + L::S_KB, blob + kBlobKb, 16384, bar);
@@ -559,7 +565,7 @@ __global__ void __launch_bounds__(NTS, 1)
     };
     if (tid == 0) {
         issue_loads(0);
-        if (nch > 1) issue_loads(1);
+        if (NSET == 2 && nch > 1) issue_loads(1);
     }
     uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] (and evbar[i]) in bit i
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
@@ -571,24 +577,25 @@ __global__ void __launch_bounds__(NTS, 1)
 
     int c_stop = nch;  // the step the loop stopped at (nch when it ran to the end)
     for (int c = 0; c < nch; ++c) {
-        const int b = c & 1;
-        uint8_t* set = sm + b * L::SET;
+        const int b = c & 1;               // TMEM half of this chunk's X
+        const int sb = NSET == 2 ? b : 0;  // its operand set
+        uint8_t* set = sm + sb * L::SET;
         const float* evs = reinterpret_cast<const float*>(set + L::S_EV);
         const int64_t t0 = t_begin + static_cast<int64_t>(c) * C;
         const int Lc = static_cast<int>(t_end - t0 < C ? t_end - t0 : C);
         // Every thread waits for the exp vectors only; the state conversion below overlaps the rest
         // of the copies, which thread 0 waits for before the block barrier (all threads in the last,
         // ragged chunk, whose v rows past the sequence end they clear).
-        const uint32_t par = (ph_load >> b) & 1u;
-        ph_load ^= 1u << b;
+        const uint32_t par = (ph_load >> sb) & 1u;
+        ph_load ^= 1u << sb;
         if (Lc < C) {  // rows of v past the sequence end -> 0
-            if (!mbar_wait_pipe(&bars[b], par)) *abort_s = 1;
+            if (!mbar_wait_pipe(&bars[sb], par)) *abort_s = 1;
             for (int e = tid; e < (C - Lc) * 8; e += NTS) {
                 const int r = Lc + (e >> 3);
                 *reinterpret_cast<uint4*>(set + L::S_V + sw128_chunk(r, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        if (!mbar_wait_pipe(&evbar[b], par)) *abort_s = 1;
+        if (!mbar_wait_pipe(&evbar[sb], par)) *abort_s = 1;
         {  // Sm = Diag(exp(gm)) S -> OP_SM (row rho, chunks PC*cq/8 ..)
             const float sc = evs[rho];
 #pragma unroll
@@ -600,7 +607,7 @@ __global__ void __launch_bounds__(NTS, 1)
             }
         }
         fence_async_smem();
-        if (Lc == C && tid == 0 && !mbar_wait_pipe(&bars[b], par)) *abort_s = 1;
+        if (Lc == C && tid == 0 && !mbar_wait_pipe(&bars[sb], par)) *abort_s = 1;
         tc_fence_before();
         __syncthreads();
         if (*abort_s) {  // a bounded wait expired: every thread sees it after the barrier
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(NTS, 1)
         }
         // the other set held chunk c-1, consumed by the end of the previous step: fetch chunk c+1
         // (a warp other than the MMA issuer issues the copies)
-        if (tid == 32 && c >= 1 && c + 1 < nch) issue_loads(c + 1);
+        if (NSET == 2 && tid == 32 && c >= 1 && c + 1 < nch) issue_loads(c + 1);
         wait_bar(&bars[2], ph_c1);
         tc_fence_after();
         if (qw < 2) {  // U -> OP_U (row r, chunks PC*cq/8 ..)
@@ -687,6 +694,11 @@ __global__ void __launch_bounds__(NTS, 1)
                 static_cast<int64_t>(H) * D, Lc - row0, a, set + L::S_KB + ((qw - 2) + 2 * cq) * (32 * PC * 4),
                 lane);
         }
+        if (NSET == 1 && c + 1 < nch) {  // every read of the set (MMAs, staging) is done: refill it
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 32) issue_loads(c + 1);
+        }
         tc_fence_before();
     }
     __syncthreads();
@@ -696,8 +708,9 @@ __global__ void __launch_bounds__(NTS, 1)
         mma_commit(&bars[4]);
         (void)mbar_wait(&bars[4], 0, kDrainLimit);
         // a step's loads are waited for (to completion) in that step; the next chunk's are issued
-        // after the step's barrier, so only a stop at step 0 leaves chunk 1's (issued up front) in flight
-        if (c_stop == 0 && nch > 1) {
+        // after the step's barrier (one set: at its end), so only a stop at step 0 of the two-set form
+        // leaves chunk 1's (issued up front) in flight
+        if (NSET == 2 && c_stop == 0 && nch > 1) {
             (void)mbar_wait(&evbar[1], 0, kDrainLimit);
             (void)mbar_wait(&bars[1], 0, kDrainLimit);
         }
@@ -772,21 +785,42 @@ cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_
     return launch_chunk_scan(tm_v, a, out_f32, stream);
 }
 
-template <typename OutT>
+template <typename OutT, int NSET>
 cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigned ctas, cudaStream_t stream) {
     constexpr int NTS = 256;  // 512 threads (16 columns each) measured no faster: the chunk is not epilogue-bound
+    constexpr uint32_t alloc = ScanSmemT<NSET>::ALLOC;
     static int configured[64];
-    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, NTS>, ScanSmem::ALLOC, configured);
+    cudaError_t err = set_smem(kda_chunk_scan_kernel<OutT, NTS, NSET>, alloc, configured);
     if (err != cudaSuccess) return err;
-    kda_chunk_scan_kernel<OutT, NTS><<<ctas, NTS, ScanSmem::ALLOC, stream>>>(tm_v, a);
+    if (NSET == 1) {  // all of the unified L1 as shared memory: two CTAs per SM
+        static int carveout[64];
+        err = set_attr_once(kda_chunk_scan_kernel<OutT, NTS, NSET>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                            cudaSharedmemCarveoutMaxShared, carveout);
+        if (err != cudaSuccess) return err;
+    }
+    kda_chunk_scan_kernel<OutT, NTS, NSET><<<ctas, NTS, alloc, stream>>>(tm_v, a);
     return cudaGetLastError();
 }
 
+// One scan CTA per (sequence, head, dv slice).  A grid that fits the GPU at one CTA per SM runs the
+// two-set form (each chain at its shortest).  A larger one runs the one-set form, two CTAs per SM,
+// where that pays (A/B, 32 heads, bitwise-equal outputs): when the grid fits at two per SM (3 x 8192
+// tokens: 0.821 against 0.842 ms, the two-set form leaving a tail wave of whole chains), or when the
+// sequences average at most 32 chunks, so each CTA's start (state, first copies) is hidden behind the
+// other's chain (64 x 1024 tokens: 1.87 against 2.00 ms).  Longer sequences in several waves keep
+// the two-set form (16 x 4096 tokens: 1.82 against 1.87 ms; the varlen mix of 1k-64k tokens even).
 cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
     const unsigned n = static_cast<unsigned>(scan_ctas);
-    return out_f32 ? launch_scan_t<float>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16>(tm_v, a, n, stream);
+    const bool short_chains = a.total_tokens <= static_cast<int64_t>(32 * C) * a.num_seqs;
+    if (scan_ctas > sms && (scan_ctas <= 2LL * sms || short_chains))
+        return out_f32 ? launch_scan_t<float, 1>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16, 1>(tm_v, a, n, stream);
+    return out_f32 ? launch_scan_t<float, 2>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16, 2>(tm_v, a, n, stream);
 }
 
 // ============================================================ output gate ==

@@ -11,7 +11,8 @@ the inputs but the slot, which every build checks (KDA_DEV_BAD_SLOT).
 Each case runs the same call through the release library and the checked one: the status words must
 match and carry no KDA_DEV_BOUNDS, and every output must be bitwise equal (the checks change nothing
 when nothing is out of range).  The cases cover the layouts the kernels index differently: packed
-varlen batches with empty and one-token sequences, the piecewise schedule of long sequences, the
+varlen batches with empty and one-token sequences, scan grids of one and two CTAs per SM, the
+piecewise schedule of long sequences, the
 single-pass path, snapshots, the fused prologue and the output gate, decode with permuted
 and bad slots, multi-token decode over several token batches, the backward (plain, fused, gated),
 and a malformed cu_seqlens.
@@ -73,6 +74,19 @@ def test_prefill_varlen(libs, dtype, path):
     st = _both(libs, lambda s: kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0,
                                                device_status=s, path=path))
     assert st == 0
+
+
+def test_prefill_one_set_scan(libs):
+    # more scan CTAs than SMs: the one-operand-set scan, two CTAs per SM, plain and with snapshots
+    lengths = [300, 0, 64, 1, 129, 200, 65, 63, 513, 7, 1000, 130]
+    H = torch.cuda.get_device_properties(0).multi_processor_count // (2 * len(lengths)) + 1
+    p = synth.prefill_inputs(lengths, H, s0_std=0.02, seed=907, device="cuda")
+    assert _both(libs, lambda s: kda.kda_prefill(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0,
+                                                 device_status=s)) == 0
+    seq = torch.tensor([0, 0, 3, 4, 8, 8, 10, 11], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([64, 300, 1, 129, 448, 513, 1000, 64], dtype=torch.int32, device="cuda")
+    assert _both(libs, lambda s: kda.kda_prefill_snapshots(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, seq,
+                                                           pos, p.S0, device_status=s)) == 0
 
 
 def test_prefill_piecewise_long_sequences(libs):

@@ -77,6 +77,18 @@ def test_expired_waits_report_timeout_and_the_next_call_is_exact(wait_lib, path)
     _check_normal_call(p)
 
 
+def test_expired_waits_in_the_one_set_scan(wait_lib):
+    """A scan grid larger than the SM count runs with one operand set per CTA (two CTAs per SM), whose
+    next chunk's copies are issued at the end of each step: its expired waits wind down the same way."""
+    lengths = [300, 77, 130, 0, 64, 65, 1, 200, 129, 63, 500, 7]
+    H = torch.cuda.get_device_properties(0).multi_processor_count // (2 * len(lengths)) + 1
+    p = synth.prefill_inputs(lengths, H, s0_std=0.02, seed=814, device="cuda")
+    rc, status = _call(wait_lib, p, "two_pass")
+    assert rc == kda.KDA_OK
+    assert status & kda.KDA_DEV_TIMEOUT
+    _check_normal_call(p)
+
+
 def test_expired_waits_with_the_output_gate(wait_lib):
     """With the output gate the scan's waits expire the same way, and the gate's pass after the scan
     (which waits on nothing) still runs to the end of the call."""
