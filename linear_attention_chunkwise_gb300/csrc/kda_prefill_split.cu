@@ -334,8 +334,8 @@ struct ScanSmemT {
     static constexpr uint32_t S_EV = 81920;      // f32 [3][128]
     static constexpr uint32_t OP_SM = NSET * SET;  // [128 rows][128 B]: Sm slice
     static constexpr uint32_t OP_U = OP_SM + 16384;  // [64 rows][128 B]: U slice
-    static constexpr uint32_t BARS = OP_U + 8192;    // 5 x u64: load0, load1, c1, c2, fin
-    static constexpr uint32_t TMEM_SLOT = BARS + 40;
+    static constexpr uint32_t BARS = OP_U + 8192;    // 6 x u64: load0, load1, c1, c2, fin, c3
+    static constexpr uint32_t TMEM_SLOT = BARS + 48;
     static constexpr uint32_t ABORT = TMEM_SLOT + 4;
     static constexpr uint32_t EVBAR = ABORT + 4;     // 2 x u64: a set's exp vectors landed (by chunk parity)
     static constexpr uint32_t TOTAL = EVBAR + 16;
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
     volatile int* abort_s = reinterpret_cast<volatile int*>(sm + L::ABORT);
     if (tid == 0) {
         *abort_s = 0;
-        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
         mbar_init(&evbar[0], 1);
         mbar_init(&evbar[1], 1);
         fence_mbar_init();
@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
         issue_loads(0);
         if (NSET == 2 && nch > 1) issue_loads(1);
     }
-    uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0;  // ph_load: parity of bars[i] (and evbar[i]) in bit i
+    uint32_t ph_load = 0, ph_c1 = 0, ph_c2 = 0, ph_c3 = 0;  // ph_load: parity of bars[i] (and evbar[i]) in bit i
     auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
         if (!mbar_wait_pipe(bar, ph)) *abort_s = 1;
         ph ^= 1u;
@@ -655,10 +655,11 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
 #pragma unroll
             for (int s = 0; s < 4; ++s)  // D_S = Kb^T U
                 mma_bf16(tmem + TM_DS, d_kb + 128 * s, d_u + 128 * s, id_s, s > 0);
+            mma_commit(&bars[3]);  // the state update needs only D_S
 #pragma unroll
             for (int s = 0; s < 4; ++s)  // X += [0; M] U  (zero rows, then M, at 8 KB into the tile)
                 mma_bf16(tx, d_a3 + 512 + 2 * s, d_u + 128 * s, id_o, 1u);
-            mma_commit(&bars[3]);
+            mma_commit(&bars[5]);  // the output rows
         }
         wait_bar(&bars[3], ph_c2);
         tc_fence_after();
@@ -682,6 +683,8 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
             }
         }
         if (qw >= 2) {  // O rows -> global
+            wait_bar(&bars[5], ph_c3);
+            tc_fence_after();
             float a[PC];
             tmem_ld_cols<PC>(tq + TM_X + 64 * b + PC * cq, a);
             tmem_ld_wait();
