@@ -222,15 +222,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 // so one per row would stall the chain) come into shared memory, and the SM's
 // share of HBM stays busy through the token chain.  Tokens past the first NB
 // of a unit are read with plain loads when their batch starts.  Measured at
-// 256 x 32 units, bf16: T = 4 in 198 us (16-byte
-// cp.async pieces for the state instead: 202-207 us; a CTA per unit with
+// 256 x 32 units, bf16: T = 4 in 186 us (the state blocks packed without
+// padding, so a quarter-warp's two row groups read the same banks: 198 us;
+// 16-byte cp.async pieces for the state: 202-207 us; a CTA per unit with
 // two block barriers per token: 253 us).
 template <typename IoT>
 struct MultiLayout {
     static constexpr int NB = sizeof(IoT) == 2 ? 8 : 4;           // tokens per batch (two CTAs per SM fit)
     static constexpr uint32_t ROW = kHeadDim * sizeof(IoT);         // one token's q / k / v / gate row
-    static constexpr uint32_t STATE = 0;                            // f32 [128][128], as in HBM
-    static constexpr uint32_t Q = kHeadDim * kHeadDim * 4;          // IoT [NB][128] each
+    // f32 [8 blocks][16 rows][128], block b (one bulk copy) at b * BLK floats: 16 floats of padding
+    // per block put the row groups a quarter-warp reads (16 rows apart) in different banks
+    static constexpr uint32_t BLK = 16 * kHeadDim + 16;
+    static constexpr uint32_t STATE = 0;
+    static constexpr uint32_t Q = 8 * BLK * 4;                      // IoT [NB][128] each
     static constexpr uint32_t K = Q + NB * ROW;
     static constexpr uint32_t V = K + NB * ROW;
     static constexpr uint32_t G = V + NB * ROW;
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     auto fetch_state = [&](int u, int32_t slot) {
         if (slot >= 0 && slot < num_slots && lane == 0)
-            bulk_g2s(st_buf + warp * 16 * kHeadDim,
+            bulk_g2s(st_buf + warp * L::BLK,
                      S + ((static_cast<size_t>(slot) * H + (u % H)) * kHeadDim + 16 * warp) * kHeadDim,
                      16 * kHeadDim * 4u, bar);
     };
@@ -401,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         float4 s[16];
         if (valid) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) s[i] = *reinterpret_cast<const float4*>(st_buf + (r0 + i) * kHeadDim + c0);
+            for (int i = 0; i < 16; ++i)
+                s[i] = *reinterpret_cast<const float4*>(st_buf + (lane >> 2) * L::BLK + i * kHeadDim + c0);
         }
         if (warp < nb0) convert_token(warp, true, 0);
         if (un < units) post_state(nslot);
