@@ -78,7 +78,10 @@ int sm_count() {
 // (launch, state carry, first copies), which bounds the piece count.
 constexpr int64_t kScanPieceChunks = 48;  // smallest scan piece (chunks per sequence); each piece costs a few us
 constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
-constexpr double kPrepLag = 0.1;           // lead of pass 1, as a fraction of the chunks scanned after piece 0
+// lead of pass 1, as a fraction of the chunks scanned after piece 0 (A/B of 0.1 / 0.05 / 0.02 / 0: 8k
+// 322 / 317 / 319 / 321 us, 1M tokens 28.15 / 27.46 / 27.30 / 27.32 ms, two 32k sequences 2.10 / 2.11 /
+// 2.11 / 2.11 ms)
+constexpr double kPrepLag = 0.05;
 constexpr double kPrepLagPrologue = 0.2;   // the same with the fused prologue (a slower pass 1; 8k: 345 -> 337 us)
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
