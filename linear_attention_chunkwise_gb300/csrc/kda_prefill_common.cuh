@@ -189,10 +189,12 @@ __device__ __forceinline__ uint2 pack4(float a, float b, float c, float d) {
 }
 
 //   g    : this thread's log_alpha rows from gate_load4 (overwritten)
-//   opa, opkb, Lc, beta_s, beta_cur, egm/egc/egcm, inv_norm: as gate_chunk; red: f32 [8][128] scratch
+//   opa, opkb, Lc, beta_s, beta_cur, egm/egc/egcm: as gate_chunk; red: f32 [8][128] scratch
+//   l2n  : the fused L2 normalisation of the k and q rows, 1 / sqrt(|row|^2 + eps): the warp holds
+//          whole rows, so each row's sum of squares is a butterfly over its lanes
 __device__ __forceinline__ void gate_chunk4(float4 (&g)[8], uint8_t* opa, uint8_t* opkb, int Lc, float* red,
                                             float* beta_s, float beta_cur, float* egm, float* egc, float* egcm,
-                                            int tid, const float* inv_norm = nullptr) {
+                                            int tid, bool l2n = false, float eps = 0.f) {
     const int c4 = tid & 31, rg = tid >> 5;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -234,8 +236,15 @@ __device__ __forceinline__ void gate_chunk4(float4 (&g)[8], uint8_t* opa, uint8_
             const uint2 qw = *reinterpret_cast<const uint2*>(opa + qoff);
             k01 = unpack_bf16(kw.x); k23 = unpack_bf16(kw.y);
             q01 = unpack_bf16(qw.x); q23 = unpack_bf16(qw.y);
-            if (inv_norm) {  // fused L2 normalisation of k and q rows
-                const float ik = inv_norm[r], iq = inv_norm[64 + r];
+            if (l2n) {  // fused L2 normalisation of k and q rows (r < Lc is uniform over the warp)
+                float sk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
+                float sq = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                }
+                const float ik = rsqrtf(sk + eps), iq = rsqrtf(sq + eps);
                 k01.x *= ik; k01.y *= ik; k23.x *= ik; k23.y *= ik;
                 q01.x *= iq; q01.y *= iq; q23.x *= iq; q23.y *= iq;
             }
@@ -244,22 +253,6 @@ __device__ __forceinline__ void gate_chunk4(float4 (&g)[8], uint8_t* opa, uint8_
         *reinterpret_cast<uint2*>(opa + qoff) = pack4(q01.x * e0, q01.y * e1, q23.x * e2, q23.y * e3);
         *reinterpret_cast<uint2*>(opkb + sw128_off(r, 4 * c4, 8192)) =
             pack4(k01.x * f0, k01.y * f1, k23.x * f2, k23.y * f3);
-    }
-}
-
-// 1 / sqrt(|x|^2 + eps) of the 128 rows of an operand tile [2 blk][128 rows][128 B]
-// (rows 0..63 k, 64..127 q) into inv[128]; all NT threads, no barrier inside.
-__device__ __forceinline__ void row_inv_norms(const uint8_t* opa, float eps, float* inv, int tid) {
-    const int warp = tid >> 5, lane = tid & 31;
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-        const int r = 16 * warp + i;
-        const uint2 w = *reinterpret_cast<const uint2*>(opa + sw128_off(r, 4 * lane, 16384));
-        const float2 a = unpack_bf16(w.x), b = unpack_bf16(w.y);
-        float ss = a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) inv[r] = rsqrtf(ss + eps);
     }
 }
 

@@ -141,8 +141,7 @@ struct PrepSmem {
     static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [8][128] gate partial sums (Tb rows, gate phase)
     static constexpr uint32_t EV = 65536;        // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
     static constexpr uint32_t BETA = EV + 1536;  // f32 [64]
-    static constexpr uint32_t INV = BETA + 256;  // f32 [128]: 1/|row| of k (0..63) and q (64..127)
-    static constexpr uint32_t BARS = INV + 512;  // 2 x u64: q/k loaded, mma
+    static constexpr uint32_t BARS = BETA + 256;  // 2 x u64: q/k loaded, mma
     static constexpr uint32_t TMEM_SLOT = BARS + 16;
     static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
@@ -224,13 +223,8 @@ __global__ void __launch_bounds__(NT, 3)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tq = tmem + tmem_lane(qw);
 
-    float* inv = nullptr;
-    if (p.fuse_flags & KDA_FUSE_L2NORM_QK) {  // read by gate_chunk after its internal barrier
-        inv = reinterpret_cast<float*>(sm + L::INV);
-        row_inv_norms(sm + L::OP_A, p.l2_eps, inv, tid);
-    }
     gate_chunk4(g, sm + L::OP_A, sm + L::OP_KB, Lc, reinterpret_cast<float*>(sm + L::RED), beta_s, beta_cur, ev,
-                ev + 128, ev + 256, tid, inv);
+                ev + 128, ev + 256, tid, (p.fuse_flags & KDA_FUSE_L2NORM_QK) != 0, p.l2_eps);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
