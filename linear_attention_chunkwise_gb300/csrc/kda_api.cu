@@ -82,7 +82,9 @@ constexpr int64_t kMaxScanPieces = 32;     // longer sequences get longer pieces
 // 322 / 317 / 319 / 321 us, 1M tokens 28.15 / 27.46 / 27.30 / 27.32 ms, two 32k sequences 2.10 / 2.11 /
 // 2.11 / 2.11 ms)
 constexpr double kPrepLag = 0.05;
-constexpr double kPrepLagPrologue = 0.2;   // the same with the fused prologue (a slower pass 1; 8k: 345 -> 337 us)
+// the same with the fused prologue (a slower pass 1): A/B of 0.2 / 0.1 / 0.05, 8k with the prologue
+// 337.1 / 333.8 / 339.2 us, with every fusion 372.1 / 369.3 / 375.8 us
+constexpr double kPrepLagPrologue = 0.1;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
