@@ -305,10 +305,14 @@ __device__ __forceinline__ void store_tb(uint8_t* tile, const Rows64& Tf, const 
 // for block distance d = R - I = 1, 2, 3.  All NT threads; ends synchronised.
 // Diagonal 16 x 16 blocks of T = (I + N)^-1 by forward substitution (warps 0..3, one column per
 // lane of the first half-warp).  No barrier inside.
+__device__ __forceinline__ void lower_inverse_diag_col(const Rows64& Nf, const Rows64& Tf, int B, int j);
 __device__ __forceinline__ void lower_inverse_diag(const Rows64& Nf, const Rows64& Tf, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
-    if (warp < 4 && lane < 16) {
-        const int B = warp, j = lane;
+    if (warp < 4 && lane < 16) lower_inverse_diag_col(Nf, Tf, warp, lane);
+}
+// Column j of diagonal block B of T by forward substitution (one thread).
+__device__ __forceinline__ void lower_inverse_diag_col(const Rows64& Nf, const Rows64& Tf, int B, int j) {
+    {
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -386,10 +390,13 @@ __device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf
 // warps), X staged through the warp's own 16 x 8 slot of Xs (f32 [6][16][8]).  Three block
 // barriers instead of six, and a fraction of the instructions of the CUDA-core products; the
 // operands are rounded to tf32 (2^-11), below the bf16 rounding Tb takes afterwards.  Needs NT >= 192
-// threads; ends synchronised.
-__device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
-    lower_inverse_diag(Nf, Tf, tid);
-    __syncthreads();
+// threads; ends synchronised.  diag_done: the caller has solved the diagonal blocks and synchronised.
+__device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid,
+                                                 bool diag_done = false) {
+    if (!diag_done) {
+        lower_inverse_diag(Nf, Tf, tid);
+        __syncthreads();
+    }
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     float* xs = Xs + warp * 128;  // [16][8]

@@ -266,8 +266,15 @@ __global__ void __launch_bounds__(NT, 3)
             store_m_row(sm + L::OP_A3, 64 + rr, rr, hw, a);
         }
     }
+    // The 16 x 16 diagonal blocks of T lie in the N rows a warp has just written: warp 0 holds rows and
+    // columns 0..31 (blocks 0, 1), warp 5 rows and columns 32..63 (blocks 2, 3); each solves its two
+    // blocks, a column per lane, without waiting for the other warps.
+    if (warp == 0 || warp == 5) {
+        __syncwarp();
+        lower_inverse_diag_col(rows64(Nf), Tf, (warp == 0 ? 0 : 2) + (lane >> 4), lane & 15);
+    }
     __syncthreads();
-    lower_inverse_tc(rows64(Nf), Tf, reinterpret_cast<float*>(sm + L::XS), tid);
+    lower_inverse_tc(rows64(Nf), Tf, reinterpret_cast<float*>(sm + L::XS), tid, true);
     store_tb(sm + L::OP_A3, Tf, beta_s, tid);
     fence_async_smem();
     tc_fence_before();
