@@ -64,8 +64,8 @@ int sm_count() {
     return count[dev];
 }
 
-// Piecewise schedule of the two-pass prefill.  When the scan has no more CTAs
-// than the GPU has SMs (few sequences), the scan runs in pieces of 48 or more
+// Piecewise schedule of the two-pass prefill.  When the scan takes at most half
+// of the GPU's SMs (few sequences), the scan runs in pieces of 48 or more
 // chunks per sequence (at most 32 pieces) and pass 1 runs ahead of it, all on
 // the caller's stream: a first pass-1 launch prepares a lead of chunks on the
 // whole GPU; then each scan piece is followed by the next pass-1 share,
@@ -376,7 +376,10 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const int64_t sq = (seq_chunks + (seq_chunks + sq0 - 1) / sq0 - 1) / ((seq_chunks + sq0 - 1) / sq0);
         const int64_t pieces = (seq_chunks + sq - 1) / sq;
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        const bool piecewise = pieces > 1 && static_cast<int64_t>(num_seqs) * H * 2 <= sm_count() &&
+        // (a scan on more than half the SMs leaves pass 1 too few beside it: A/B, one prep + one scan
+        // instead, 2 x 8192 tokens x 32 heads 559 -> 497 us, 4 x 16k x 16 heads 1267 -> 940 us, 3 x 32k x 16
+        // heads 1779 -> 1552 us; two sequences of 32k + 20k tokens x 24 heads 1389 -> 1409 us)
+        const bool piecewise = pieces > 1 && 2 * (static_cast<int64_t>(num_seqs) * H * 2) <= sm_count() &&
                                cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
         if (!piecewise)
             return out_gate(kda::launch_prefill_split(tm_q, tm_k, tm_v, a, max_chunks(num_seqs, total_tokens), out_f32,
