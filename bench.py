@@ -282,7 +282,7 @@ class CopyOverlap:
         self.cs.wait_stream(self.d2h)
 
 
-def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.1):
+def piecewise_launches(seq_chunks: int, min_piece: int = 48, max_pieces: int = 32, lag: float = 0.05):
     """(pass-1 launches, scan launches) of the library's piecewise prefill schedule for one sequence
     of seq_chunks chunks: the piece count from pieces of max(min_piece, ceil(n / max_pieces)) chunks,
     then equal pieces of sq chunks; pass 1 a lead of sq + lag * sq * (pieces - 1) chunks, then
@@ -429,7 +429,7 @@ def bench_prefill(cx: Ctx, args):
     # kernels per call: schedule + chunk table + the pass-1 and scan launches of the piecewise
     # schedule (one sequence here, so the scan leaves SMs idle), else one prep + one scan
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
-    n_prep, n_scan = piecewise_launches(-(-T // 64)) if H * 2 <= sms else (1, 1)
+    n_prep, n_scan = piecewise_launches(-(-T // 64)) if 2 * H * 2 <= sms else (1, 1)
     pk = cx.peaks
     return {
         "value": whole_job_mtok_s(T, cx.ws, ms),
@@ -771,7 +771,7 @@ def bench_backward(cx: Ctx, args):
     # kernels per call: chunk table + snapshot entries, the internal forward (schedule + chunk table + its
     # pass-1 and scan launches), then prep, adjoint scan, value and key
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
-    n_prep, n_scan = piecewise_launches(-(-T // 64)) if H * 2 <= sms else (1, 1)
+    n_prep, n_scan = piecewise_launches(-(-T // 64)) if 2 * H * 2 <= sms else (1, 1)
     launches = 2 + (2 + n_prep + n_scan) + 4
     return {
         "workload": "KDA prefill backward B=1 H=32 T=8192 d=128, bf16 q/k/v/grad_o, fp32 gates, S0=0, "
