@@ -14,7 +14,8 @@
 //             exp(gm), exp(gC), exp(gC-gm) (3 x 512 B)
 //   pass 2  scan, one CTA per (sequence, head, 64-column slice of dv): the
 //           sequential chain only.  Per chunk it bulk-copies the images (one
-//           chunk ahead, double-buffered), TMA-loads its slice of v, and runs
+//           chunk ahead into a second operand set; grids larger than one wave
+//           use a single set, two CTAs per SM), TMA-loads its slice of v, and runs
 //             X  = [Tb; 0] V + [-W; Qh] Sm      (= [U; Qh Sm])
 //             D_S = Kb^T U,  X += [0; M] U      (= [U; O])
 //             S <- Diag(exp(gC)) S + Diag(exp(gC-gm)) D_S
