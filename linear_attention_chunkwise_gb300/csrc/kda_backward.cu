@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
             }
     }
     __syncthreads();
-    pf::lower_inverse(pf::rows64(NF), pf::rows64(TF), XS, tid);  // T = (I + N)^-1, ends synchronised
+    pf::lower_inverse_tc(pf::rows64(NF), pf::rows64(TF), XS, tid);  // T = (I + N)^-1, ends synchronised
     for (int e = tid; e < C * C; e += BT) {
         const int r = e >> 6, s = e & 63;
         const float tb = s <= r ? pf::m1(TF, r, s) * bet[s] : 0.f;

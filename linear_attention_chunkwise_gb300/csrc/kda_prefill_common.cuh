@@ -300,11 +300,8 @@ __device__ __forceinline__ void store_tb(uint8_t* tile, const Rows64& Tf, const 
     }
 }
 
-// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
-// diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
-// for block distance d = R - I = 1, 2, 3.  All NT threads; ends synchronised.
-// Diagonal 16 x 16 blocks of T = (I + N)^-1 by forward substitution (warps 0..3, one column per
-// lane of the first half-warp).  No barrier inside.
+// Diagonal 16 x 16 blocks of T = (I + N)^-1 for strictly lower N (64 x 64, fp32) by forward
+// substitution (warps 0..3, one column per lane of the first half-warp).  No barrier inside.
 __device__ __forceinline__ void lower_inverse_diag_col(const Rows64& Nf, const Rows64& Tf, int B, int j);
 __device__ __forceinline__ void lower_inverse_diag(const Rows64& Nf, const Rows64& Tf, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
@@ -339,56 +336,13 @@ __device__ __forceinline__ void lower_inverse_diag_col(const Rows64& Nf, const R
     }
 }
 
-// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks:
-// diagonal blocks by forward substitution, then T_RI = -T_RR sum_J N_RJ T_JI
-// for block distance d = R - I = 1, 2, 3, in fp32.  All NT threads; ends synchronised.
-__device__ __forceinline__ void lower_inverse(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid) {
-    lower_inverse_diag(Nf, Tf, tid);
-    __syncthreads();
-    const int I = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
-#pragma unroll 1
-    for (int d = 1; d <= 3; ++d) {
-        const bool act = I < 4 - d;
-        const int R = I + d;
-        if (act) {
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-            for (int J = I; J < R; ++J) {
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
-                    const float4 nv = m4(Nf, 16 * R + r, 4 * J + mm);
-                    acc0 = fma4(nv.x, m4(Tf, 16 * J + 4 * mm + 0, 4 * I + cq), acc0);
-                    acc1 = fma4(nv.y, m4(Tf, 16 * J + 4 * mm + 1, 4 * I + cq), acc1);
-                    acc0 = fma4(nv.z, m4(Tf, 16 * J + 4 * mm + 2, 4 * I + cq), acc0);
-                    acc1 = fma4(nv.w, m4(Tf, 16 * J + 4 * mm + 3, 4 * I + cq), acc1);
-                }
-            }
-            reinterpret_cast<float4*>(Xs)[(I * 16 + r) * 4 + cq] =
-                make_float4(acc0.x + acc1.x, acc0.y + acc1.y, acc0.z + acc1.z, acc0.w + acc1.w);
-        }
-        __syncthreads();
-        if (act) {
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-            const float4* X4 = reinterpret_cast<const float4*>(Xs);
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const float4 tv = m4(Tf, 16 * R + r, 4 * R + mm);
-                acc0 = fma4(tv.x, X4[(I * 16 + 4 * mm + 0) * 4 + cq], acc0);
-                acc1 = fma4(tv.y, X4[(I * 16 + 4 * mm + 1) * 4 + cq], acc1);
-                acc0 = fma4(tv.z, X4[(I * 16 + 4 * mm + 2) * 4 + cq], acc0);
-                acc1 = fma4(tv.w, X4[(I * 16 + 4 * mm + 3) * 4 + cq], acc1);
-            }
-            m4(Tf, 16 * R + r, 4 * I + cq) = make_float4(-(acc0.x + acc1.x), -(acc0.y + acc1.y),
-                                                         -(acc0.z + acc1.z), -(acc0.w + acc1.w));
-        }
-        __syncthreads();
-    }
-}
-
-// The same inverse with the off-diagonal block products on the tensor cores: per level d,
+// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks: the diagonal blocks by
+// forward substitution (lower_inverse_diag), then, with the off-diagonal block products on the
+// tensor cores, per level d,
 //   X = sum_{J=I}^{R-1} N_RJ T_JI,  T_RI = -T_RR X   (R = I + d)
 // as tf32 mma.sync products with fp32 accumulation, one warp per 16 x 8 column tile of T_RI (2 (4 - d)
 // warps), X staged through the warp's own 16 x 8 slot of Xs (f32 [6][16][8]).  Three block
-// barriers instead of six, and a fraction of the instructions of the CUDA-core products; the
+// barriers instead of six and a fraction of the instructions of products on the CUDA cores; the
 // operands are rounded to tf32 (2^-11), below the bf16 rounding Tb takes afterwards.  Needs NT >= 192
 // threads; ends synchronised.  diag_done: the caller has solved the diagonal blocks and synchronised.
 __device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid,
