@@ -336,3 +336,17 @@ def test_backward_gated_8k_sampled_heads():
     torch.cuda.synchronize()
     heads = [0, 31]
     _compare_gated(got, _gated_oracle(p, dY, dSf, gate, w, True, True, heads), heads, with_dw=False)
+
+
+def test_backward_one_set_forward_grid():
+    # more scan CTAs than SMs: the internal forward (a snapshot after every chunk) runs the scan's
+    # one-operand-set form, two CTAs per SM; three sampled heads against the oracle
+    lengths = [130, 0, 7, 64, 300, 1, 129, 65, 513, 63, 200, 33]
+    H = torch.cuda.get_device_properties(0).multi_processor_count // (2 * len(lengths)) + 1
+    p = synth.prefill_inputs(lengths, H=H, s0_std=0.02, seed=91)
+    dO, dSf = _cotangents(p, 92)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _gpu(p, dO, dSf, status)
+    assert int(status.item()) == 0
+    heads = [0, H // 2, H - 1]
+    _compare(got, _oracle(p, dO, dSf, heads), heads)

@@ -259,3 +259,20 @@ def test_decode_multi_fused_prologue_only(dtype):
     assert rell2(host(d.S), S_ref) < 1e-4
     # the last step's state is the state written back
     assert torch.equal(steps[:, T - 1], d.S[d.state_indices.long()])
+
+
+def test_prefill_fused_one_set_scan_grid():
+    # more scan CTAs (sequences x heads x 2) than SMs: the scan's one-operand-set form, two CTAs per SM,
+    # with the fused prologue in pass 1 and the output gate after the scan
+    lengths = [130, 0, 7, 64, 300, 1, 129, 65, 513, 63, 200, 33]
+    H = torch.cuda.get_device_properties(0).multi_processor_count // (2 * len(lengths)) + 1
+    p, gate, w = _raw_inputs(lengths, H, torch.bfloat16, 631)
+    fz = kda.Fusion(l2norm_qk=True, beta_sigmoid=True, l2_eps=L2_EPS, out_gate=gate, rms_weight=w, rms_eps=RMS_EPS)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, sf = kda.kda_prefill_ex(p.q, p.k, p.v, p.log_alpha, p.beta, p.cu_seqlens, p.S0, fusion=fz,
+                               device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    heads = [0, H // 2, H - 1]
+    outs, finals = _oracle(p, gate, w, heads)
+    _check(p, o, sf, outs, finals, heads)
