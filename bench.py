@@ -426,15 +426,15 @@ def bench_prefill(cx: Ctx, args):
     chain = {"us": chain_us, "frac": round(chain_us / (ms * 1e3), 4),
              "what": "the same 8192-token sequence with 1 head: the scan's 128-chunk serial chain with the GPU "
                      "otherwise idle; frac = that floor / this call's time"}
-    # kernels per call: schedule + chunk table + the pass-1 and scan launches of the piecewise
-    # schedule (one sequence here, so the scan leaves SMs idle), else one prep + one scan
+    # kernels per call: the chunk table (one sequence: no schedule kernel) + the pass-1 and scan launches
+    # of the piecewise schedule (the scan leaves SMs idle), else one prep + one scan
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
     n_prep, n_scan = piecewise_launches(-(-T // 64)) if 2 * H * 2 <= sms else (1, 1)
     pk = cx.peaks
     return {
         "value": whole_job_mtok_s(T, cx.ws, ms),
         "ms": ms,
-        "launches": (2 + n_prep + n_scan) * args.steps,
+        "launches": (1 + n_prep + n_scan) * args.steps,
         "variants": variants,
         "chain_bound": chain,
         "tokens": T,
@@ -768,11 +768,11 @@ def bench_backward(cx: Ctx, args):
     cx.stream.synchronize()
     ms_gated = ev0.elapsed_time(ev1) / n
     del work, grads, grads_g, gate
-    # kernels per call: chunk table + snapshot entries, the internal forward (schedule + chunk table + its
-    # pass-1 and scan launches), then prep, adjoint scan, value and key
+    # kernels per call: chunk table + snapshot entries, the internal forward (chunk table + its pass-1 and
+    # scan launches; one sequence: no schedule kernel), then prep, adjoint scan and value+key
     sms = torch.cuda.get_device_properties(cx.dev).multi_processor_count
     n_prep, n_scan = piecewise_launches(-(-T // 64)) if 2 * H * 2 <= sms else (1, 1)
-    launches = 2 + (2 + n_prep + n_scan) + 4
+    launches = 2 + (1 + n_prep + n_scan) + 3
     return {
         "workload": "KDA prefill backward B=1 H=32 T=8192 d=128, bf16 q/k/v/grad_o, fp32 gates, S0=0, "
                     "grad_S_final given; fp32 gradients of q, k, v, log_alpha, beta, S0",

@@ -332,14 +332,18 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         return KDA_ERR_CUDA;
     const bool og = (fz.flags & KDA_FUSE_OUT_GATE) != 0;
 
-    if (kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
+    // the longest-first order of the sequences; one sequence in the two-pass path needs none (its chunk
+    // table kernel checks cu_seqlens as the schedule kernel does)
+    const bool need_order = !two_pass || num_seqs > 1;
+    if (need_order &&
+        kda::launch_schedule(cu_seqlens, num_seqs, total_tokens, order, device_status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     kda::PrefillArgs a;
     a.log_alpha = log_alpha;
     a.beta = beta;
     a.S0 = S0;
     a.cu_seqlens = cu_seqlens;
-    a.order = order;
+    a.order = need_order ? order : nullptr;
     a.chunk_off = two_pass ? reinterpret_cast<const int32_t*>(ws + two.table) : nullptr;
     a.blobs = two_pass ? ws + two.blobs : nullptr;
     a.blob_units = two_pass ? static_cast<int64_t>(max_chunks(num_seqs, total_tokens)) * H : 0;
@@ -661,7 +665,7 @@ kda_status backward_impl(const void* q, const void* k, const void* v, kda_dtype 
     a.beta = bc;
     a.S0 = S0;
     a.cu_seqlens = cu_seqlens;
-    a.order = reinterpret_cast<const int32_t*>(ws);  // the prefill's schedule
+    a.order = num_seqs > 1 ? reinterpret_cast<const int32_t*>(ws) : nullptr;  // the prefill's schedule
     a.chunk_off = chunk_off;
     a.ckpt = ckpt;
     a.dO = gate ? static_cast<const void*>(ws + lay.o) : grad_o;

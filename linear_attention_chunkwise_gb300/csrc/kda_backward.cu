@@ -411,7 +411,8 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
     const int H = a.H, N = a.num_seqs;
     if (a.chunk_off[N + 1] == 0) return;
     const int unit = blockIdx.x;  // (rank of the sequence, longest first) x H x slices
-    const int n = a.order[unit / (H * kSlices)], h = (unit / kSlices) % H, c0 = (unit % kSlices) * NCS;
+    const int pos = unit / (H * kSlices);
+    const int n = a.order ? a.order[pos] : pos, h = (unit / kSlices) % H, c0 = (unit % kSlices) * NCS;
     if (!KDA_BOUNDS(n >= 0 && n < N && h < H, a.device_status)) return;
     float *XS = sm + L::XS, *DY = sm + L::DY;
     const size_t sidx = (static_cast<size_t>(n) * H + h) * D * D;

@@ -57,7 +57,7 @@ struct PrefillArgs {
     const float* beta;
     const float* S0;
     const int32_t* cu_seqlens;
-    const int32_t* order;      // schedule: longest sequences first (workspace)
+    const int32_t* order;      // schedule: longest sequences first (workspace), or NULL (one sequence)
     const int32_t* chunk_off;  // two-pass path: chunk offsets [N + 2] (workspace)
     uint8_t* blobs;            // two-pass path: per (chunk, head) operand images (workspace)
     void* o;
@@ -127,7 +127,7 @@ struct BackwardArgs {
     const float* beta = nullptr;
     const float* S0 = nullptr;
     const int32_t* cu_seqlens = nullptr;
-    const int32_t* order = nullptr;      // sequences, longest first
+    const int32_t* order = nullptr;      // sequences, longest first (NULL: in index order, one sequence)
     const int32_t* chunk_off = nullptr;  // chunk table
     const float* ckpt = nullptr;         // state after every chunk: entry (chunk_off[n] + c) x H + h
     const void* dO = nullptr;
