@@ -100,10 +100,41 @@ __device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16* p) {
 //   BK: B(k, n) = B[k * ldb + n]     BN: B(k, n) = B[n * ldb + k]
 enum { AR = 0, AC = 1, BK = 0, BN = 1 };
 
+// Inside a k-step the fragments may take the step's eight k indices in any order that A and B
+// share.  With B(k, n) = B[k * ldb + n] (BK) lane (g, t) takes k = 2t, 2t + 1 instead of the
+// fragment's t, t + 4: for the tiles' row strides (4 mod 32 words) the B reads then fall on 32
+// distinct banks (t, t + 4 put two lanes on each of 16 banks), and so do the AC reads of A; the AR
+// reads of A, a quarter of the loads, become two-way.
 template <int NT, int AM, int BM>
 __device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int lda, const float* B, int ldb, int K,
                                       int r0, int c0, int lane) {
     const int g = lane >> 2, t = lane & 3;
+    if constexpr (BM == BK) {
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            const int k = k0 + 2 * t;
+            uint32_t a[4];
+            if (AM == AR) {
+                const float2 lo = *reinterpret_cast<const float2*>(A + (r0 + g) * lda + k);
+                const float2 hi = *reinterpret_cast<const float2*>(A + (r0 + g + 8) * lda + k);
+                a[0] = to_tf32(lo.x);
+                a[1] = to_tf32(hi.x);
+                a[2] = to_tf32(lo.y);
+                a[3] = to_tf32(hi.y);
+            } else {
+                a[0] = to_tf32(A[k * lda + r0 + g]);
+                a[1] = to_tf32(A[k * lda + r0 + g + 8]);
+                a[2] = to_tf32(A[(k + 1) * lda + r0 + g]);
+                a[3] = to_tf32(A[(k + 1) * lda + r0 + g + 8]);
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int n = c0 + 8 * j + g;
+                mma_tf32(acc[j], a, to_tf32(B[k * ldb + n]), to_tf32(B[(k + 1) * ldb + n]));
+            }
+        }
+        return;
+    }
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t a[4];
@@ -158,40 +189,54 @@ __device__ __forceinline__ void load_tile(float* dst, const T* src, int64_t t0, 
             make_float4(v[it].x * scale, v[it].y * scale, v[it].z * scale, v[it].w * scale);
     }
 }
-// ROWS x 128 fp32 rows of a state (stride 128) starting at row i0, each row scaled by sc[row],
-// -> tile (stride LDW)
-template <int ROWS>
-__device__ __forceinline__ void load_state_rows(float* dst, const float* S, int i0, const float* sc, int tid) {
-    constexpr int IT = ROWS * (D / 4) / BT;
-    float4 v[IT];
+__device__ __forceinline__ void cp16(float* dst, const float* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// State slabs through cp.async (16 bytes per copy), so that the next slab is in flight while the
+// products read the current one.  Each thread scales, after its own cp_wait, the very 16-byte chunks
+// it copied (its own asynchronous writes are visible to it), in the same fp32 multiply as a direct
+// load would do; the products that read the slab follow a __syncthreads.
+// 32 rows i0 .. i0+31 of a state (stride 128) -> [32][LDW] tile
+__device__ __forceinline__ void fetch_state_rows(float* dst, const float* S, int i0, int tid) {
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
+    for (int it = 0; it < 32 * (D / 4) / BT; ++it) {
         const int e = tid + it * BT;
-        v[it] = *reinterpret_cast<const float4*>(S + (i0 + (e >> 5)) * D + (e & 31) * 4);
-    }
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int e = tid + it * BT, r = e >> 5;
-        const float f = sc[i0 + r];
-        *reinterpret_cast<float4*>(dst + r * LDW + (e & 31) * 4) =
-            make_float4(v[it].x * f, v[it].y * f, v[it].z * f, v[it].w * f);
+        cp16(dst + (e >> 5) * LDW + (e & 31) * 4, S + (i0 + (e >> 5)) * D + (e & 31) * 4);
     }
 }
-// 32 columns j0 .. j0+31 of all 128 rows of a state, row i scaled by sc[i] -> [128][LDS] tile
-__device__ __forceinline__ void load_state_cols(float* dst, const float* S, int j0, const float* sc, int tid) {
-    constexpr int IT = D * 8 / BT;  // 4
-    float4 v[IT];
+// row r of the slab times sc[i0 + r]
+__device__ __forceinline__ void scale_state_rows(float* dst, int i0, const float* sc, int tid) {
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
+    for (int it = 0; it < 32 * (D / 4) / BT; ++it) {
         const int e = tid + it * BT;
-        v[it] = *reinterpret_cast<const float4*>(S + (e >> 3) * D + j0 + (e & 7) * 4);
+        float4* t = reinterpret_cast<float4*>(dst + (e >> 5) * LDW + (e & 31) * 4);
+        const float f = sc[i0 + (e >> 5)];
+        const float4 v = *t;
+        *t = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
     }
+}
+// 32 columns j0 .. j0+31 of all 128 rows of a state -> [128][LDS] tile
+__device__ __forceinline__ void fetch_state_cols(float* dst, const float* S, int j0, int tid) {
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int e = tid + it * BT, i = e >> 3;
-        const float f = sc[i];
-        *reinterpret_cast<float4*>(dst + i * LDS + (e & 7) * 4) =
-            make_float4(v[it].x * f, v[it].y * f, v[it].z * f, v[it].w * f);
+    for (int it = 0; it < D * 8 / BT; ++it) {
+        const int e = tid + it * BT;
+        cp16(dst + (e >> 3) * LDS + (e & 7) * 4, S + (e >> 3) * D + j0 + (e & 7) * 4);
+    }
+}
+// row i of the slab times sc[i]
+__device__ __forceinline__ void scale_state_cols(float* dst, const float* sc, int tid) {
+#pragma unroll
+    for (int it = 0; it < D * 8 / BT; ++it) {
+        const int e = tid + it * BT;
+        float4* t = reinterpret_cast<float4*>(dst + (e >> 3) * LDS + (e & 7) * 4);
+        const float f = sc[e >> 3];
+        const float4 v = *t;
+        *t = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
     }
 }
 
@@ -381,14 +426,6 @@ struct ScanL {
     static constexpr int FLOATS = DY + 64 * LDS;
 };
 
-__device__ __forceinline__ void cp16(float* dst, const float* src) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 __device__ __forceinline__ void scan_fetch(float* st, const float* rec, int c0, int tid) {
     for (int e = tid; e < C * (D / 4); e += BT) {
         const int r = e >> 5, c4 = (e & 31) * 4;
@@ -506,24 +543,39 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
 struct ValueKeyL {
     static constexpr int T0 = 0, T1 = TILE, T2 = 2 * TILE, T3 = 3 * TILE;
     static constexpr int P0 = 4 * TILE, P1 = P0 + PTILE;
-    static constexpr int ST = P1 + PTILE;        // [32][LDW] state slab or Tb [64][LDN]; then [128][LDS] slabs
-    static constexpr int VB = ST + 128 * LDS;    // egm[128], egcm[128], dbeta halves [2][64] / boundary terms
+    // two slab buffers: [32][LDW] row slabs of a state (value phase), [128][LDS] column slabs (key
+    // phase); ST2 holds Tb [64][LDN] between the start-state and adjoint slabs
+    static constexpr int ST = P1 + PTILE;
+    static constexpr int ST2 = ST + 128 * LDS;
+    static constexpr int VB = ST2 + 128 * LDS;   // egm[128], egcm[128], dbeta halves [2][64] / boundary terms
     static constexpr int FLOATS = VB + 384;
 };
 static_assert(32 * LDW <= 128 * LDS && C * LDN <= 128 * LDS, "the value phase's slabs fit the ST slot");
+static_assert(ValueKeyL::ST % 4 == 0 && ValueKeyL::ST2 % 4 == 0, "16-byte aligned slab buffers");
+static_assert(ValueKeyL::FLOATS * 4 <= 232448, "value+key shared memory over the per-CTA limit");
 
 // The key products of one (chunk, head), with dO in T0, U in T1 and dY in T2 already resident; T3
-// takes the gates, ST the state and adjoint column slabs ([128][LDS]).  Ends with dq, dk, dlog alpha.
+// takes the gates, ST and ST2 the state and adjoint column slabs ([128][LDS]), two in flight at a
+// time.  Ends with dq, dk, dlog alpha.
 template <typename IoT>
 __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos& p, int gc, int h, float* T0, float* T1,
-                                          float* T2, float* T3, float* P0, float* P1, float* ST, float* egm,
-                                          float* egcm, float* bnd, int tid) {
+                                          float* T2, float* T3, float* P0, float* P1, float* ST, float* ST2,
+                                          float* egm, float* egcm, float* bnd, int tid) {
     const int lane = tid & 31, warp = tid >> 5;
     const int r0 = 16 * (warp & 3), c64 = 32 * (warp >> 2), c128 = 64 * (warp >> 2);
     const int H = a.H;
     const IoT* q = static_cast<const IoT*>(a.q);
     const IoT* k = static_cast<const IoT*>(a.k);
     const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
+    const float* S = chunk_start_state(a, p, gc, h);
+    // column slabs: those of the start state (dO Sm^T, dY Sm^T; none when it is zero), then the
+    // adjoint's (U Xc^T); the first two are fetched while the gates and the triangular products run
+    const int nslab = S ? 8 : 4;
+    auto slab_src = [&](int i) { return (S && i < 4) ? S : X; };
+    fetch_state_cols(ST, slab_src(0), 0, tid);
+    cp_commit();
+    fetch_state_cols(ST2, slab_src(1), 32, tid);
+    cp_commit();
 
     chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
     {   // boundary term of the last row: rowsum(S_next * X), S_next = the snapshot after this chunk
@@ -559,24 +611,24 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
     zero(aq);
     zero(aka);
     zero(akb);
-    const float* S = chunk_start_state(a, p, gc, h);
-    for (int pass = 0; pass < 2; ++pass) {  // dO Sm^T, dY Sm^T; then U Xc^T (states in 32-column slabs)
-        const float* M = pass == 0 ? S : X;
-        if (!M) continue;
-        const float* sc = pass == 0 ? egm : egcm;
-        for (int j0 = 0; j0 < D; j0 += 32) {
-            __syncthreads();
-            load_state_cols(ST, M, j0, sc, tid);
-            __syncthreads();
-            if (pass == 0) {
-                mma16<8, AR, BN>(aq, T0 + j0, LDW, ST, LDS, 32, r0, c128, lane);
-                mma16<8, AR, BN>(akb, T2 + j0, LDW, ST, LDS, 32, r0, c128, lane);
-            } else {
-                mma16<8, AR, BN>(aka, T1 + j0, LDW, ST, LDS, 32, r0, c128, lane);
-            }
+    for (int i = 0; i < nslab; ++i) {  // dO Sm^T, dY Sm^T; then U Xc^T (states in 32-column slabs)
+        float* buf = (i & 1) ? ST2 : ST;
+        const bool of_s = S && i < 4;
+        const int j0 = 32 * (i & 3);
+        cp_wait<1>();  // slab i has landed (slab i + 1 may be in flight)
+        scale_state_cols(buf, of_s ? egm : egcm, tid);
+        __syncthreads();
+        if (of_s) {
+            mma16<8, AR, BN>(aq, T0 + j0, LDW, buf, LDS, 32, r0, c128, lane);
+            mma16<8, AR, BN>(akb, T2 + j0, LDW, buf, LDS, 32, r0, c128, lane);
+        } else {
+            mma16<8, AR, BN>(aka, T1 + j0, LDW, buf, LDS, 32, r0, c128, lane);
         }
+        __syncthreads();  // buf is read no more
+        if (i + 2 < nslab) fetch_state_cols(buf, slab_src(i + 2), 32 * ((i + 2) & 3), tid);
+        cp_commit();
     }
-    __syncthreads();  // dO, U, dY are read no more
+    // dO, U, dY are read no more
     load_tile(T2, k, p.t0, p.L, H, h, tid);
     load_tile(T1, q, p.t0, p.L, H, h, tid);
     __syncthreads();
@@ -644,8 +696,18 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
     ChunkPos p;
     if (!chunk_pos(a, gc, p)) return;
     float *T0 = sm + L::T0, *T1 = sm + L::T1, *T2 = sm + L::T2, *T3 = sm + L::T3, *P0 = sm + L::P0,
-          *P1 = sm + L::P1, *ST = sm + L::ST, *egm = sm + L::VB, *egcm = egm + 128, *dbh = egcm + 128;
+          *P1 = sm + L::P1, *ST = sm + L::ST, *ST2 = sm + L::ST2, *egm = sm + L::VB, *egcm = egm + 128,
+          *dbh = egcm + 128;
     const IoT* k = static_cast<const IoT*>(a.k);
+    const float* S = chunk_start_state(a, p, gc, h);
+    const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
+    // the start state's first two 32-row slabs are in flight while the gates and Grams are formed
+    if (S) {
+        fetch_state_rows(ST, S, 0, tid);
+        cp_commit();
+        fetch_state_rows(ST2, S, 32, tid);
+        cp_commit();
+    }
 
     load_tile(T1, k, p.t0, p.L, H, h, tid);
     load_tile(T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
@@ -675,28 +737,35 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
                 P1[r * LDN + s] = s <= r ? am[j][e] : 0.f;
             }
     }
-    // Kh Sm, the start state streamed in 32-row slabs
+    // Kh Sm, the start state streamed in 32-row slabs, two in flight
     float acc[8][4];
     zero(acc);
-    const float* S = chunk_start_state(a, p, gc, h);
     if (S) {
-        for (int i0 = 0; i0 < D; i0 += 32) {
+        for (int i = 0; i < D / 32; ++i) {
+            float* buf = (i & 1) ? ST2 : ST;
+            cp_wait<1>();  // slab i has landed (slab i + 1 may be in flight)
+            scale_state_rows(buf, 32 * i, egm, tid);
             __syncthreads();
-            load_state_rows<32>(ST, S, i0, egm, tid);
-            __syncthreads();
-            mma16<8, AR, BK>(acc, T0 + i0, LDW, ST, LDW, 32, r0, c128, lane);
+            mma16<8, AR, BK>(acc, T0 + 32 * i, LDW, buf, LDW, 32, r0, c128, lane);
+            __syncthreads();  // buf is read no more
+            if (i + 2 < D / 32) fetch_state_rows(buf, S, 32 * (i + 2), tid);
+            cp_commit();
         }
     }
-    __syncthreads();  // T2 (Qh) and ST are read no more
-    load_tile(T2, static_cast<const IoT*>(a.v), p.t0, p.L, H, h, tid);
-    {
+    __syncthreads();  // T2 (Qh), ST and ST2 are read no more
+    {   // Tb -> ST2 and the adjoint's first slab -> ST, in flight while v loads
         const float* tbg = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats + kRecTb;
 #pragma unroll
         for (int it = 0; it < C * (C / 4) / BT; ++it) {
             const int e = tid + it * BT, r = e >> 4, c4 = (e & 15) * 4;
-            *reinterpret_cast<float4*>(ST + r * LDN + c4) = *reinterpret_cast<const float4*>(tbg + r * C + c4);
+            cp16(ST2 + r * LDN + c4, tbg + r * C + c4);
         }
+        cp_commit();
+        fetch_state_rows(ST, X, 0, tid);
+        cp_commit();
     }
+    load_tile(T2, static_cast<const IoT*>(a.v), p.t0, p.L, H, h, tid);
+    cp_wait<1>();  // Tb has landed
     __syncthreads();
     float rr[8][4];  // Y1 = V - Kh Sm (own elements), later R
 #pragma unroll
@@ -713,7 +782,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
         for (int e = 0; e < 4; ++e) T2[frow(r0, lane, e) * LDW + fcol(c128, lane, j, e)] = rr[j][e];
     __syncthreads();
     zero(acc);
-    mma16<8, AR, BK>(acc, ST, LDN, T2, LDW, C, r0, c128, lane);  // U = Tb Y1
+    mma16<8, AR, BK>(acc, ST2, LDN, T2, LDW, C, r0, c128, lane);  // U = Tb Y1
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
@@ -729,21 +798,24 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
     for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) rr[j][e] -= acc[j][e];  // R
-    __syncthreads();  // T0 (Kh), T2 and ST are read no more
+    __syncthreads();  // T0 (Kh), T2 and ST2 (Tb) are read no more
+    fetch_state_rows(ST2, X, 32, tid);
+    cp_commit();
     load_tile(T2, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
     load_tile(T0, a.dv, p.t0, p.L, H, h, tid, -1.f);  // dY = -dv
     __syncthreads();
     zero(acc);
     mma16<8, AC, BK>(acc, P1, LDN, T2, LDW, C, r0, c128, lane);  // Mm^T dO
     mma16<8, AC, BK>(acc, P0, LDN, T0, LDW, C, r0, c128, lane);  // + Lm^T dY
-    {   // + Kb Xc, X streamed in 32-row slabs
-        const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
-        for (int i0 = 0; i0 < D; i0 += 32) {
-            __syncthreads();
-            load_state_rows<32>(ST, X, i0, egcm, tid);
-            __syncthreads();
-            mma16<8, AR, BK>(acc, T1 + i0, LDW, ST, LDW, 32, r0, c128, lane);
-        }
+    for (int i = 0; i < D / 32; ++i) {  // + Kb Xc, X streamed in 32-row slabs, two in flight
+        float* buf = (i & 1) ? ST2 : ST;
+        cp_wait<1>();
+        scale_state_rows(buf, 32 * i, egcm, tid);
+        __syncthreads();
+        mma16<8, AR, BK>(acc, T1 + 32 * i, LDW, buf, LDW, 32, r0, c128, lane);
+        __syncthreads();  // buf is read no more
+        if (i + 2 < D / 32) fetch_state_rows(buf, X, 32 * (i + 2), tid);
+        cp_commit();
     }
     // dbeta_t = <du_t, r_t>: rows g, g + 8 of the warp; columns over the 4 threads of a group
     // and the two warps (warp, warp + 4) that share the rows
@@ -768,7 +840,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
 
     // ---- key phase: dq, dk, dlog alpha.  dO (T2), U (T3) and dY (T0) are resident; the tiles are
     // renamed to the key products' roles: K0 = dO, K1 = U, K2 = dY, K3 = the gates (into Kb's tile)
-    key_phase<IoT>(a, p, gc, h, T2, T3, T0, T1, P0, P1, ST, egm, egcm, egcm + 128, tid);
+    key_phase<IoT>(a, p, gc, h, T2, T3, T0, T1, P0, P1, ST, ST2, egm, egcm, egcm + 128, tid);
 }
 
 // ============================================================ fused prologue ==
