@@ -81,16 +81,6 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
     w.y = *reinterpret_cast<const uint32_t*>(&b);
     *reinterpret_cast<uint2*>(p) = w;
 }
-// two adjacent elements (p even-aligned)
-template <typename T>
-__device__ __forceinline__ float2 ld2(const T* p);
-template <>
-__device__ __forceinline__ float2 ld2<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
-template <>
-__device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16* p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
-
 // ---- products on shared tiles ---------------------------------------------------------------
 // Tensor-core products of fp32 shared tiles: operands rounded to tf32 (cvt.rna), fp32 accumulate,
 // mma.sync m16n8k8.  One warp owns 16 output rows from r0 and NT 8-column tiles from c0; its
@@ -133,28 +123,26 @@ __device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int l
                 mma_tf32(acc[j], a, to_tf32(B[k * ldb + n]), to_tf32(B[(k + 1) * ldb + n]));
             }
         }
-        return;
-    }
+    } else {  // B(k, n) = B[n * ldb + k]: the fragment's own k indices t, t + 4
 #pragma unroll 2
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t a[4];
-        if (AM == AR) {
-            a[0] = to_tf32(A[(r0 + g) * lda + k0 + t]);
-            a[1] = to_tf32(A[(r0 + g + 8) * lda + k0 + t]);
-            a[2] = to_tf32(A[(r0 + g) * lda + k0 + t + 4]);
-            a[3] = to_tf32(A[(r0 + g + 8) * lda + k0 + t + 4]);
-        } else {
-            a[0] = to_tf32(A[(k0 + t) * lda + r0 + g]);
-            a[1] = to_tf32(A[(k0 + t) * lda + r0 + g + 8]);
-            a[2] = to_tf32(A[(k0 + t + 4) * lda + r0 + g]);
-            a[3] = to_tf32(A[(k0 + t + 4) * lda + r0 + g + 8]);
-        }
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            uint32_t a[4];
+            if (AM == AR) {
+                a[0] = to_tf32(A[(r0 + g) * lda + k0 + t]);
+                a[1] = to_tf32(A[(r0 + g + 8) * lda + k0 + t]);
+                a[2] = to_tf32(A[(r0 + g) * lda + k0 + t + 4]);
+                a[3] = to_tf32(A[(r0 + g + 8) * lda + k0 + t + 4]);
+            } else {
+                a[0] = to_tf32(A[(k0 + t) * lda + r0 + g]);
+                a[1] = to_tf32(A[(k0 + t) * lda + r0 + g + 8]);
+                a[2] = to_tf32(A[(k0 + t + 4) * lda + r0 + g]);
+                a[3] = to_tf32(A[(k0 + t + 4) * lda + r0 + g + 8]);
+            }
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int n = c0 + 8 * j + g;
-            const uint32_t b0 = to_tf32(BM == BK ? B[(k0 + t) * ldb + n] : B[n * ldb + k0 + t]);
-            const uint32_t b1 = to_tf32(BM == BK ? B[(k0 + t + 4) * ldb + n] : B[n * ldb + k0 + t + 4]);
-            mma_tf32(acc[j], a, b0, b1);
+            for (int j = 0; j < NT; ++j) {
+                const int n = c0 + 8 * j + g;
+                mma_tf32(acc[j], a, to_tf32(B[n * ldb + k0 + t]), to_tf32(B[n * ldb + k0 + t + 4]));
+            }
         }
     }
 }
@@ -197,10 +185,33 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Two such tiles with all sixteen loads of a thread in flight before its first store (separate
+// calls would wait for the first tile's loads before issuing the second's).
+template <typename TA, typename TB>
+__device__ __forceinline__ void load_tile2(float* dst_a, const TA* src_a, float* dst_b, const TB* src_b, int64_t t0,
+                                           int L, int H, int h, int tid, float scale_b = 1.f) {
+    constexpr int IT = C * (D / 4) / BT;  // 8
+    float4 va[IT], vb[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
+        const size_t o = (static_cast<size_t>(t0 + r) * H + h) * D + c4;
+        va[it] = r < L ? ld4(src_a + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        vb[it] = r < L ? ld4(src_b + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
+        *reinterpret_cast<float4*>(dst_a + r * LDW + c4) = va[it];
+        *reinterpret_cast<float4*>(dst_b + r * LDW + c4) =
+            make_float4(vb[it].x * scale_b, vb[it].y * scale_b, vb[it].z * scale_b, vb[it].w * scale_b);
+    }
+}
+
 // State slabs through cp.async (16 bytes per copy), so that the next slab is in flight while the
-// products read the current one.  Each thread scales, after its own cp_wait, the very 16-byte chunks
-// it copied (its own asynchronous writes are visible to it), in the same fp32 multiply as a direct
-// load would do; the products that read the slab follow a __syncthreads.
+// products read the current one.  Where a slab's rows must be scaled, each thread scales, after its
+// own cp_wait, the very 16-byte chunks it copied (its own asynchronous writes are visible to it); the
+// products that read the slab follow a __syncthreads.
 // 32 rows i0 .. i0+31 of a state (stride 128) -> [32][LDW] tile
 __device__ __forceinline__ void fetch_state_rows(float* dst, const float* S, int i0, int tid) {
 #pragma unroll
@@ -228,25 +239,11 @@ __device__ __forceinline__ void fetch_state_cols(float* dst, const float* S, int
         cp16(dst + (e >> 3) * LDS + (e & 7) * 4, S + (e >> 3) * D + j0 + (e & 7) * 4);
     }
 }
-// row i of the slab times sc[i]
-__device__ __forceinline__ void scale_state_cols(float* dst, const float* sc, int tid) {
-#pragma unroll
-    for (int it = 0; it < D * 8 / BT; ++it) {
-        const int e = tid + it * BT;
-        float4* t = reinterpret_cast<float4*>(dst + (e >> 3) * LDS + (e & 7) * 4);
-        const float f = sc[e >> 3];
-        const float4 v = *t;
-        *t = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
-    }
-}
 
-// Cumulative log-decay of the chunk into G (rows >= L hold gC): log_alpha staged through G, then
-// summed down the rows by 128 threads.  e^{gm}, e^{gC - gm} (and e^{gC}) to vectors.  Contains a
-// barrier: every thread of the CTA calls it.
-__device__ __forceinline__ void chunk_gates(float* G, const float* la, int64_t t0, int L, int H, int h, int tid,
-                                            float* egm, float* egcm, float* egc) {
-    load_tile(G, la, t0, L, H, h, tid);
-    __syncthreads();
+// Cumulative log-decay of the chunk in G (the log_alpha rows already loaded, rows >= L zero; after
+// it rows >= L hold gC), summed down the rows by 128 threads; e^{gm}, e^{gC - gm} (and e^{gC}) to
+// vectors.  The caller synchronises the CTA before and after.
+__device__ __forceinline__ void sum_gates(float* G, int tid, float* egm, float* egcm, float* egc) {
     if (tid < D) {
         float s = 0.f, gm = 0.f;
 #pragma unroll 8
@@ -325,8 +322,10 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
     load_tile(KB, k, p.t0, p.L, H, h, tid);
     load_tile(QH, q, p.t0, p.L, H, h, tid);
     load_tile(DO, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
-    chunk_gates(G, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, egc);
+    load_tile(G, a.log_alpha, p.t0, p.L, H, h, tid);
     if (tid < C) bet[tid] = tid < p.L ? a.beta[(p.t0 + tid) * H + h] : 0.f;
+    __syncthreads();
+    sum_gates(G, tid, egm, egcm, egc);
     __syncthreads();
     for (int e = tid; e < C * D; e += BT) {  // gated operands
         const int r = e >> 7, i = e & 127;
@@ -576,8 +575,9 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
     cp_commit();
     fetch_state_cols(ST2, slab_src(1), 32, tid);
     cp_commit();
-
-    chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
+    load_tile(T3, a.log_alpha, p.t0, p.L, H, h, tid);
+    __syncthreads();
+    sum_gates(T3, tid, egm, egcm, nullptr);
     {   // boundary term of the last row: rowsum(S_next * X), S_next = the snapshot after this chunk
         const float* Sn = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D;
         const int i = tid >> 1, j0 = (tid & 1) * 64;
@@ -611,12 +611,14 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
     zero(aq);
     zero(aka);
     zero(akb);
-    for (int i = 0; i < nslab; ++i) {  // dO Sm^T, dY Sm^T; then U Xc^T (states in 32-column slabs)
+    // dO S^T, dY S^T; then U X^T (states in 32-column slabs).  The row scalings of Sm = Diag(e^{gm}) S
+    // and Xc = Diag(e^{gC-gm}) X scale the products' output columns, so they are applied to the
+    // accumulators afterwards instead of to every slab.
+    for (int i = 0; i < nslab; ++i) {
         float* buf = (i & 1) ? ST2 : ST;
         const bool of_s = S && i < 4;
         const int j0 = 32 * (i & 3);
         cp_wait<1>();  // slab i has landed (slab i + 1 may be in flight)
-        scale_state_cols(buf, of_s ? egm : egcm, tid);
         __syncthreads();
         if (of_s) {
             mma16<8, AR, BN>(aq, T0 + j0, LDW, buf, LDS, 32, r0, c128, lane);
@@ -628,9 +630,17 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
         if (i + 2 < nslab) fetch_state_cols(buf, slab_src(i + 2), 32 * ((i + 2) & 3), tid);
         cp_commit();
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = fcol(c128, lane, j, e);
+            aq[j][e] *= egm[i];
+            akb[j][e] *= egm[i];
+            aka[j][e] *= egcm[i];
+        }
     // dO, U, dY are read no more
-    load_tile(T2, k, p.t0, p.L, H, h, tid);
-    load_tile(T1, q, p.t0, p.L, H, h, tid);
+    load_tile2(T2, k, T1, q, p.t0, p.L, H, h, tid);
     __syncthreads();
     for (int e = tid; e < C * D; e += BT) {  // T0 = Kh, T1 = Qh, T2 = Kb
         const int r = e >> 7, i = e & 127;
@@ -651,7 +661,7 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
             const int r = frow(r0, lane, e), i = fcol(c128, lane, j, e);
-            float dq[2], dk[2], dg[2] = {0.f, 0.f}, dd[2];
+            float dq[2], dk[2], dg[2] = {0.f, 0.f}, dd[2], qv[2], kv[2];
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 const float gx = T3[r * LDW + i + x] - T3[(C / 2 - 1) * LDW + i + x];
@@ -660,12 +670,14 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
                 dq[x] = eq * aq[j][e + x];
                 dk[x] = dka + dkb;
                 dd[x] = dkb - dka;
+                // q and k back from the gated tiles (Qh = q e^{g-gm}, Kb = k e^{gm-g}), to fp32 rounding
+                qv[x] = T1[r * LDW + i + x] * eb;
+                kv[x] = T2[r * LDW + i + x] * eq;
             }
             if (r < p.L) {
                 const size_t o = (static_cast<size_t>(p.t0 + r) * H + h) * D + i;
-                const float2 qv = ld2(q + o), kv = ld2(k + o);
-                dg[0] = qv.x * dq[0] + kv.x * dd[0];
-                dg[1] = qv.y * dq[1] + kv.y * dd[1];
+                dg[0] = qv[0] * dq[0] + kv[0] * dd[0];
+                dg[1] = qv[1] * dq[1] + kv[1] * dd[1];
                 if (r == p.L - 1) {
                     dg[0] += bnd[i];
                     dg[1] += bnd[i + 1];
@@ -711,7 +723,9 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
 
     load_tile(T1, k, p.t0, p.L, H, h, tid);
     load_tile(T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
-    chunk_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid, egm, egcm, nullptr);
+    load_tile(T3, a.log_alpha, p.t0, p.L, H, h, tid);
+    __syncthreads();
+    sum_gates(T3, tid, egm, egcm, nullptr);
     __syncthreads();
     for (int e = tid; e < C * D; e += BT) {  // T0 = Kh, T1 = Kb, T2 = Qh
         const int r = e >> 7, i = e & 127;
