@@ -181,6 +181,11 @@ __device__ __forceinline__ void cp16(float* dst, const float* src) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
+// 16 bytes, or 16 zero bytes when !valid (nothing is read then; src must still be a mapped address)
+__device__ __forceinline__ void cp16z(float* dst, const float* src, bool valid) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -240,9 +245,18 @@ __device__ __forceinline__ void fetch_state_cols(float* dst, const float* S, int
     }
 }
 
-// Cumulative log-decay of the chunk in G (the log_alpha rows already loaded, rows >= L zero; after
-// it rows >= L hold gC), summed down the rows by 128 threads; e^{gm}, e^{gC - gm} (and e^{gC}) to
-// vectors.  The caller synchronises the CTA before and after.
+// Cumulative log-decay of the chunk in G: fetch_gates issues the cp.async copies of the log_alpha
+// rows (rows >= L zero-filled; the caller commits, waits and synchronises the CTA), sum_gates sums
+// down the rows (128 threads; rows >= L then hold gC) and writes e^{gm}, e^{gC - gm} (and e^{gC}) to
+// vectors.  The caller synchronises the CTA after it.
+__device__ __forceinline__ void fetch_gates(float* G, const float* la, int64_t t0, int L, int H, int h, int tid) {
+    const float* row0 = la + (static_cast<size_t>(t0) * H + h) * D;
+#pragma unroll
+    for (int it = 0; it < C * (D / 4) / BT; ++it) {
+        const int e = tid + it * BT, r = e >> 5, c4 = (e & 31) * 4;
+        cp16z(G + r * LDW + c4, r < L ? row0 + static_cast<size_t>(r) * H * D + c4 : row0, r < L);
+    }
+}
 __device__ __forceinline__ void sum_gates(float* G, int tid, float* egm, float* egcm, float* egc) {
     if (tid < D) {
         float s = 0.f, gm = 0.f;
@@ -319,11 +333,12 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
     float *NF = sm + L::NF, *TF = sm + L::TF, *XS = sm + L::XS, *MM = sm + L::MM, *TB = sm + L::TB;
     float *bet = sm + L::VB, *egm = bet + 64, *egcm = egm + 128, *egc = egcm + 128;
 
-    load_tile(KB, k, p.t0, p.L, H, h, tid);
-    load_tile(QH, q, p.t0, p.L, H, h, tid);
+    fetch_gates(G, a.log_alpha, p.t0, p.L, H, h, tid);
+    cp_commit();
+    load_tile2(KB, k, QH, q, p.t0, p.L, H, h, tid);
     load_tile(DO, static_cast<const IoT*>(a.dO), p.t0, p.L, H, h, tid);
-    load_tile(G, a.log_alpha, p.t0, p.L, H, h, tid);
     if (tid < C) bet[tid] = tid < p.L ? a.beta[(p.t0 + tid) * H + h] : 0.f;
+    cp_wait<0>();
     __syncthreads();
     sum_gates(G, tid, egm, egcm, egc);
     __syncthreads();
@@ -713,17 +728,19 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_value_key_kernel(const Backward
     const IoT* k = static_cast<const IoT*>(a.k);
     const float* S = chunk_start_state(a, p, gc, h);
     const float* X = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
-    // the start state's first two 32-row slabs are in flight while the gates and Grams are formed
+    // the log_alpha rows, then the start state's first two 32-row slabs are in flight while k and q
+    // load and the gates and Grams are formed
+    fetch_gates(T3, a.log_alpha, p.t0, p.L, H, h, tid);
+    cp_commit();
     if (S) {
         fetch_state_rows(ST, S, 0, tid);
         cp_commit();
         fetch_state_rows(ST2, S, 32, tid);
         cp_commit();
     }
-
-    load_tile(T1, k, p.t0, p.L, H, h, tid);
-    load_tile(T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
-    load_tile(T3, a.log_alpha, p.t0, p.L, H, h, tid);
+    load_tile2(T1, k, T2, static_cast<const IoT*>(a.q), p.t0, p.L, H, h, tid);
+    if (S) cp_wait<2>();
+    else cp_wait<0>();
     __syncthreads();
     sum_gates(T3, tid, egm, egcm, nullptr);
     __syncthreads();
