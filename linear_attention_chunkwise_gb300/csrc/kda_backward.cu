@@ -44,6 +44,7 @@ constexpr int D = kHeadDim;   // 128
 constexpr int LDW = 132;      // row stride (floats) of 128-wide shared tiles: conflict-free column reads
 constexpr int LDN = 68;       // of 64-wide tiles
 constexpr int LDS = 36;       // of 32-wide tiles
+constexpr int LDX = 40;       // of 32-wide tiles read as adjacent pairs in fragment layout (8 mod 32 words)
 constexpr int TILE = C * LDW;
 constexpr int PTILE = C * LDN;
 constexpr int NCS = 32;       // state columns per scan CTA
@@ -88,7 +89,8 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
 // (g = lane >> 2, t = lane & 3).  Operand element addressing:
 //   AR: A(m, k) = A[m * lda + k]     AC: A(m, k) = A[k * lda + m]
 //   BK: B(k, n) = B[k * ldb + n]     BN: B(k, n) = B[n * ldb + k]
-enum { AR = 0, AC = 1, BK = 0, BN = 1 };
+//   BK8: as BK, for a B whose row stride is 8 mod 32 words (fragment k indices t, t + 4 conflict-free)
+enum { AR = 0, AC = 1, BK = 0, BN = 1, BK8 = 2 };
 
 // Inside a k-step the fragments may take the step's eight k indices in any order that A and B
 // share.  With B(k, n) = B[k * ldb + n] (BK) lane (g, t) takes k = 2t, 2t + 1 instead of the
@@ -123,7 +125,7 @@ __device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int l
                 mma_tf32(acc[j], a, to_tf32(B[k * ldb + n]), to_tf32(B[(k + 1) * ldb + n]));
             }
         }
-    } else {  // B(k, n) = B[n * ldb + k]: the fragment's own k indices t, t + 4
+    } else {  // BN and BK8: the fragment's own k indices t, t + 4
 #pragma unroll 2
         for (int k0 = 0; k0 < K; k0 += 8) {
             uint32_t a[4];
@@ -141,7 +143,8 @@ __device__ __forceinline__ void mma16(float (&acc)[NT][4], const float* A, int l
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int n = c0 + 8 * j + g;
-                mma_tf32(acc[j], a, to_tf32(B[n * ldb + k0 + t]), to_tf32(B[n * ldb + k0 + t + 4]));
+                if (BM == BN) mma_tf32(acc[j], a, to_tf32(B[n * ldb + k0 + t]), to_tf32(B[n * ldb + k0 + t + 4]));
+                else mma_tf32(acc[j], a, to_tf32(B[(k0 + t) * ldb + n]), to_tf32(B[(k0 + t + 4) * ldb + n]));
             }
         }
     }
@@ -431,14 +434,15 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
 struct ScanL {
     static constexpr int WB = 0;                 // [64][LDW]   Wbc
     static constexpr int KM = TILE;              // [64][LDW]   Khm
-    static constexpr int PS = 2 * TILE;          // [128][LDS]  P, this CTA's columns
-    static constexpr int Y0 = PS + 128 * LDS;    // [64][LDS]   dY0, this CTA's columns
-    static constexpr int GM = Y0 + 64 * LDS;     // [128]       e^{gC}
+    static constexpr int PS = 2 * TILE;          // [128][LDX]  P, this CTA's columns
+    static constexpr int Y0 = PS + 128 * LDX;    // [64][LDX]   dY0, this CTA's columns
+    static constexpr int GM = Y0 + 64 * LDX;     // [128]       e^{gC}
     static constexpr int STAGE = GM + 128;
-    static constexpr int XS = 2 * STAGE;         // [128][LDS]  X
-    static constexpr int DY = XS + 128 * LDS;    // [64][LDS]   dY
+    static constexpr int XS = 2 * STAGE;         // [128][LDX]  X
+    static constexpr int DY = XS + 128 * LDX;    // [64][LDS]   dY
     static constexpr int FLOATS = DY + 64 * LDS;
 };
+static_assert(ScanL::FLOATS * 4 <= 232448, "adjoint scan shared memory over the per-CTA limit");
 
 __device__ __forceinline__ void scan_fetch(float* st, const float* rec, int c0, int tid) {
     for (int e = tid; e < C * (D / 4); e += BT) {
@@ -448,8 +452,8 @@ __device__ __forceinline__ void scan_fetch(float* st, const float* rec, int c0, 
     }
     for (int e = tid; e < D * (NCS / 4); e += BT) {
         const int r = e >> 3, c4 = (e & 7) * 4;
-        cp16(st + ScanL::PS + r * LDS + c4, rec + kRecP + r * D + c0 + c4);
-        if (r < C) cp16(st + ScanL::Y0 + r * LDS + c4, rec + kRecDY0 + r * D + c0 + c4);
+        cp16(st + ScanL::PS + r * LDX + c4, rec + kRecP + r * D + c0 + c4);
+        if (r < C) cp16(st + ScanL::Y0 + r * LDX + c4, rec + kRecDY0 + r * D + c0 + c4);
     }
     if (tid < D / 4) cp16(st + ScanL::GM + 4 * tid, rec + kRecGam + 4 * tid);
 }
@@ -496,28 +500,30 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 4; e += 2) {  // elements e, e + 1 are adjacent columns of one row
                 const int r = frow(16 * warp, lane, e), col = fcol(0, lane, j, e);
-                XS[r * LDS + col] = X[j][e];
+                *reinterpret_cast<float2*>(XS + r * LDX + col) = make_float2(X[j][e], X[j][e + 1]);
             }
         cp_wait<1>();  // this chunk's stage has landed
         __syncthreads();
         // the adjoint of this chunk's end state, as whole 128-byte row segments of the slice
         for (int e = tid; e < D * (NCS / 4); e += BT) {
             const int r = e / (NCS / 4), c4 = 4 * (e % (NCS / 4));
-            *reinterpret_cast<float4*>(xo + r * D + c0 + c4) = *reinterpret_cast<const float4*>(XS + r * LDS + c4);
+            *reinterpret_cast<float4*>(xo + r * D + c0 + c4) = *reinterpret_cast<const float4*>(XS + r * LDX + c4);
         }
         {   // dY = dY0 - Wbc X  (64 x 32: warp rows 16 (warp & 3), columns 16 (warp >> 2))
             const int r0 = 16 * (warp & 3), cc = 16 * (warp >> 2);
             float acc[2][4];
             zero(acc);
-            mma16<2, AR, BK>(acc, st + L::WB, LDW, XS, LDS, D, r0, cc, lane);
+            mma16<2, AR, BK8>(acc, st + L::WB, LDW, XS, LDX, D, r0, cc, lane);
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; e += 2) {
                     const int r = frow(r0, lane, e), col = fcol(cc, lane, j, e);
-                    DY[r * LDS + col] = st[L::Y0 + r * LDS + col] - acc[j][e];
+                    const float2 y0 = *reinterpret_cast<const float2*>(st + L::Y0 + r * LDX + col);
+                    DY[r * LDS + col] = y0.x - acc[j][e];
+                    DY[r * LDS + col + 1] = y0.y - acc[j][e + 1];
                 }
         }
         __syncthreads();
@@ -534,9 +540,12 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; e += 2) {
                     const int r = frow(16 * warp, lane, e), col = fcol(0, lane, j, e);
-                    X[j][e] = fmaf(st[L::GM + r], X[j][e], st[L::PS + r * LDS + col] + acc[j][e]);
+                    const float2 ps = *reinterpret_cast<const float2*>(st + L::PS + r * LDX + col);
+                    const float gm = st[L::GM + r];
+                    X[j][e] = fmaf(gm, X[j][e], ps.x + acc[j][e]);
+                    X[j][e + 1] = fmaf(gm, X[j][e + 1], ps.y + acc[j][e + 1]);
                 }
         }
     }
