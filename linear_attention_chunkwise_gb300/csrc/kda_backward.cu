@@ -26,8 +26,9 @@
 //
 // Kernels (all 256 threads; products on fp32 shared tiles as tf32 mma.sync, fp32 accumulation):
 //   prep      per (chunk, head): the X-independent pieces -> a per-chunk record
-//   scan      per (sequence, head, 32 state columns): the walk of X; writes dv = -dY
-//             and X after every chunk
+//   scan      per (sequence, head, 32 state columns): the walk of X; writes dv = -dY,
+//             X after every chunk and its columns' part of rowsum(S_next X) (into the
+//             consumed record)
 //   value+key per (chunk, head): U, dbeta, then dq, dk, dlog_alpha (U, dO, dY kept in shared memory)
 // The chunk-start states come from the chunkwise prefill (a snapshot after every chunk).
 #include <cuda_bf16.h>
@@ -49,6 +50,7 @@ constexpr int TILE = C * LDW;
 constexpr int PTILE = C * LDN;
 constexpr int NCS = 32;       // state columns per scan CTA
 constexpr int kSlices = D / NCS;
+static_assert(kSlices == 4, "the boundary term sums four slice parts");
 
 // per-(chunk, head) record of the prep kernel (fp32)
 constexpr int kRecWbc = 0;        // [64][128]  Tb^T Kb Diag(e^{gC-gm})
@@ -497,6 +499,20 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
         if (c > 0) scan_fetch(sm + (s ^ 1) * L::STAGE, rec_of(c - 1), c0, tid);
         cp_commit();
         float* xo = a.xbuf + (static_cast<size_t>(gc) * H + h) * D * D;
+        // the state after this chunk at this thread's X elements, in flight until the X update
+        float sn[4][4];
+        {
+            const float* snp = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D + c0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const float2 v = *reinterpret_cast<const float2*>(snp + frow(16 * warp, lane, e) * D +
+                                                                      fcol(0, lane, j, e));
+                    sn[j][e] = v.x;
+                    sn[j][e + 1] = v.y;
+                }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -532,6 +548,26 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_scan_kernel(const BackwardArgs 
             const float4 dy = *reinterpret_cast<const float4*>(DY + r * LDS + c4);
             *reinterpret_cast<float4*>(a.dv + (static_cast<size_t>(t0 + r) * H + h) * D + c0 + c4) =
                 make_float4(-dy.x, -dy.y, -dy.z, -dy.w);
+        }
+        {   // this slice's part of rowsum(S_next * X), the last row's boundary term of dlog_alpha, into
+            // row i >> 5, column c0 + (i & 31) of the record's P block (consumed: the stage holds it)
+            float p_lo = 0.f, p_hi = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                p_lo = fmaf(sn[j][0], X[j][0], fmaf(sn[j][1], X[j][1], p_lo));
+                p_hi = fmaf(sn[j][2], X[j][2], fmaf(sn[j][3], X[j][3], p_hi));
+            }
+#pragma unroll
+            for (int off = 1; off < 4; off <<= 1) {
+                p_lo += __shfl_xor_sync(0xffffffffu, p_lo, off);
+                p_hi += __shfl_xor_sync(0xffffffffu, p_hi, off);
+            }
+            if ((lane & 3) == 0) {
+                float* bp = rec_of(c) + kRecP + c0;
+                const int i_lo = frow(16 * warp, lane, 0), i_hi = i_lo + 8;
+                bp[(i_lo >> 5) * D + (i_lo & 31)] = p_lo;
+                bp[(i_hi >> 5) * D + (i_hi & 31)] = p_hi;
+            }
         }
         {   // X <- Diag(e^{gC}) X + P + Khm^T dY
             float acc[4][4];
@@ -602,18 +638,9 @@ __device__ __forceinline__ void key_phase(const BackwardArgs& a, const ChunkPos&
     load_tile(T3, a.log_alpha, p.t0, p.L, H, h, tid);
     __syncthreads();
     sum_gates(T3, tid, egm, egcm, nullptr);
-    {   // boundary term of the last row: rowsum(S_next * X), S_next = the snapshot after this chunk
-        const float* Sn = a.ckpt + (static_cast<size_t>(gc) * H + h) * D * D;
-        const int i = tid >> 1, j0 = (tid & 1) * 64;
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            const float4 sv = *reinterpret_cast<const float4*>(Sn + i * D + j0 + j);
-            const float4 xv = *reinterpret_cast<const float4*>(X + i * D + j0 + j);
-            s = fmaf(sv.x, xv.x, fmaf(sv.y, xv.y, fmaf(sv.z, xv.z, fmaf(sv.w, xv.w, s))));
-        }
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        if ((tid & 1) == 0) bnd[i] = s;
+    if (tid < D) {  // boundary term of the last row, rowsum(S_next * X): the adjoint scan's four slice parts
+        const float* bp = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats + kRecP + (tid >> 5) * D + (tid & 31);
+        bnd[tid] = (bp[0] + bp[NCS]) + (bp[2 * NCS] + bp[3 * NCS]);
     }
     __syncthreads();
     {   // P0 = lower (dO U^T) incl. diagonal; P1 = strict upper (U dY^T)
