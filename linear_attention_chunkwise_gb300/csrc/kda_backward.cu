@@ -314,13 +314,14 @@ struct PrepL {
     static constexpr int NF = 4 * TILE;          // [64][64] (m4 layout); NF..TF+4096 hold g first
     static constexpr int TF = NF + 4096;
     static constexpr int GS = NF;                // g scratch [64][LDW] spans NF, TF, XS and part of MM
-    static constexpr int XS = TF + 4096;
+    static constexpr int XS = TF + 4096;         // padding under the g scratch
     static constexpr int MM = XS + 768;
     static constexpr int TB = MM + PTILE;
     static constexpr int VB = TB + PTILE;        // beta[64], egm[128], egcm[128], egc[128]
     static constexpr int FLOATS = VB + 448;
 };
 static_assert(PrepL::GS + TILE <= PrepL::MM, "g scratch must end before Mm");
+static_assert(PTILE >= pf::kInvScratchFloats, "the inverse's scratch fits the Tb tile");
 
 template <typename IoT>
 __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs a) {
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
     const IoT* k = static_cast<const IoT*>(a.k);
     float* rec = a.rec + (static_cast<size_t>(gc) * H + h) * kRecFloats;
     float *KH = sm + L::KH, *QH = sm + L::QH, *KB = sm + L::KB, *DO = sm + L::DO, *G = sm + L::GS;
-    float *NF = sm + L::NF, *TF = sm + L::TF, *XS = sm + L::XS, *MM = sm + L::MM, *TB = sm + L::TB;
+    float *NF = sm + L::NF, *TF = sm + L::TF, *MM = sm + L::MM, *TB = sm + L::TB;
     float *bet = sm + L::VB, *egm = bet + 64, *egcm = egm + 128, *egc = egcm + 128;
 
     fetch_gates(G, a.log_alpha, p.t0, p.L, H, h, tid);
@@ -391,7 +392,8 @@ __global__ void __launch_bounds__(BT, 1) kda_bwd_prep_kernel(const BackwardArgs 
             }
     }
     __syncthreads();
-    pf::lower_inverse_tc(pf::rows64(NF), pf::rows64(TF), XS, tid);  // T = (I + N)^-1, ends synchronised
+    // T = (I + N)^-1 (scratch in TB, written only after it), ends synchronised
+    pf::lower_inverse_tc(pf::rows64(NF), pf::rows64(TF), TB, tid);
     for (int e = tid; e < C * C; e += BT) {
         const int r = e >> 6, s = e & 63;
         const float tb = s <= r ? pf::m1(TF, r, s) * bet[s] : 0.f;

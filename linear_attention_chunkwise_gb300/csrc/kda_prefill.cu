@@ -63,8 +63,8 @@ struct Smem {
     static constexpr uint32_t INV_T = OP_SM + 16384;      // f32 [64][64]
     static constexpr uint32_t OP_U = OP_SM + 32768;       // [2 blk][64 rows][128 B]: U
     static constexpr uint32_t SMALL = OP_U + 16384;
-    static constexpr uint32_t XS = SMALL;                 // f32 [6][16][8] inverse scratch
-    static constexpr uint32_t BETA = XS + 3 * 256 * 4;    // f32 [64]
+    static constexpr uint32_t XS = SMALL;                 // f32 inverse scratch
+    static constexpr uint32_t BETA = XS + kInvScratchFloats * 4;  // f32 [64]
     static constexpr uint32_t RED = BETA + 64 * 4;        // f32 [4][128] cumsum partials
     static constexpr uint32_t EGM = RED + 4 * 128 * 4;    // f32 [128] exp(gm)
     static constexpr uint32_t EGC = EGM + 128 * 4;        // f32 [2][128] exp(gC), by chunk parity

@@ -336,15 +336,18 @@ __device__ __forceinline__ void lower_inverse_diag_col(const Rows64& Nf, const R
     }
 }
 
-// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks: the diagonal blocks by
-// forward substitution (lower_inverse_diag), then, with the off-diagonal block products on the
-// tensor cores, per level d,
-//   X = sum_{J=I}^{R-1} N_RJ T_JI,  T_RI = -T_RR X   (R = I + d)
-// as tf32 mma.sync products with fp32 accumulation, one warp per 16 x 8 column tile of T_RI (2 (4 - d)
-// warps), X staged through the warp's own 16 x 8 slot of Xs (f32 [6][16][8]).  Three block
-// barriers instead of six and a fraction of the instructions of products on the CUDA cores; the
-// operands are rounded to tf32 (2^-11), below the bf16 rounding Tb takes afterwards.  Needs NT >= 192
-// threads; ends synchronised.  diag_done: the caller has solved the diagonal blocks and synchronised.
+// T = (I + N)^-1 for strictly lower N (64 x 64, fp32), by 16 x 16 blocks: the diagonal blocks T_II by
+// forward substitution (lower_inverse_diag), then, with the block products on the tensor cores,
+//   (a) the two 32 x 32 diagonal halves:  T_10 = -T_11 (N_10 T_00),  T_32 = -T_33 (N_32 T_22)
+//       (four warps, one 16 x 8 column tile each, X staged through the warp's own slot of Xs);
+//   (b) the lower-left 32 x 32 block of the halves T_ll, T_hh just completed:
+//       X = N_hl T_ll, then T_hl = -T_hh X  (all eight warps, one 16 x 8 tile of the 32 x 32 result
+//       each; X through Xs as [32][40] fp32, a barrier between the two products).
+// tf32 mma.sync products with fp32 accumulation; the operands are rounded to tf32 (2^-11), below the
+// bf16 rounding Tb takes afterwards.  Only blocks on or below the diagonal are read.  Needs NT >= 256
+// threads and 1280 floats of Xs; ends synchronised.  diag_done: the caller has solved the diagonal
+// blocks and synchronised.
+constexpr int kInvScratchFloats = 32 * 40;
 __device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64& Tf, float* Xs, int tid,
                                                  bool diag_done = false) {
     if (!diag_done) {
@@ -353,43 +356,69 @@ __device__ __forceinline__ void lower_inverse_tc(const Rows64& Nf, const Rows64&
     }
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    float* xs = Xs + warp * 128;  // [16][8]
-#pragma unroll 1
-    for (int d = 1; d <= 3; ++d) {
-        if (warp < 2 * (4 - d)) {
-            const int I = warp >> 1, R = I + d, n0 = 16 * I + 8 * (warp & 1);
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int J = I; J < R; ++J) {
+    if (warp < 4) {  // (a) block (R, I) = (I + 1, I), I = 0 or 2; column tile n0
+        const int I = 2 * (warp >> 1), R = I + 1, n0 = 16 * I + 8 * (warp & 1);
+        float* xs = Xs + warp * 128;  // [16][8]
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int kk = 0; kk < 16; kk += 8) {
-                    const int k0 = 16 * J + kk;
-                    const uint32_t a[4] = {to_tf32(m1(Nf, 16 * R + g, k0 + t)), to_tf32(m1(Nf, 16 * R + g + 8, k0 + t)),
-                                           to_tf32(m1(Nf, 16 * R + g, k0 + t + 4)),
-                                           to_tf32(m1(Nf, 16 * R + g + 8, k0 + t + 4))};
-                    mma_tf32(x, a, to_tf32(m1(Tf, k0 + t, n0 + g)), to_tf32(m1(Tf, k0 + t + 4, n0 + g)));
-                }
-            }
-            xs[g * 8 + 2 * t] = x[0];
-            xs[g * 8 + 2 * t + 1] = x[1];
-            xs[(g + 8) * 8 + 2 * t] = x[2];
-            xs[(g + 8) * 8 + 2 * t + 1] = x[3];
-            __syncwarp();
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < 16; kk += 8) {
-                const int k0 = 16 * R + kk;
-                const uint32_t a[4] = {to_tf32(m1(Tf, 16 * R + g, k0 + t)), to_tf32(m1(Tf, 16 * R + g + 8, k0 + t)),
-                                       to_tf32(m1(Tf, 16 * R + g, k0 + t + 4)),
-                                       to_tf32(m1(Tf, 16 * R + g + 8, k0 + t + 4))};
-                mma_tf32(y, a, to_tf32(xs[(kk + t) * 8 + g]), to_tf32(xs[(kk + t + 4) * 8 + g]));
-            }
-            // columns n0 + 2t, +1 share one swizzled float4 group: one 8-byte store per row
-            *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g, n0 + 2 * t)) = make_float2(-y[0], -y[1]);
-            *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g + 8, n0 + 2 * t)) = make_float2(-y[2], -y[3]);
+        for (int kk = 0; kk < 16; kk += 8) {
+            const int k0 = 16 * I + kk;
+            const uint32_t a[4] = {to_tf32(m1(Nf, 16 * R + g, k0 + t)), to_tf32(m1(Nf, 16 * R + g + 8, k0 + t)),
+                                   to_tf32(m1(Nf, 16 * R + g, k0 + t + 4)),
+                                   to_tf32(m1(Nf, 16 * R + g + 8, k0 + t + 4))};
+            mma_tf32(x, a, to_tf32(m1(Tf, k0 + t, n0 + g)), to_tf32(m1(Tf, k0 + t + 4, n0 + g)));
         }
-        __syncthreads();
+        xs[g * 8 + 2 * t] = x[0];
+        xs[g * 8 + 2 * t + 1] = x[1];
+        xs[(g + 8) * 8 + 2 * t] = x[2];
+        xs[(g + 8) * 8 + 2 * t + 1] = x[3];
+        __syncwarp();
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 16; kk += 8) {
+            const int k0 = 16 * R + kk;
+            const uint32_t a[4] = {to_tf32(m1(Tf, 16 * R + g, k0 + t)), to_tf32(m1(Tf, 16 * R + g + 8, k0 + t)),
+                                   to_tf32(m1(Tf, 16 * R + g, k0 + t + 4)),
+                                   to_tf32(m1(Tf, 16 * R + g + 8, k0 + t + 4))};
+            mma_tf32(y, a, to_tf32(xs[(kk + t) * 8 + g]), to_tf32(xs[(kk + t + 4) * 8 + g]));
+        }
+        // columns n0 + 2t, +1 share one swizzled float4 group: one 8-byte store per row
+        *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g, n0 + 2 * t)) = make_float2(-y[0], -y[1]);
+        *reinterpret_cast<float2*>(&m1(Tf, 16 * R + g + 8, n0 + 2 * t)) = make_float2(-y[2], -y[3]);
     }
+    __syncthreads();
+    // (b) warp -> rows 16 rb .. of the 32 x 32 block (rows 32 + 16 rb of T), columns n0 .. n0 + 7
+    constexpr int LX = 40;  // Xs row stride: the paired stores and the B reads below hit distinct banks
+    const int rb = warp & 1, n0 = 8 * (warp >> 1);
+    {   // X = N_hl T_ll; T_ll[k][n] = 0 for k in an upper block, so columns 16.. need k >= 16 only
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = 32 + 16 * rb;
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (n0 >= 16 && k0 < 16) continue;
+            const uint32_t a[4] = {to_tf32(m1(Nf, r + g, k0 + t)), to_tf32(m1(Nf, r + g + 8, k0 + t)),
+                                   to_tf32(m1(Nf, r + g, k0 + t + 4)), to_tf32(m1(Nf, r + g + 8, k0 + t + 4))};
+            mma_tf32(x, a, to_tf32(m1(Tf, k0 + t, n0 + g)), to_tf32(m1(Tf, k0 + t + 4, n0 + g)));
+        }
+        *reinterpret_cast<float2*>(Xs + (16 * rb + g) * LX + n0 + 2 * t) = make_float2(x[0], x[1]);
+        *reinterpret_cast<float2*>(Xs + (16 * rb + g + 8) * LX + n0 + 2 * t) = make_float2(x[2], x[3]);
+    }
+    __syncthreads();
+    {   // T_hl = -T_hh X; row block rb of T_hh is nonzero in columns 32 .. 32 + 16 rb + 15 only
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = 32 + 16 * rb;
+#pragma unroll
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+            if (k0 >= 16 * (rb + 1)) continue;
+            const uint32_t a[4] = {to_tf32(m1(Tf, r + g, 32 + k0 + t)), to_tf32(m1(Tf, r + g + 8, 32 + k0 + t)),
+                                   to_tf32(m1(Tf, r + g, 32 + k0 + t + 4)),
+                                   to_tf32(m1(Tf, r + g + 8, 32 + k0 + t + 4))};
+            mma_tf32(y, a, to_tf32(Xs[(k0 + t) * LX + n0 + g]), to_tf32(Xs[(k0 + t + 4) * LX + n0 + g]));
+        }
+        *reinterpret_cast<float2*>(&m1(Tf, r + g, n0 + 2 * t)) = make_float2(-y[0], -y[1]);
+        *reinterpret_cast<float2*>(&m1(Tf, r + g + 8, n0 + 2 * t)) = make_float2(-y[2], -y[3]);
+    }
+    __syncthreads();
 }
 
 }  // namespace pf

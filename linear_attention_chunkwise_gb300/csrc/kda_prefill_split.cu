@@ -138,7 +138,7 @@ struct PrepSmem {
     static constexpr uint32_t T_HI = OP_A + 16384 + 8192;   // f32 rows 32..63 of T (blk 1's Qh rows)
     static constexpr uint32_t OP_KB = 32768;     // [2 blk][64 rows][128 B]: Kb, then f32 [64][64] N
     static constexpr uint32_t OP_A3 = 49152;     // [Tb (64 rows) | M (64 rows)] x 128 B
-    static constexpr uint32_t XS = OP_A3;        // f32 [6][16][8] block products (Tb rows, before Tb)
+    static constexpr uint32_t XS = OP_A3;        // f32 inverse scratch (Tb rows, before Tb)
     static constexpr uint32_t RED = OP_A3 + 4096;  // f32 [8][128] gate partial sums (Tb rows, gate phase)
     static constexpr uint32_t EV = 65536;        // f32 [3][128]: exp(gm), exp(gC), exp(gC - gm)
     static constexpr uint32_t BETA = EV + 1536;  // f32 [64]
@@ -147,8 +147,9 @@ struct PrepSmem {
     static constexpr uint32_t TOTAL = TMEM_SLOT + 8;
     static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
-static_assert(PrepSmem::XS + 3072 <= PrepSmem::RED && PrepSmem::RED + 4096 <= PrepSmem::OP_A3 + 8192,
-              "scratch inside the Tb rows");
+static_assert(PrepSmem::XS + kInvScratchFloats * 4 <= PrepSmem::OP_A3 + 8192 &&
+                  PrepSmem::RED + 4096 <= PrepSmem::OP_A3 + 8192,
+              "scratch inside the Tb rows (the gate sums are dead before the inverse)");
 static_assert(3 * (PrepSmem::ALLOC + 1024) <= 233472, "three prep CTAs must fit on one SM");
 
 __global__ void __launch_bounds__(NT, 3)
