@@ -330,6 +330,13 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         !make_map(&tm_la, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_tokens ? static_cast<const void*>(log_alpha) : dummy,
                   kHeadDim, Hh, T, kHeadDim, kda::kChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
         return KDA_ERR_CUDA;
+    // the snapshots as [entries x H x 128 rows][128] fp32: the scan stores 32 x 32 blocks, 128B-swizzled
+    CUtensorMap tm_snap;
+    const bool have_snaps = snap.count > 0;
+    if (!make_map(&tm_snap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_snaps ? static_cast<const void*>(snap.S) : dummy,
+                  kHeadDim, 1, have_snaps ? static_cast<uint64_t>(snap.count) * Hh * kHeadDim : kHeadDim, 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return KDA_ERR_CUDA;
     const bool og = (fz.flags & KDA_FUSE_OUT_GATE) != 0;
 
     // the longest-first order of the sequences; one sequence in the two-pass path needs none (its chunk
@@ -386,7 +393,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
         const bool piecewise = pieces > 1 && 2 * (static_cast<int64_t>(num_seqs) * H * 2) <= sm_count() &&
                                cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
         if (!piecewise)
-            return out_gate(kda::launch_prefill_split(tm_q, tm_k, tm_v, a, max_chunks(num_seqs, total_tokens), out_f32,
+            return out_gate(kda::launch_prefill_split(tm_q, tm_k, tm_v, tm_snap, a, max_chunks(num_seqs, total_tokens), out_f32,
                                                       stream) == cudaSuccess);
         // Scan piece j covers chunks [j sq, (j+1) sq).  Pass 1's first launch prepares a lead of L0
         // chunks; its launch j (j >= 1) prepares the next share of the rest beside scan piece j-1.  L0
@@ -411,7 +418,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
             }
             a.piece_begin = static_cast<int32_t>(j * sq);
             a.piece_len = static_cast<int32_t>(scan_end - j * sq);
-            ok = ok && kda::launch_chunk_scan(tm_v, a, out_f32, stream) == cudaSuccess;
+            ok = ok && kda::launch_chunk_scan(tm_v, tm_snap, a, out_f32, stream) == cudaSuccess;
         }
         return out_gate(ok);
     } else if (kda::launch_prefill_fused(tm_q, tm_k, tm_v, tm_la, a, out_f32, stream) != cudaSuccess) {

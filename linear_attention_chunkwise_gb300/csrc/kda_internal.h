@@ -103,8 +103,11 @@ cudaError_t launch_prefill_fused(const CUtensorMap& tm_q, const CUtensorMap& tm_
 cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
                                int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
                                int32_t num_snaps, cudaStream_t stream);
+// tm_snap: a map over S_snap as [num_snaps x H x 128 rows][128] fp32 (3-D, middle extent 1), boxes of
+// 32 rows x 32 columns, 128B-swizzled; any valid map when there are no snapshots.
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const PrefillArgs& a, int64_t max_chunks, bool out_f32, cudaStream_t stream);
+                                 const CUtensorMap& tm_snap, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
+                                 cudaStream_t stream);
 // The two passes separately, for the piecewise schedule.  Pass 1's grid is
 // `units` x H CTAs: units = chunk slots of the whole batch (piece_len = 0) or
 // num_seqs x piece_len (piece mode); with beside_previous it is launched as a
@@ -115,7 +118,8 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 // y = RMSNorm(o) * w * gate in place on o ([rows, 128], the input dtype), w NULL = ones.
 cudaError_t launch_out_gate(bool f32_io, void* o, const void* gate, const float* w, float eps, int64_t rows,
                             cudaStream_t stream);
-cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream);
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap& tm_snap, const PrefillArgs& a, bool out_f32,
+                              cudaStream_t stream);
 
 // Reverse-mode gradient of the prefill (kda_backward.cu).  Gradients are fp32,
 // [T, H, 128] for q/k/v/log_alpha, [T, H] for beta, [N, H, 128, 128] for S0.

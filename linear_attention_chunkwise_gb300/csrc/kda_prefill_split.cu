@@ -360,14 +360,21 @@ constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 1536 + 8192;
 // warp's own 32 x PC floats of shared memory (16-byte chunks xor-swizzled by the row), so each store
 // instruction writes whole PC * 4-byte row segments of 32 / (PC / 4) rows instead of 16 bytes in each
 // of 32 rows.
+// The staging alone: lane = block row, row r's 16-byte chunk j at position j ^ (r mod CH).  For PC = 32
+// (128-byte rows) on a 1024-byte aligned stage this is the 128B-swizzled layout of a tensor copy's box.
 template <int PC>
-__device__ __forceinline__ void store_state_rows(float* dst, const float (&S)[PC], float* stage, int lane) {
-    constexpr int CH = PC / 4;    // 16-byte chunks per row
-    constexpr int RPI = 32 / CH;  // rows per store instruction
+__device__ __forceinline__ void stage_state_rows(const float (&S)[PC], float* stage, int lane) {
+    constexpr int CH = PC / 4;
 #pragma unroll
     for (int j = 0; j < CH; ++j)
         *reinterpret_cast<float4*>(stage + lane * PC + 4 * (j ^ (lane & (CH - 1)))) =
             make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+}
+template <int PC>
+__device__ __forceinline__ void store_state_rows(float* dst, const float (&S)[PC], float* stage, int lane) {
+    constexpr int CH = PC / 4;    // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;  // rows per store instruction
+    stage_state_rows<PC>(S, stage, lane);
     __syncwarp();
     const int rr = lane / CH, j = lane % CH;
 #pragma unroll
@@ -442,7 +449,8 @@ __device__ __forceinline__ void store_out_rows(OutT* dst, int64_t row_stride, in
 // read), column group cq = w / 4.
 template <typename OutT, int NTS, int NSET>
 __global__ void __launch_bounds__(NTS, 3 - NSET)
-    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const PrefillArgs p) {
+    kda_chunk_scan_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_snap,
+                          const PrefillArgs p) {
     using L = ScanSmemT<NSET>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -535,6 +543,7 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
         mbar_init(&evbar[1], 1);
         fence_mbar_init();
         prefetch_tmap(&tm_v);
+        if (p.num_snaps > 0) prefetch_tmap(&tm_snap);
     }
     for (int e = tid; e < NSET * 512; e += NTS)  // zero rows of every set's [Tb | 0 | M] tile
         reinterpret_cast<uint4*>(sm + (e >> 9) * L::SET + L::S_A3 + 8192)[e & 511] = make_uint4(0u, 0u, 0u, 0u);
@@ -674,13 +683,25 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
 #pragma unroll
             for (int e = 0; e < PC; ++e) S[e] = fmaf(dc, S[e], dcm * a[e]);
         }
-        {  // state snapshots at the end of this chunk (positions are sequence-relative)
+        bool snap_stored = false;
+        {  // state snapshots at the end of this chunk (positions are sequence-relative): each warp stages its
+           // 32 x 32 block in this chunk's operand set (its MMAs have completed) in the 128B-swizzled
+           // layout of the snapshot map's box, and its lane 0 stores it with one tensor copy
             const int64_t done = min(static_cast<int64_t>(cb + c + 1) * C, seq_len);
             while (next_snap <= done) {
-                if (next_snap == done)  // staged in this chunk's operand set: its MMAs have completed
-                    store_state_rows<PC>(
-                        p.S_snap + ((static_cast<size_t>(si) * H + h) * D + 32 * qw) * D + j0 + PC * cq, S,
-                        reinterpret_cast<float*>(set) + warp * 32 * PC, lane);
+                if (next_snap == done) {
+                    float* stage = reinterpret_cast<float*>(set) + warp * 32 * PC;
+                    if (snap_stored && lane == 0) bulk_wait_read();  // a second entry at the same position
+                    __syncwarp();
+                    stage_state_rows<PC>(S, stage, lane);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_snap, stage, j0 + PC * cq, 0, (si * H + h) * D + 32 * qw);
+                        bulk_commit();
+                    }
+                    snap_stored = true;
+                }
                 ++si;
                 next_snap = si < se ? p.snap_pos[si] : INT_MAX;
             }
@@ -700,6 +721,7 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
                 static_cast<int64_t>(H) * D, Lc - row0, a, set + L::S_KB + ((qw - 2) + 2 * cq) * (32 * PC * 4),
                 lane);
         }
+        if (snap_stored && lane == 0) bulk_wait_read();  // the snapshot copies have read the staged blocks
         if (NSET == 1 && c + 1 < nch) {  // every read of the set (MMAs, staging) is done: refill it
             fence_async_smem();
             __syncthreads();
@@ -785,14 +807,16 @@ cudaError_t launch_chunk_prep(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 }
 
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                 const PrefillArgs& a, int64_t max_chunks, bool out_f32, cudaStream_t stream) {
+                                 const CUtensorMap& tm_snap, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
+                                 cudaStream_t stream) {
     const cudaError_t err = launch_chunk_prep(tm_q, tm_k, a, max_chunks, stream, false);
     if (err != cudaSuccess) return err;
-    return launch_chunk_scan(tm_v, a, out_f32, stream);
+    return launch_chunk_scan(tm_v, tm_snap, a, out_f32, stream);
 }
 
 template <typename OutT, int NSET>
-cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigned ctas, cudaStream_t stream) {
+cudaError_t launch_scan_t(const CUtensorMap& tm_v, const CUtensorMap& tm_snap, const PrefillArgs& a, unsigned ctas,
+                          cudaStream_t stream) {
     constexpr int NTS = 256;  // 512 threads (16 columns each) measured no faster: the chunk is not epilogue-bound
     constexpr uint32_t alloc = ScanSmemT<NSET>::ALLOC;
     static int configured[64];
@@ -804,7 +828,7 @@ cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigne
                             cudaSharedmemCarveoutMaxShared, carveout);
         if (err != cudaSuccess) return err;
     }
-    kda_chunk_scan_kernel<OutT, NTS, NSET><<<ctas, NTS, alloc, stream>>>(tm_v, a);
+    kda_chunk_scan_kernel<OutT, NTS, NSET><<<ctas, NTS, alloc, stream>>>(tm_v, tm_snap, a);
     return cudaGetLastError();
 }
 
@@ -815,7 +839,8 @@ cudaError_t launch_scan_t(const CUtensorMap& tm_v, const PrefillArgs& a, unsigne
 // sequences average at most 32 chunks, so each CTA's start (state, first copies) is hidden behind the
 // other's chain (64 x 1024 tokens: 1.87 against 2.00 ms).  Longer sequences in several waves keep
 // the two-set form (16 x 4096 tokens: 1.82 against 1.87 ms; the varlen mix of 1k-64k tokens even).
-cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, bool out_f32, cudaStream_t stream) {
+cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const CUtensorMap& tm_snap, const PrefillArgs& a, bool out_f32,
+                              cudaStream_t stream) {
     const long long scan_ctas = static_cast<long long>(a.num_seqs) * a.H * (D / NV);
     if (scan_ctas == 0) return cudaSuccess;
     int dev = 0, sms = 0;
@@ -825,8 +850,10 @@ cudaError_t launch_chunk_scan(const CUtensorMap& tm_v, const PrefillArgs& a, boo
     const unsigned n = static_cast<unsigned>(scan_ctas);
     const bool short_chains = a.total_tokens <= static_cast<int64_t>(32 * C) * a.num_seqs;
     if (scan_ctas > sms && (scan_ctas <= 2LL * sms || short_chains))
-        return out_f32 ? launch_scan_t<float, 1>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16, 1>(tm_v, a, n, stream);
-    return out_f32 ? launch_scan_t<float, 2>(tm_v, a, n, stream) : launch_scan_t<__nv_bfloat16, 2>(tm_v, a, n, stream);
+        return out_f32 ? launch_scan_t<float, 1>(tm_v, tm_snap, a, n, stream)
+                       : launch_scan_t<__nv_bfloat16, 1>(tm_v, tm_snap, a, n, stream);
+    return out_f32 ? launch_scan_t<float, 2>(tm_v, tm_snap, a, n, stream)
+                   : launch_scan_t<__nv_bfloat16, 2>(tm_v, tm_snap, a, n, stream);
 }
 
 // ============================================================ output gate ==
