@@ -333,9 +333,10 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, kda_dtype q
     // the snapshots as [entries x H x 128 rows][128] fp32: the scan stores 32 x 32 blocks, 128B-swizzled
     CUtensorMap tm_snap;
     const bool have_snaps = snap.count > 0;
+    const uint64_t snap_rows =
+        have_snaps ? std::min<uint64_t>(static_cast<uint64_t>(snap.count) * Hh * kHeadDim, kda::kSnapMapRows) : kHeadDim;
     if (!make_map(&tm_snap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, have_snaps ? static_cast<const void*>(snap.S) : dummy,
-                  kHeadDim, 1, have_snaps ? static_cast<uint64_t>(snap.count) * Hh * kHeadDim : kHeadDim, 32, 32,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+                  kHeadDim, 1, snap_rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return KDA_ERR_CUDA;
     const bool og = (fz.flags & KDA_FUSE_OUT_GATE) != 0;
 

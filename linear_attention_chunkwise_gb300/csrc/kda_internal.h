@@ -103,8 +103,10 @@ cudaError_t launch_prefill_fused(const CUtensorMap& tm_q, const CUtensorMap& tm_
 cudaError_t launch_chunk_table(const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t* chunk_off,
                                int32_t* device_status, const int32_t* snap_seq, const int32_t* snap_pos,
                                int32_t num_snaps, cudaStream_t stream);
-// tm_snap: a map over S_snap as [num_snaps x H x 128 rows][128] fp32 (3-D, middle extent 1), boxes of
-// 32 rows x 32 columns, 128B-swizzled; any valid map when there are no snapshots.
+// tm_snap: a map over S_snap as [num_snaps x H x 128 rows][128] fp32 (3-D, middle extent 1; at most
+// kSnapMapRows rows, the rest stored without it), boxes of 32 rows x 32 columns, 128B-swizzled; any
+// valid map when there are no snapshots.
+constexpr int64_t kSnapMapRows = (int64_t{1} << 31) - 64;
 cudaError_t launch_prefill_split(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                  const CUtensorMap& tm_snap, const PrefillArgs& a, int64_t max_chunks, bool out_f32,
                                  cudaStream_t stream);

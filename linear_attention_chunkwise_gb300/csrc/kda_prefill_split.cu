@@ -691,16 +691,21 @@ __global__ void __launch_bounds__(NTS, 3 - NSET)
             while (next_snap <= done) {
                 if (next_snap == done) {
                     float* stage = reinterpret_cast<float*>(set) + warp * 32 * PC;
+                    const int64_t row = (static_cast<int64_t>(si) * H + h) * D + 32 * qw;
                     if (snap_stored && lane == 0) bulk_wait_read();  // a second entry at the same position
                     __syncwarp();
-                    stage_state_rows<PC>(S, stage, lane);
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&tm_snap, stage, j0 + PC * cq, 0, (si * H + h) * D + 32 * qw);
-                        bulk_commit();
+                    if (row + 32 <= kSnapMapRows) {  // the map's coordinates are 32-bit
+                        stage_state_rows<PC>(S, stage, lane);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tm_snap, stage, j0 + PC * cq, 0, static_cast<int32_t>(row));
+                            bulk_commit();
+                        }
+                        snap_stored = true;
+                    } else {
+                        store_state_rows<PC>(p.S_snap + row * D + j0 + PC * cq, S, stage, lane);
                     }
-                    snap_stored = true;
                 }
                 ++si;
                 next_snap = si < se ? p.snap_pos[si] : INT_MAX;
